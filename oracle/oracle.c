@@ -181,6 +181,8 @@ static int mx_exponent(double amax, double qmax) {
 
 /* MXFP4 encoder (32-weight blocks, fp32 input). */
 void orc_encode_mxfp4(const float* w, int64_t nblk, uint8_t* out) {
+  /* blocks are independent; each block's arithmetic is sequential */
+#pragma omp parallel for schedule(static)
   for (int64_t b = 0; b < nblk; ++b) {
     const float* x = w + b * 32;
     uint8_t* blk = out + b * 17;
@@ -244,6 +246,7 @@ static float rne_int(float v) {
  * amax is clamped to at least 1e-8. The stored scale is the bf16 rounding of the winning s. */
 void orc_encode_int4(const float* w, int64_t nblk, uint8_t* out) {
   const float grid[6] = {6.0f / 7.0f, 0.9f, 0.95f, 1.0f, 1.05f, 1.1f};
+#pragma omp parallel for schedule(static)
   for (int64_t b = 0; b < nblk; ++b) {
     const float* x = w + b * 32;
     uint8_t* blk = out + b * 18;
@@ -267,7 +270,9 @@ void orc_encode_int4(const float* w, int64_t nblk, uint8_t* out) {
         float sq = d * d;
         mse = mse + sq;
       }
-      if (mse < best_mse) { best_mse = mse; best_s = s; memcpy(best_q, q, sizeof q); }
+      /* the first candidate is the initial best; a later one replaces it only with a strictly smaller error
+         (so a group whose errors all overflow to inf keeps r = 6/7) */
+      if (gi == 0 || mse < best_mse) { best_mse = mse; best_s = s; memcpy(best_q, q, sizeof q); }
     }
     memset(blk, 0, 16);
     for (int j = 0; j < 32; ++j) {
@@ -318,6 +323,7 @@ void orc_decode_q2k(const uint8_t* blocks, int64_t nblk, float* out) {
  *   q_i = round_half_even((w_i + dmin*m_g) / (d*sc_g)) clamped to [0,3] (0 if d*sc_g == 0)
  * All arithmetic fp32 with RNE. */
 void orc_encode_q2k(const float* w, int64_t nblk, uint8_t* out) {
+#pragma omp parallel for schedule(static)
   for (int64_t b = 0; b < nblk; ++b) {
     const float* x = w + b * 256;
     uint8_t* blk = out + b * 84;
@@ -502,8 +508,13 @@ static void decode_matrix(int fmt, const uint8_t* mat, int64_t rows, int K, doub
   int nb = fmt_bytes(fmt);
   for (int64_t b = 0; b < nblk; ++b) {
     const uint8_t* blk = mat + b * nb;
-    if (fmt == 1) { for (int j = 0; j < 32; ++j) out[b * 32 + j] = mxfp4_weight(blk, j); }
-    else if (fmt == 2) { for (int j = 0; j < 32; ++j) out[b * 32 + j] = int4_weight(blk, j); }
+    if (fmt == 1) {
+      double s = orc_e8m0_scale(blk[0]);
+      for (int j = 0; j < 32; ++j) out[b * 32 + j] = E2M1[mxfp4_code(blk, j)] * s;
+    } else if (fmt == 2) {
+      double s = int4_scale(blk);
+      for (int j = 0; j < 32; ++j) out[b * 32 + j] = int4_code(blk, j) * s;
+    }
     else { orc_decode_q2k(blk, 1, tmp); for (int j = 0; j < 256; ++j) out[b * 256 + j] = (double)tmp[j]; }
   }
   free(tmp);
