@@ -1,0 +1,392 @@
+"""Benchmark: routed-MoE decode on one DeepSeek-V4-Flash-shaped layer (hidden 4096, expert intermediate 2048,
+256 routed experts, top-6, fp16 router), batch 1, 1000 independent seeded tokens, expert weights MXFP4
+(also INT4 g32 and Q2_K with --fmt). One step = for each of the 1000 tokens: router top-6, then the fused
+expert FFN (gate+up, SiLU*up, down, weighted combine), one token at a time, as a CUDA graph.
+
+Prints one JSON line. value = tokens/s of the whole step; roofline = the fused FFN kernel's algorithmic bytes
+(packed bytes of the token's 6 active experts) / its measured average launch time, against the measured HBM copy
+bandwidth. `--impl reference` times the CPU oracle on the host cores instead (a bounded sample of the workload).
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+H, I, E, K_TOP, NTOK = 4096, 2048, 256, 6, 1000
+FMT_IDS = {"mxfp4": 1, "int4g32": 2, "q2k": 3}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=5)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--fmt", default="mxfp4", choices=list(FMT_IDS))
+    p.add_argument("--tokens", type=int, default=NTOK)
+    p.add_argument("--seed", type=int, default=1)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0)
+    return p.parse_args()
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while the timed region runs."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------------ GPU arm
+def run_ours(args):
+    import torch
+    import bit_moe_decode_gb300 as m
+    from moe_inputs import GATE, UP, DOWN, expert_stack_f32, router_f16_bits, x_bf16_bits
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    if m.moe_check_device() != 0:
+        raise RuntimeError("libmoe: device is not sm_103")
+    fmt = FMT_IDS[args.fmt]
+    T = args.tokens
+
+    # ---- weights: seeded fp32 -> packed on the GPU by the library's encoder (replica per rank, same weights)
+    layer = m.Layer(fmt, H, I, E, device=dev)
+    t0 = time.time()
+    batch = 16
+    pool = cf.ThreadPoolExecutor(2)
+
+    def gen(e0):
+        ex = range(e0, min(E, e0 + batch))
+        return [expert_stack_f32(args.seed, 0, ex, which, H, I) for which in (GATE, UP, DOWN)]
+
+    fut = pool.submit(gen, 0)
+    for e0 in range(0, E, batch):
+        g, u, d = fut.result()
+        if e0 + batch < E:
+            fut = pool.submit(gen, e0 + batch)
+        layer.pack(m.MOE_SRC_F32, torch.from_numpy(g).to(dev), torch.from_numpy(u).to(dev),
+                   torch.from_numpy(d).to(dev), e0=e0)
+    torch.cuda.synchronize()
+    setup_s = time.time() - t0
+
+    wr = torch.from_numpy(router_f16_bits(args.seed, 0, E, H).view(np.int16)).to(dev)
+    x_host = x_bf16_bits(args.seed + rank * 7919, range(T), H)   # each rank decodes its own tokens
+    x = torch.from_numpy(x_host.view(np.int16)).to(dev)
+    idx = torch.zeros((T, K_TOP), dtype=torch.int32, device=dev)
+    w = torch.zeros((T, K_TOP), dtype=torch.float32, device=dev)
+    y = torch.zeros((T, H), dtype=torch.float32, device=dev)
+    ws = layer.workspace(1, K_TOP)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step_launch():
+        for t in range(T):
+            m.moe_route_topk(wr, x[t], 1, H, E, K_TOP, None, None, 0, idx[t], w[t], stream=stream)
+            m.moe_expert_ffn_decode(layer, x[t], idx[t], w[t], K_TOP, y[t], None, False, ws, stream=stream)
+
+    def ffn_only_launch():
+        for t in range(T):
+            m.moe_expert_ffn_decode(layer, x[t], idx[t], w[t], K_TOP, y[t], None, False, ws, stream=stream)
+
+    idx2 = torch.zeros_like(idx)
+    w2 = torch.zeros_like(w)
+
+    def route_only_launch():
+        for t in range(T):
+            m.moe_route_topk(wr, x[t], 1, H, E, K_TOP, None, None, 0, idx2[t], w2[t], stream=stream)
+
+    with torch.cuda.stream(stream):
+        step_launch()   # warm the attribute setup outside capture
+    stream.synchronize()
+    if m.moe_get_device_status(ws, stream) != 0:
+        raise RuntimeError("device status after warm-up")
+    use_graph = True
+    try:
+        g_step = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_step, stream=stream):
+            step_launch()
+        g_ffn = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_ffn, stream=stream):
+            ffn_only_launch()
+        g_route = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_route, stream=stream):
+            route_only_launch()
+    except Exception as ex:  # capture unsupported: launch eagerly (host launch cost then counts)
+        print("graph capture failed (%s); timing eager launches" % ex, file=sys.stderr)
+        use_graph = False
+
+    def run_step():
+        with torch.cuda.stream(stream):
+            if use_graph:
+                g_step.replay()
+            else:
+                step_launch()
+
+    def run_ffn():
+        with torch.cuda.stream(stream):
+            if use_graph:
+                g_ffn.replay()
+            else:
+                ffn_only_launch()
+
+    for _ in range(args.warmup):
+        run_step()
+    stream.synchronize()
+
+    # ---- timed region: K steps, barrier + sync on both sides, events on the launching stream
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        run_step()
+    ev1.record(stream)
+    ev1.synchronize()
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    clk = clocks.stop()
+    if dist:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+        dist.barrier()
+    status = m.moe_get_device_status(ws, stream)
+    if status != 0:
+        raise RuntimeError("device status %d after timed region" % status)
+
+    # ---- the dominant kernel alone (routing fixed): average launch duration
+    for _ in range(2):
+        run_ffn()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    reps = max(2, args.steps)
+    for _ in range(reps):
+        run_ffn()
+    e1.record(stream)
+    e1.synchronize()
+    ffn_us = e0.elapsed_time(e1) * 1e3 / (reps * T)
+    route_us = None
+    if use_graph:
+        with torch.cuda.stream(stream):
+            g_route.replay()
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(reps):
+                g_route.replay()
+        e1.record(stream)
+        e1.synchronize()
+        route_us = e0.elapsed_time(e1) * 1e3 / (reps * T)
+        assert torch.equal(idx2, idx), "router results differ between runs"
+    # routing alone
+    idx_np = idx.cpu().numpy()
+    uniq = np.mean([len(set(r)) for r in idx_np])
+    per_expert = m.moe_packed_bytes(fmt, 0, 0, 1, H, I) + m.moe_packed_bytes(fmt, 0, 1, 1, H, I)
+    alg_bytes = float(np.mean([len(set(r)) for r in idx_np])) * per_expert
+
+    # ---- end to end through the public API with host buffers (pinned), copies inside the timed region
+    xh = torch.from_numpy(x_host.view(np.int16)).pin_memory()
+    yh = torch.empty((T, H), dtype=torch.float32).pin_memory()
+    torch.cuda.synchronize()
+    e2e_steps = max(1, min(args.steps, 3))
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(e2e_steps):
+        with torch.cuda.stream(stream):
+            x.copy_(xh, non_blocking=True)
+        run_step()
+        with torch.cuda.stream(stream):
+            yh.copy_(y, non_blocking=True)
+    s1.record(stream)
+    s1.synchronize()
+    e2e_ms = s0.elapsed_time(s1) / e2e_steps
+    if dist:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    out = None
+    if rank == 0:
+        peaks = measured_peaks()
+        peak = float(peaks["hbm_gbs"]) if peaks else 6800.0
+        achieved = alg_bytes / (ffn_us * 1e-6) / 1e9
+        ms_step = ms / args.steps
+        value = world * T / (ms_step * 1e-3)
+        out = {
+            "metric": "routed-MoE decode tok/s and HBM GB/s (% of 8 TB/s), MXFP4/Q2_K/INT4 experts",
+            "value": round(value, 1), "unit": "tok/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": {1: "mxfp4", 2: "int4g32", 3: "q2k"}[fmt] + " weights, bf16 x, fp16/fp32 mma",
+            "data": "synthetic (seeded N(0,0.02) weights quantised on the GPU, N(0,1) bf16 tokens)",
+            "config": {"workload": "DS4-Flash routed-MoE layer decode, batch 1, %d independent tokens" % T,
+                       "H": H, "I": I, "experts": E, "top_k": K_TOP, "format": args.fmt,
+                       "l2": "inputs larger than L2 (3.4 GB of experts, random routing)",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "gpu_launches": 2 * T * args.steps,
+            "hbm_gbs_step": round(alg_bytes * T / (ms_step * 1e-3) / 1e9, 1),
+            "pct_of_8tbs_step": round(100 * alg_bytes * T / (ms_step * 1e-3) / 8e12, 2),
+            "ffn_kernel_us": round(ffn_us, 3),
+            "route_kernel_us": round(route_us, 3) if route_us else None,
+            "ffn_tok_s": round(1e6 / ffn_us, 1),
+            "ffn_pct_of_8tbs": round(100 * alg_bytes / (ffn_us * 1e-6) / 8e12, 2),
+            "mean_unique_experts": float(uniq),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": None,
+                         "kernel": "ffn_kernel<%s>" % args.fmt, "bytes_per_launch": alg_bytes,
+                         "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if peaks else "fallback"},
+            "e2e": {"value": round(world * T / (e2e_ms * 1e-3), 1), "unit": "tok/s",
+                    "h2d_bytes_per_step": int(T * H * 2), "d2h_bytes_per_step": int(T * H * 4)},
+            "clocks": clk,
+            "setup_s": round(setup_s, 1),
+            "cuda_graph": use_graph,
+        }
+    if dist:
+        dist.destroy_process_group()
+    return out
+
+
+# ------------------------------------------------------------------------------------------------ CPU oracle
+class CpuOracle:
+    """The oracle as it stands, on the host cores: one token per thread, tokens of the same layer and routing
+    rule. The sampled tokens' expert weights are encoded once, before any timing."""
+
+    def __init__(self, fmt_name, seed):
+        import oracle
+        from moe_inputs import expert_matrix_f32, router_f16_bits, x_bf16_bits
+        self.oracle = oracle
+        self.fmt = FMT_IDS[fmt_name]
+        self.cores = os.cpu_count() or 1
+        self.n = self.cores
+        wr = router_f16_bits(seed, 0, E, H)
+        self.x = x_bf16_bits(seed, range(self.n), H)
+        self.idx, self.w, _, _ = oracle.route_topk(wr, self.x, K_TOP)
+        self.cache = {}
+        for e in np.unique(self.idx):
+            for which in range(3):
+                self.cache[(int(e), which)] = oracle.encode(self.fmt, expert_matrix_f32(seed, 0, int(e), which, H, I))
+
+    def _one(self, t):
+        c = self.cache
+        self.oracle.moe_tokens(self.fmt, H, I, lambda e: c[(int(e), 0)], lambda e: c[(int(e), 1)],
+                               lambda e: c[(int(e), 2)], self.idx[t:t + 1], self.w[t:t + 1], self.x[t:t + 1])
+
+    def run(self, seconds):
+        done = 0
+        t0 = time.time()
+        with cf.ThreadPoolExecutor(self.cores) as ex:
+            while time.time() - t0 < seconds or done == 0:
+                list(ex.map(self._one, range(self.n)))
+                done += self.n
+        el = time.time() - t0
+        return {"value": round(done / el, 3), "unit": "tok/s", "cores": self.cores, "kind": "oracle",
+                "sample": "%d tokens (%d per thread) of the same layer and routing rule in %.1f s wall; fp64 C oracle, "
+                          "one token per thread" % (done, done // self.cores, el)}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        if rank != 0:
+            return
+        t0 = time.time()
+        per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+        co = CpuOracle(args.fmt, args.seed)
+        for _ in range(args.warmup):
+            co.run(per_step / 4)
+        vals = [co.run(per_step) for _ in range(args.steps)]
+        v = float(np.median([r["value"] for r in vals]))
+        cb = dict(vals[0])
+        cb["value"] = v
+        out = {"impl": "reference", "metric": "routed-MoE decode tok/s and HBM GB/s (% of 8 TB/s), MXFP4/Q2_K/INT4 experts",
+               "value": v, "unit": "tok/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+               "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+               "dtype": "f64", "data": "synthetic",
+               "config": {"workload": "DS4-Flash routed-MoE layer decode, batch 1, sampled tokens", "H": H, "I": I,
+                          "experts": E, "top_k": K_TOP, "format": args.fmt},
+               "cpu_baseline": cb, "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+               "wall_s": round(time.time() - t0, 1)}
+        print(json.dumps(out))
+        return
+    out = run_ours(args)
+    if out is not None:
+        if not args.no_cpu_baseline and int(os.environ.get("WORLD_SIZE", "1")) == 1:
+            out["cpu_baseline"] = CpuOracle(args.fmt, args.seed).run(args.cpu_seconds)
+        print(json.dumps(out))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,632 @@
+// ffn.cu -- fused routed-expert FFN for decode (T = 1) and speculative verify (T <= 8) in one persistent kernel.
+//
+// What it computes: y_t = sum_r w[t,r] * Down_e( SiLU(Gate_e x_t) * (Up_e x_t) ), e = idx[t,r]
+//   ("quantization" glossary, ds4-learning.pages.dev, "Q4_K routed experts": fused gate+up mat-vec, then the down
+//   projection accumulated into the output; "Mixed-precision compression of DeepSeek-V4-Flash" (lumirain.cn),
+//   "What compression does not solve": decode is bound by one read of the active expert weights per token;
+//   "Width drift" / "Why this is not a host-side patch": a verify of width 1+K must read each weight once while
+//   reproducing width-1 arithmetic bit for bit).
+//
+// Design (one CTA per SM, cooperative launch so all CTAs are co-resident):
+//   * The union of the experts of the T tokens is formed on the device (sorted, deduplicated); each expert in it
+//     is read exactly once per call, whatever T is.
+//   * Work units are 16-row tiles: phase G (gate/up tiles of each union expert) then phase D (down tiles). Each
+//     CTA owns a contiguous range of G units and of D units.
+//   * A producer warp streams tiles from HBM into an 8-13 stage shared-memory ring with 1-D bulk copies
+//     (cp.async.bulk, mbarrier completion, L2 evict-first); 8 consumer warps split K of every tile, run the
+//     tensor-core mat-vec (mma.m16n8k16, weights as A decoded in registers, the T tokens as the 8 B columns) and
+//     reduce across warps in a fixed order through shared memory.
+//   * Numerics: weights are decoded exactly to fp16; x is rescaled per token by 2^sigma into fp16; block scales
+//     multiply fp32 partial sums; h = SiLU(g)*u in fp32 is rescaled per (expert, token) into fp16 for the down
+//     projection; the combine sums the ranks in rank order with fp32 FMAs.
+//   * Width-1 exactness: a token's column goes through the same instructions whatever T is (column-independent
+//     MMA, per-token rescale, fixed warp and rank orders), so verify row t equals decode of token t bitwise.
+//   * Handoff G -> D: per-expert counters (acquire/release); D units wait (bounded) for all G tiles of their
+//     expert. The combine for a 16-row output tile is done by the CTA that finishes its last expert (counter),
+//     so no floating-point atomics are used anywhere. The last CTA to finish clears the counters.
+#include "common.cuh"
+#include "layout.cuh"
+#include "api_internal.h"
+
+namespace moe {
+
+constexpr int kCW = 8;                 // consumer warps
+constexpr int kThreads = (kCW + 1) * 32;
+constexpr int kMaxT = 8;
+constexpr int kMaxK = 8;
+constexpr int kMaxU = kMaxT * kMaxK;   // 64
+constexpr int kMaxRowTiles = 4096 / 16;
+
+// workspace: [header 256][cnt_g 64 u32][amax_h 64*8 u32] -> 4096 bytes, then h [U, 8, I] and d [U, H, 8] fp32
+constexpr size_t kWsCounters = 4096;
+constexpr size_t kOffCntG = 256, kOffAmax = kOffCntG + kMaxU * 4;
+static_assert(kOffAmax + kMaxU * kMaxT * 4 <= kWsCounters, "counter area");
+
+struct FfnArgs {
+  const uint8_t* gate_up;
+  const uint8_t* down;
+  const uint16_t* x;   // [T, H] bf16
+  const int32_t* idx;  // [T, k]
+  const float* w;      // [T, k]
+  float* y;            // [T, H]
+  uint16_t* y_bf16;    // [T, H] or null
+  int accumulate;
+  int H, I, E, T, k;
+  WsHeader* hdr;
+  uint32_t* cnt_g;     // [kMaxU]
+  uint32_t* amax_h;    // [kMaxU * 8]
+  float* hbuf;         // [U, 8, I]
+  float* dbuf;         // [U, H, 8]
+  long long wait_ns;
+};
+
+template <int FMT> struct Cfg {
+  using F = Fmt<FMT>;
+  static constexpr int SB = F::CPS * F::CB;                                // stage bytes (2048 columns)
+  static constexpr int NS = FMT == MOE_FMT_Q2K ? 13 : 8;                   // ring stages
+  static constexpr int NCH = 4096 / F::CK / kCW;                           // max chunks per warp per tile
+  static constexpr int NPS = F::CPS / kCW;                                 // chunks per warp per stage
+  static constexpr int SXF = FMT == MOE_FMT_Q2K ? kCW * NCH * F::STEPS * kMaxT : 0;  // group sums of x (floats)
+  static constexpr int RED = 2 * kCW * 32 * 4;                             // double-buffered reduction (floats)
+  static constexpr size_t SMEM = (size_t)NS * SB + (size_t)(RED + SXF) * 4;
+};
+
+__device__ __forceinline__ float e8m0_to_f32(uint32_t e) {
+  return e == 255u ? __uint_as_float(0x7fc00000u) : __uint_as_float(e << 23);
+}
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+__device__ __forceinline__ float h16_to_f32(uint32_t b) { return __half2float(__ushort_as_half((unsigned short)b)); }
+
+// Process one chunk: acc += (A . B) with the format's block scaling. bx: the warp's B fragments for this chunk.
+template <int FMT>
+__device__ __forceinline__ void chunk_mma(const uint8_t* cp, int lane, const uint32_t (&bx)[Fmt<FMT>::STEPS][2],
+                                          const float* sx /* Q2_K group sums [STEPS][8] or null */, float (&acc)[4]) {
+  const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+  if constexpr (FMT == MOE_FMT_MXFP4) {
+    const uint4 cw = *reinterpret_cast<const uint4*>(cp + lane * 16);
+    const uint32_t sw = *reinterpret_cast<const uint32_t*>(cp + 512 + (lane >> 2) * 4);
+    const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+      float c[4];
+      const uint32_t w0 = words[2 * blk], w1 = words[2 * blk + 1];
+      mma_f16(c, e2m1x2_to_f16x2(w0, 0), e2m1x2_to_f16x2(w0, 1), e2m1x2_to_f16x2(w0, 2), e2m1x2_to_f16x2(w0, 3),
+              bx[2 * blk][0], bx[2 * blk][1], zero);
+      mma_f16(c, e2m1x2_to_f16x2(w1, 0), e2m1x2_to_f16x2(w1, 1), e2m1x2_to_f16x2(w1, 2), e2m1x2_to_f16x2(w1, 3),
+              bx[2 * blk + 1][0], bx[2 * blk + 1][1], c);
+      const float sr = e8m0_to_f32((sw >> (16 * blk)) & 255u), sr8 = e8m0_to_f32((sw >> (16 * blk + 8)) & 255u);
+      acc[0] = fmaf(c[0], sr, acc[0]);
+      acc[1] = fmaf(c[1], sr, acc[1]);
+      acc[2] = fmaf(c[2], sr8, acc[2]);
+      acc[3] = fmaf(c[3], sr8, acc[3]);
+    }
+  } else if constexpr (FMT == MOE_FMT_INT4G32) {
+    const uint4 cw = *reinterpret_cast<const uint4*>(cp + lane * 16);
+    const uint2 sc = *reinterpret_cast<const uint2*>(cp + 512 + (lane >> 2) * 8);
+    const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+    // nibble n (two's complement) -> fp16 1024 + (n^8) [low nibble slot] or 1024 + 16 (n^8) [high nibble slot],
+    // then an exact fma maps it to n.
+    const uint32_t one = 0x3C003C00u, m1032 = 0xE408E408u, sixteenth = 0x2C002C00u, m72 = 0xD480D480u;
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+      float c[4];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t W = words[2 * blk + h], W8 = W >> 8;
+        const uint32_t a0 = hfma2(lop3_and_xor(W, 0x000F000Fu, 0x64086408u), one, m1032);
+        const uint32_t a1 = hfma2(lop3_and_xor(W, 0x00F000F0u, 0x64806480u), sixteenth, m72);
+        const uint32_t a2 = hfma2(lop3_and_xor(W8, 0x000F000Fu, 0x64086408u), one, m1032);
+        const uint32_t a3 = hfma2(lop3_and_xor(W8, 0x00F000F0u, 0x64806480u), sixteenth, m72);
+        if (h == 0) mma_f16(c, a0, a1, a2, a3, bx[2 * blk][0], bx[2 * blk][1], zero);
+        else mma_f16(c, a0, a1, a2, a3, bx[2 * blk + 1][0], bx[2 * blk + 1][1], c);
+      }
+      const uint32_t sv = blk == 0 ? sc.x : sc.y;
+      const float sr = bf16_bits_to_f32(sv & 0xFFFFu), sr8 = bf16_bits_to_f32(sv >> 16);
+      acc[0] = fmaf(c[0], sr, acc[0]);
+      acc[1] = fmaf(c[1], sr, acc[1]);
+      acc[2] = fmaf(c[2], sr8, acc[2]);
+      acc[3] = fmaf(c[3], sr8, acc[3]);
+    }
+  } else {  // Q2_K: one chunk = one 256-weight super-block per row, 16 groups of 16 = 16 mma steps
+    const uint4 cw0 = *reinterpret_cast<const uint4*>(cp + lane * 32);
+    const uint4 cw1 = *reinterpret_cast<const uint4*>(cp + lane * 32 + 16);
+    const uint32_t words[8] = {cw0.x, cw0.y, cw0.z, cw0.w, cw1.x, cw1.y, cw1.z, cw1.w};
+    const int r = lane >> 2;
+    const uint4 sr4 = *reinterpret_cast<const uint4*>(cp + 1024 + r * 32);
+    const uint4 sr84 = *reinterpret_cast<const uint4*>(cp + 1024 + r * 32 + 16);
+    const uint2 dd = *reinterpret_cast<const uint2*>(cp + 1280 + r * 8);
+    const float d_r = h16_to_f32(dd.x & 0xFFFFu), dm_r = h16_to_f32(dd.x >> 16);
+    const float d_r8 = h16_to_f32(dd.y & 0xFFFFu), dm_r8 = h16_to_f32(dd.y >> 16);
+    const uint32_t s_r[4] = {sr4.x, sr4.y, sr4.z, sr4.w}, s_r8[4] = {sr84.x, sr84.y, sr84.z, sr84.w};
+    // 2-bit code at bit 2b of a half's low byte -> fp16 1024 + 4^b q -> exact fma -> q
+    const uint32_t mul[4] = {0x3C003C00u, 0x34003400u, 0x2C002C00u, 0x24002400u};
+    const uint32_t add[4] = {0xE400E400u, 0xDC00DC00u, 0xD400D400u, 0xCC00CC00u};
+    const int q = lane & 3;
+#pragma unroll
+    for (int s = 0; s < 16; ++s) {
+      const uint32_t W = (s & 1) ? (words[s >> 1] >> 8) : words[s >> 1];
+      uint32_t a[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) a[b] = hfma2(lop3_and_xor(W, 0x00030003u << (2 * b), 0x64006400u), mul[b], add[b]);
+      float c[4];
+      mma_f16(c, a[0], a[1], a[2], a[3], bx[s][0], bx[s][1], zero);
+      const uint32_t br = (s_r[s >> 2] >> (8 * (s & 3))) & 255u, br8 = (s_r8[s >> 2] >> (8 * (s & 3))) & 255u;
+      const float A_r = d_r * (float)(br & 15u), B_r = dm_r * (float)(br >> 4);
+      const float A_r8 = d_r8 * (float)(br8 & 15u), B_r8 = dm_r8 * (float)(br8 >> 4);
+      const float sx0 = sx[s * kMaxT + 2 * q], sx1 = sx[s * kMaxT + 2 * q + 1];
+      acc[0] = fmaf(-B_r, sx0, fmaf(c[0], A_r, acc[0]));
+      acc[1] = fmaf(-B_r, sx1, fmaf(c[1], A_r, acc[1]));
+      acc[2] = fmaf(-B_r8, sx0, fmaf(c[2], A_r8, acc[2]));
+      acc[3] = fmaf(-B_r8, sx1, fmaf(c[3], A_r8, acc[3]));
+    }
+  }
+}
+
+// Consumer side of one tile (G or D): waits the tile's stages, runs the warp's chunks, releases the stages.
+// Returns false on a timeout (the caller marks the CTA aborted).
+template <int FMT>
+__device__ __forceinline__ bool consume_tile(uint8_t* ring, uint64_t* full, uint64_t* empty, uint32_t& it, int nchunks,
+                                             int warp, int lane, const uint32_t (&b)[Cfg<FMT>::NCH][Fmt<FMT>::STEPS][2],
+                                             const float* sxw, float (&acc)[4], long long wait_ns, volatile int* abort) {
+  using C = Cfg<FMT>;
+  using F = Fmt<FMT>;
+  const int nst = (nchunks + F::CPS - 1) / F::CPS;
+  bool ok = true;
+  int slot = 0;
+#pragma unroll
+  for (int n = 0; n < C::NCH; ++n) {
+    const int s = n / C::NPS;
+    if (n % C::NPS == 0 && s < nst) {
+      slot = (int)((it + s) % C::NS);
+      const uint32_t par = ((it + s) / C::NS) & 1;
+      if (*abort || !mbar_wait(&full[slot], par, wait_ns)) ok = false;
+    }
+    const int c = warp + kCW * n;
+    if (ok && c < nchunks) {
+      const uint8_t* cp = ring + (size_t)slot * C::SB + (size_t)(c - s * F::CPS) * F::CB;
+      chunk_mma<FMT>(cp, lane, b[n], sxw ? sxw + n * F::STEPS * kMaxT : nullptr, acc);
+    }
+    if (((n + 1) % C::NPS == 0) && s < nst) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+  }
+  it += nst;
+  return ok;
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, 1) ffn_kernel(const FfnArgs a) {
+  using C = Cfg<FMT>;
+  using F = Fmt<FMT>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ring = smem;
+  float* red = reinterpret_cast<float*>(smem + (size_t)C::NS * C::SB);
+  float* sx = red + C::RED;
+  __shared__ __align__(8) uint64_t full[C::NS], empty[C::NS];
+  __shared__ int s_val[kMaxU], s_first[kMaxU], s_slot[kMaxU], s_union[kMaxU];
+  __shared__ float s_wsum[kMaxT][kMaxU];        // per token: summed router weight of each union expert
+  __shared__ int s_routed[kMaxT][kMaxU];        // per token: does it route to this union expert
+  __shared__ int s_nu[kMaxT];                   // per token: its union experts in ascending order ...
+  __shared__ int s_ulist[kMaxT][kMaxK];
+  __shared__ float s_uw[kMaxT][kMaxK];          // ... and their summed weights
+  __shared__ int s_U;
+  __shared__ volatile int s_abort;
+  __shared__ int s_sig[kMaxT];
+  __shared__ float s_colmax[kCW][kMaxT];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int T = a.T, k = a.k, H = a.H, I = a.I;
+  const int n_ent = T * k;
+
+  // ---------------- prologue: barriers, union of the tokens' experts (sorted, deduplicated), weight sums
+  if (tid == 0) {
+    for (int s = 0; s < C::NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], kCW); }
+    fence_mbar_init();
+    s_abort = 0;
+  }
+  for (int i = tid; i < kMaxT * kMaxU; i += blockDim.x) {
+    (&s_wsum[0][0])[i] = 0.f;
+    (&s_routed[0][0])[i] = 0;
+  }
+  if (tid < n_ent) s_val[tid] = a.idx[tid];
+  __syncthreads();
+  if (tid < n_ent) {
+    const int v = s_val[tid];
+    int first = 1;
+    for (int j = 0; j < tid; ++j) first &= (s_val[j] != v);
+    s_first[tid] = first;
+    if (v < 0 || v >= a.E) { s_abort = 1; if (blockIdx.x == 0) record_error(&a.hdr->status, MOE_ERR_INVALID_ARG); }
+  }
+  __syncthreads();
+  if (tid < n_ent) {
+    const int v = s_val[tid];
+    int rank = 0;
+    for (int j = 0; j < n_ent; ++j) rank += (s_first[j] && s_val[j] < v) ? 1 : 0;
+    s_slot[tid] = rank;
+    if (s_first[tid]) s_union[rank] = v;
+  }
+  if (tid == 0) {
+    int u = 0;
+    for (int j = 0; j < n_ent; ++j) u += s_first[j];
+    s_U = u;
+  }
+  __syncthreads();
+  if (tid < T) {  // rank order, so a token's sums do not depend on the other tokens
+    for (int r = 0; r < k; ++r) {
+      const int u = s_slot[tid * k + r];
+      s_wsum[tid][u] += __ldg(&a.w[tid * k + r]);
+      s_routed[tid][u] = 1;
+    }
+    int n = 0;
+    for (int u = 0; u < s_U; ++u)
+      if (s_routed[tid][u]) { s_ulist[tid][n] = u; s_uw[tid][n] = s_wsum[tid][u]; ++n; }
+    s_nu[tid] = n;
+  }
+  __syncthreads();
+  const int U = s_U;
+  const int G = gridDim.x, bid = blockIdx.x;
+  const int gt = I / 8, dt = H / 16;  // tiles per expert
+  const int64_t NG = (int64_t)U * gt, ND = (int64_t)U * dt;
+  const int64_t g0 = NG * bid / G, g1 = NG * (bid + 1) / G;
+  const int64_t d0 = ND * bid / G, d1 = ND * (bid + 1) / G;
+  const int m0 = (int)((int64_t)dt * bid / G), m1 = (int)((int64_t)dt * (bid + 1) / G);
+  const int ncg = H / F::CK, ncd = I / F::CK;                       // chunks per G / D tile
+  const int64_t tbg = tile_bytes(FMT, H), tbd = tile_bytes(FMT, I);
+  const int64_t sgu = gate_up_stride(FMT, H, I), sdn = down_stride(FMT, H, I);
+
+  if (warp == kCW) {
+    // ================= producer: G tiles of the CTA's range, then for each union expert its D tiles [m0, m1)
+    if (lane == 0 && !s_abort) {
+      const uint64_t pol = policy_evict_first();
+      uint32_t it = 0;
+      bool ok = true;
+      auto issue_tile = [&](const uint8_t* base, int nchunks) {
+        for (int c0 = 0; c0 < nchunks && ok; c0 += F::CPS) {
+          const int nc = min(F::CPS, nchunks - c0);
+          const int slot = (int)(it % C::NS);
+          if (it >= (uint32_t)C::NS) {
+            if (s_abort || !mbar_wait(&empty[slot], ((it / C::NS) - 1) & 1, a.wait_ns)) { ok = false; break; }
+          }
+          mbar_arrive_expect_tx(&full[slot], (uint32_t)(nc * F::CB));
+          bulk_g2s(ring + (size_t)slot * C::SB, base + (size_t)c0 * F::CB, (uint32_t)(nc * F::CB), &full[slot], pol);
+          ++it;
+        }
+      };
+      for (int64_t gu = g0; gu < g1 && ok; ++gu) {
+        const int u = (int)(gu / gt), j = (int)(gu % gt);
+        issue_tile(a.gate_up + (size_t)s_union[u] * sgu + (size_t)j * tbg, ncg);
+      }
+      for (int64_t du = d0; du < d1 && ok; ++du) {
+        const int u = (int)(du / dt), m = (int)(du % dt);
+        issue_tile(a.down + (size_t)s_union[u] * sdn + (size_t)m * tbd, ncd);
+      }
+      if (!ok) {
+        record_error(&a.hdr->status, MOE_ERR_DEVICE_TIMEOUT);
+        s_abort = 1;
+        // let the copies already in flight land before the CTA can exit
+        const uint32_t lo = it > (uint32_t)C::NS ? it - C::NS : 0;
+        for (uint32_t i = lo; i < it; ++i) mbar_wait(&full[i % C::NS], (i / C::NS) & 1, a.wait_ns);
+      }
+    }
+  } else {
+    // ================= consumers
+    uint32_t it = 0;
+    const int col = lane >> 2, q = lane & 3;
+    float* sxw = (FMT == MOE_FMT_Q2K) ? sx + warp * (C::NCH * F::STEPS * kMaxT) : nullptr;
+    int bufsel = 0;
+
+    // ---- phase G: B fragments = x of the T tokens, rescaled per token into fp16
+    {
+      uint32_t bx[C::NCH][F::STEPS][2];
+      float mx = 0.f;
+#pragma unroll
+      for (int n = 0; n < C::NCH; ++n) {
+        const int c = warp + kCW * n;
+#pragma unroll
+        for (int j = 0; j < F::STEPS; ++j) {
+          uint32_t v0 = 0, v1 = 0;
+          if (c < ncg && col < T) {
+            const int k0 = c * F::CK + 16 * j + 2 * q;
+            const uint16_t* xr = a.x + (size_t)col * H;
+            v0 = __ldg(reinterpret_cast<const uint32_t*>(xr + k0));
+            v1 = __ldg(reinterpret_cast<const uint32_t*>(xr + k0 + 8));
+          }
+          bx[n][j][0] = v0;
+          bx[n][j][1] = v1;
+          mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf16_bits_to_f32(v0 & 0xFFFFu)), fabsf(bf16_bits_to_f32(v0 >> 16))),
+                               fmaxf(fabsf(bf16_bits_to_f32(v1 & 0xFFFFu)), fabsf(bf16_bits_to_f32(v1 >> 16)))));
+        }
+      }
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      if (q == 0) s_colmax[warp][col] = mx;
+      named_bar(1, kCW * 32);
+      float cm = 0.f;
+#pragma unroll
+      for (int w = 0; w < kCW; ++w) cm = fmaxf(cm, s_colmax[w][col]);
+      const int sig = rescale_exponent(cm);
+      if (warp == 0 && q == 0) s_sig[col] = sig;
+      const float sc = exp2i(sig);
+#pragma unroll
+      for (int n = 0; n < C::NCH; ++n)
+#pragma unroll
+        for (int j = 0; j < F::STEPS; ++j)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t v = bx[n][j][h];
+            const __half2 hv = __floats2half2_rn(bf16_bits_to_f32(v & 0xFFFFu) * sc, bf16_bits_to_f32(v >> 16) * sc);
+            bx[n][j][h] = *reinterpret_cast<const uint32_t*>(&hv);
+          }
+      if constexpr (FMT == MOE_FMT_Q2K) {
+        // per-group sums of the rescaled x (the min term of Q2_K), one column per lane quad
+#pragma unroll
+        for (int n = 0; n < C::NCH; ++n)
+#pragma unroll
+          for (int j = 0; j < F::STEPS; ++j) {
+            const __half2 h0 = *reinterpret_cast<const __half2*>(&bx[n][j][0]);
+            const __half2 h1 = *reinterpret_cast<const __half2*>(&bx[n][j][1]);
+            float s = (__low2float(h0) + __high2float(h0)) + (__low2float(h1) + __high2float(h1));
+            s += __shfl_xor_sync(0xffffffffu, s, 1);
+            s += __shfl_xor_sync(0xffffffffu, s, 2);
+            if (q == 0) sxw[(n * F::STEPS + j) * kMaxT + col] = s;
+          }
+        __syncwarp();
+      }
+      named_bar(1, kCW * 32);
+
+      for (int64_t gu = g0; gu < g1; ++gu) {
+        const int u = (int)(gu / gt), jt = (int)(gu % gt);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        if (!consume_tile<FMT>(ring, full, empty, it, ncg, warp, lane, bx, sxw, acc, a.wait_ns, &s_abort)) {
+          record_error(&a.hdr->status, MOE_ERR_DEVICE_TIMEOUT);
+          s_abort = 1;
+        }
+        float* rb = red + bufsel * (kCW * 32 * 4);
+        *reinterpret_cast<float4*>(rb + (warp * 32 + lane) * 4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        named_bar(1, kCW * 32);
+        if (tid < 64) {
+          // thread -> (fragment lane fl, column slot cc): g from c[cc], u from c[cc+2]; warps summed in order
+          const int fl = tid >> 1, cc = tid & 1;
+          float gs = 0.f, us = 0.f;
+#pragma unroll
+          for (int w = 0; w < kCW; ++w) {
+            gs += rb[(w * 32 + fl) * 4 + cc];
+            us += rb[(w * 32 + fl) * 4 + cc + 2];
+          }
+          const int r = fl >> 2, tc = 2 * (fl & 3) + cc;
+          if (tc < T) {
+            const float inv = exp2i_neg(s_sig[tc]);
+            const float g = gs * inv, uu = us * inv;
+            const float h = g / (1.0f + expf(-g)) * uu;
+            a.hbuf[((size_t)u * kMaxT + tc) * I + (size_t)jt * 8 + r] = h;
+            atomicMax(&a.amax_h[u * kMaxT + tc], __float_as_uint(fabsf(h)));
+          }
+        }
+        bufsel ^= 1;
+      }
+      // publish this CTA's G tiles: one release per expert it touched
+      named_bar(1, kCW * 32);
+      if (tid == 0 && g1 > g0) {
+        __threadfence();
+        int64_t gu = g0;
+        while (gu < g1) {
+          const int u = (int)(gu / gt);
+          const int64_t end = min(g1, (int64_t)(u + 1) * gt);
+          atomicAdd(&a.cnt_g[u], (uint32_t)(end - gu));
+          gu = end;
+        }
+      }
+    }
+
+    // ---- phase D: the CTA's range of down tiles (expert-major, so it loads the h of one or two experts);
+    //      B fragments = the expert's h rescaled per token into fp16; partial outputs go to d [U, H, 8]
+    {
+      uint32_t bh[C::NCH][F::STEPS][2];
+      int loaded = -1;
+      for (int64_t du = d0; du < d1; ++du) {
+        const int u = (int)(du / dt), m = (int)(du % dt);
+        if (u != loaded) {
+          if (lane == 0 && !s_abort) {
+            if (!wait_counter(&a.cnt_g[u], (uint32_t)gt, a.wait_ns)) {
+              record_error(&a.hdr->status, MOE_ERR_DEVICE_TIMEOUT);
+              s_abort = 1;
+            }
+          }
+          __syncwarp();
+          const float am = col < T ? __uint_as_float(__ldcg(&a.amax_h[u * kMaxT + col])) : 0.f;
+          const float sc = exp2i(rescale_exponent(am));
+#pragma unroll
+          for (int n = 0; n < C::NCH; ++n) {
+            const int c = warp + kCW * n;
+#pragma unroll
+            for (int j = 0; j < F::STEPS; ++j) {
+              uint32_t v[2] = {0u, 0u};
+              if (c < ncd && col < T) {
+                const float* hr = a.hbuf + ((size_t)u * kMaxT + col) * I + c * F::CK + 16 * j + 2 * q;
+                const float2 p0 = __ldcg(reinterpret_cast<const float2*>(hr));
+                const float2 p1 = __ldcg(reinterpret_cast<const float2*>(hr + 8));
+                const __half2 h0 = __floats2half2_rn(p0.x * sc, p0.y * sc);
+                const __half2 h1 = __floats2half2_rn(p1.x * sc, p1.y * sc);
+                v[0] = *reinterpret_cast<const uint32_t*>(&h0);
+                v[1] = *reinterpret_cast<const uint32_t*>(&h1);
+              }
+              bh[n][j][0] = v[0];
+              bh[n][j][1] = v[1];
+            }
+          }
+          if constexpr (FMT == MOE_FMT_Q2K) {
+#pragma unroll
+            for (int n = 0; n < C::NCH; ++n)
+#pragma unroll
+              for (int j = 0; j < F::STEPS; ++j) {
+                const __half2 h0 = *reinterpret_cast<const __half2*>(&bh[n][j][0]);
+                const __half2 h1 = *reinterpret_cast<const __half2*>(&bh[n][j][1]);
+                float s = (__low2float(h0) + __high2float(h0)) + (__low2float(h1) + __high2float(h1));
+                s += __shfl_xor_sync(0xffffffffu, s, 1);
+                s += __shfl_xor_sync(0xffffffffu, s, 2);
+                if (q == 0) sxw[(n * F::STEPS + j) * kMaxT + col] = s;
+              }
+            __syncwarp();
+          }
+          loaded = u;
+        }
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        if (!consume_tile<FMT>(ring, full, empty, it, ncd, warp, lane, bh, sxw, acc, a.wait_ns, &s_abort)) {
+          record_error(&a.hdr->status, MOE_ERR_DEVICE_TIMEOUT);
+          s_abort = 1;
+        }
+        float* rb = red + bufsel * (kCW * 32 * 4);
+        *reinterpret_cast<float4*>(rb + (warp * 32 + lane) * 4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        named_bar(1, kCW * 32);
+        if (tid < 128) {
+          const int fl = tid >> 2, cc = tid & 3;
+          const int row = (fl >> 2) + 8 * (cc >> 1), tc = 2 * (fl & 3) + (cc & 1);
+          if (tc < T && s_routed[tc][u]) {
+            float ds = 0.f;
+#pragma unroll
+            for (int w = 0; w < kCW; ++w) ds += rb[(w * 32 + fl) * 4 + cc];
+            const float am2 = __uint_as_float(__ldcg(&a.amax_h[u * kMaxT + tc]));
+            a.dbuf[((size_t)u * H + (size_t)m * 16 + row) * kMaxT + tc] = ds * exp2i_neg(rescale_exponent(am2));
+          }
+        }
+        bufsel ^= 1;
+      }
+    }
+
+    // ---- grid-wide barrier, then each CTA combines its output rows: y_t = sum over the token's own experts, in
+    //      ascending expert id, of w * d (fp32 fma), so the result does not depend on the other tokens
+    named_bar(1, kCW * 32);
+    if (tid == 0) {
+      __threadfence();
+      atomicAdd(&a.hdr->gbar, 1u);
+      if (!s_abort && !wait_counter(&a.hdr->gbar, (uint32_t)G, a.wait_ns)) {
+        record_error(&a.hdr->status, MOE_ERR_DEVICE_TIMEOUT);
+        s_abort = 1;
+      }
+    }
+    named_bar(1, kCW * 32);
+    for (int i = tid; i < (m1 - m0) * 16 * T; i += kCW * 32) {
+      const int tok = i % T, row = (i / T) % 16, mi = i / T / 16;
+      const size_t hrow = (size_t)(m0 + mi) * 16 + row;
+      const int nu = s_nu[tok];
+      float acc2 = 0.f;
+      for (int j = 0; j < nu; ++j)
+        acc2 = fmaf(s_uw[tok][j], __ldcg(&a.dbuf[((size_t)s_ulist[tok][j] * H + hrow) * kMaxT + tok]), acc2);
+      const size_t yi = (size_t)tok * H + hrow;
+      const float yv = a.accumulate ? a.y[yi] + acc2 : acc2;
+      a.y[yi] = yv;
+      if (a.y_bf16) a.y_bf16[yi] = __bfloat16_as_ushort(__float2bfloat16_rn(yv));
+    }
+  }
+
+  // ---------------- epilogue: the last CTA to finish clears the per-call counters
+  __syncthreads();
+  __shared__ int s_last;
+  if (tid == 0) {
+    __threadfence();
+    const uint32_t prev = atomicAdd(&a.hdr->done, 1u);
+    s_last = (prev == (uint32_t)(G - 1));
+  }
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    for (int i = tid; i < U; i += blockDim.x) a.cnt_g[i] = 0u;
+    for (int i = tid; i < U * kMaxT; i += blockDim.x) a.amax_h[i] = 0u;
+    if (tid == 0) { a.hdr->gbar = 0u; a.hdr->done = 0u; }
+  }
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+static size_t ws_needed(const moe_layer_t* L, int T, int k) {
+  const size_t U = (size_t)T * k;
+  return kWsCounters + U * kMaxT * L->I * sizeof(float) + U * L->H * kMaxT * sizeof(float);
+}
+
+extern "C" size_t moe_workspace_bytes(const moe_layer_t* L, int32_t T_max, int32_t k) {
+  if (!L || T_max < 1 || T_max > kMaxT || k < 1 || k > kMaxK) return 0;
+  if (!moe_internal::shape_ok(L->H, L->I)) return 0;
+  return ws_needed(L, T_max, k);
+}
+
+template <int FMT>
+static moe_status_t launch_ffn(const FfnArgs& a, cudaStream_t s) {
+  using C = Cfg<FMT>;
+  static int configured[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  if (!configured[dev]) {
+    if (cudaFuncSetAttribute(ffn_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    configured[dev] = 1;
+  }
+  const int nsm = moe_internal::num_sms();
+  if (nsm <= 0) return MOE_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nsm);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, ffn_kernel<FMT>, a) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+static moe_status_t ffn_common(const char* site, const moe_layer_t* L, const void* x, int32_t T, const int32_t* idx,
+                               const float* w, int32_t k, float* y, void* y_bf16, int32_t accumulate, void* ws,
+                               size_t ws_bytes, void* stream) {
+  if (moe_internal::fault(site)) return MOE_ERR_FAULT_INJECTED;
+  if (!L || !x || !idx || !w || !y || !ws) return MOE_ERR_INVALID_ARG;
+  if (L->fmt < MOE_FMT_MXFP4 || L->fmt > MOE_FMT_Q2K) return MOE_ERR_UNSUPPORTED_FORMAT;
+  if (L->layout != MOE_LAYOUT_DECODE) return MOE_ERR_UNSUPPORTED_FORMAT;
+  if (!L->gate_up || !L->down || ((uintptr_t)L->gate_up & 15) || ((uintptr_t)L->down & 15)) return MOE_ERR_INVALID_ARG;
+  if (((uintptr_t)x & 3) || ((uintptr_t)ws & 255) || ((uintptr_t)y & 3)) return MOE_ERR_INVALID_ARG;
+  if (y_bf16 && ((uintptr_t)y_bf16 & 1)) return MOE_ERR_INVALID_ARG;
+  if (T < 1 || T > kMaxT || k < 1 || k > kMaxK || L->E < 1) return MOE_ERR_SHAPE;
+  if (!moe_internal::shape_ok(L->H, L->I)) return MOE_ERR_SHAPE;
+  if (ws_bytes < ws_needed(L, T, k)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  moe_status_t st = moe_check_device();
+  if (st != MOE_OK) return st;
+  FfnArgs a;
+  a.gate_up = (const uint8_t*)L->gate_up;
+  a.down = (const uint8_t*)L->down;
+  a.x = (const uint16_t*)x;
+  a.idx = idx;
+  a.w = w;
+  a.y = y;
+  a.y_bf16 = (uint16_t*)y_bf16;
+  a.accumulate = accumulate;
+  a.H = L->H; a.I = L->I; a.E = L->E; a.T = T; a.k = k;
+  uint8_t* base = (uint8_t*)ws;
+  a.hdr = (WsHeader*)base;
+  a.cnt_g = (uint32_t*)(base + kOffCntG);
+  a.amax_h = (uint32_t*)(base + kOffAmax);
+  a.hbuf = (float*)(base + kWsCounters);
+  a.dbuf = a.hbuf + (size_t)T * k * kMaxT * L->I;
+  a.wait_ns = kDefaultWaitNs;
+  cudaStream_t s = (cudaStream_t)stream;
+  switch (L->fmt) {
+    case MOE_FMT_MXFP4: return launch_ffn<MOE_FMT_MXFP4>(a, s);
+    case MOE_FMT_INT4G32: return launch_ffn<MOE_FMT_INT4G32>(a, s);
+    default: return launch_ffn<MOE_FMT_Q2K>(a, s);
+  }
+}
+
+extern "C" moe_status_t moe_expert_ffn_decode(const moe_layer_t* L, const void* x_bf16, const int32_t* idx,
+                                              const float* w, int32_t k, float* y, void* y_bf16, int32_t accumulate,
+                                              void* ws, size_t ws_bytes, void* stream) {
+  return ffn_common("decode", L, x_bf16, 1, idx, w, k, y, y_bf16, accumulate, ws, ws_bytes, stream);
+}
+
+extern "C" moe_status_t moe_expert_ffn_verify(const moe_layer_t* L, const void* x_bf16, int32_t T, const int32_t* idx,
+                                              const float* w, int32_t k, float* y, void* y_bf16, int32_t accumulate,
+                                              void* ws, size_t ws_bytes, void* stream) {
+  return ffn_common("verify", L, x_bf16, T, idx, w, k, y, y_bf16, accumulate, ws, ws_bytes, stream);
+}

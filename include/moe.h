@@ -1,0 +1,177 @@
+/*
+ * moe.h -- C ABI of libmoe.so: routed-MoE feed-forward step with low-bit expert weights on one GB300 (sm_103a).
+ *
+ * What is computed (pages cited by title and section):
+ *   - Routing: "Mixed-precision compression of DeepSeek-V4-Flash" (lumirain.cn), "The recipe": the router is
+ *     kept in F16 and every token uses its top-6 of 256 routed experts. Rule: logits = W_r x, top-k by logit
+ *     (ties to the lower expert index), weights = softmax over the k chosen logits. Hash routing of the first
+ *     layers: "quant surgery" (blog.meowhead.cn), section 4 (tid2eid table, equal weights).
+ *   - Expert FFN: y = sum_r w_r * Down_r( SiLU(Gate_r x) * (Up_r x) ); the gate and up mat-vecs are fused and the
+ *     down projection accumulates into the output ("quantization" glossary, ds4-learning.pages.dev, section
+ *     "Q4_K routed experts").
+ *   - Verify of width 1+K: "Mixed-precision compression...", "What compression does not solve" and "Width drift":
+ *     several tokens share one sweep of the expert weights, and row t of a wide verify must equal the width-1
+ *     decode of token t bit for bit ("Why this is not a host-side patch").
+ *   - Weight formats: "quantization" glossary, sections "MXFP4" (17-byte blocks: one E8M0 exponent, 32 E2M1
+ *     codes; e = 0 is zero) and "core principle" (Q2_K, 84 bytes per 256 weights); INT4 group 32 with a BF16
+ *     scale: "DeepSeek-V4-Flash-0731-W4A16" model card (alphaneural.io), quantisation scheme.
+ *
+ * Conventions for every call:
+ *   - All data pointers are DEVICE pointers, allocated and owned by the caller. The library allocates nothing.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream). Calls are asynchronous on it.
+ *   - Every call returns moe_status_t. Argument and shape errors are found on the host before any launch and
+ *     nothing is launched then. MOE_ERR_CUDA reports a failed launch (cudaGetLastError).
+ *   - Device-side errors (a bounded wait that ran out) are written to a status word inside the caller's
+ *     workspace; read it with moe_get_device_status(). After such an error call moe_workspace_init() again.
+ *   - The library keeps no mutable global state except a per-process cache of device properties.
+ *   - Host-side fault injection for tests: if the environment variable MOE_FAULT names a call
+ *     ("pack", "route", "decode", "verify", "prefill", "encode"), that call returns MOE_ERR_FAULT_INJECTED
+ *     without launching anything.
+ */
+#ifndef BIT_MOE_DECODE_GB300_MOE_H
+#define BIT_MOE_DECODE_GB300_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_FMT_MXFP4 = 1,   /* 17 B per 32 weights: byte 0 = E8M0 e, bytes 1..16 codes; element 2j = high nibble of
+                          byte 1+j, element 2j+1 = low nibble; value E2M1[code] * 2^(e-127), e=0 -> 0, e=255 -> NaN */
+  MOE_FMT_INT4G32 = 2, /* 18 B per 32 weights: bytes 0..15 two's-complement 4-bit codes (same nibble order),
+                          bytes 16..17 bf16 scale (little endian); value q * scale */
+  MOE_FMT_Q2K = 3      /* 84 B per 256 weights: scales[16] (sc = low nibble, m = high nibble, one per 16 weights),
+                          qs[64] (weight i = bits 2(i%4)..2(i%4)+1 of qs[i/4]), fp16 d, fp16 dmin;
+                          value d*sc*q - dmin*m */
+} moe_format_t;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,         /* null pointer, bad enum, misaligned pointer */
+  MOE_ERR_SHAPE = 2,               /* a size the kernels do not support (see each call) */
+  MOE_ERR_UNSUPPORTED_FORMAT = 3,  /* format not available for this call */
+  MOE_ERR_UNSUPPORTED_ARCH = 4,    /* current device is not compute capability 10.3 */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 5,
+  MOE_ERR_CUDA = 6,                /* a CUDA runtime call or launch failed */
+  MOE_ERR_DEVICE_TIMEOUT = 7,      /* a bounded device-side wait ran out (see moe_get_device_status) */
+  MOE_ERR_FAULT_INJECTED = 8,      /* MOE_FAULT named this call */
+  MOE_ERR_DEVICE_NAN = 9           /* reserved */
+} moe_status_t;
+
+const char* moe_status_string(moe_status_t s);
+int32_t moe_version(void);
+/* Returns MOE_OK if the current device is sm_103 (GB300), MOE_ERR_UNSUPPORTED_ARCH otherwise. */
+moe_status_t moe_check_device(void);
+
+/* ---------------------------------------------------------------- weights ---------------------------------------- */
+
+typedef enum { MOE_SRC_BLOCKS = 0, MOE_SRC_F32 = 1 } moe_src_t;
+typedef enum { MOE_LAYOUT_DECODE = 0, MOE_LAYOUT_PREFILL = 1 } moe_layout_t;
+typedef enum { MOE_MAT_GATE_UP = 0, MOE_MAT_DOWN = 1 } moe_matrix_t;
+
+/* Bytes of `rows` x `k` weights in the canonical block format (blocks run along k, row-major). */
+size_t moe_canonical_bytes(moe_format_t fmt, int64_t rows, int64_t k);
+
+/* Bytes of the packed device layout for n_experts experts. GATE_UP holds Gate [I,H] and Up [I,H] of each expert,
+ * DOWN holds Down [H,I]. The layout is expert-major with a fixed per-expert stride equal to
+ * moe_packed_bytes(fmt, layout, kind, 1, H, I), so experts can be packed in batches at dst + e * stride.
+ * The packed layout holds exactly the canonical bytes, permuted (same bits per weight). Returns 0 for an
+ * unsupported combination. */
+size_t moe_packed_bytes(moe_format_t fmt, moe_layout_t layout, moe_matrix_t kind, int64_t n_experts, int64_t H,
+                        int64_t I);
+
+/* GPU encoder: fp32 weights [rows, k] (row-major) -> canonical blocks (moe_canonical_bytes(fmt, rows, k) bytes).
+ * MXFP4: per 32 weights e = clamp(k0 + 127, 1, 254) with k0 the smallest integer such that amax <= 6 * 2^k0;
+ *        code = nearest E2M1 value of w * 2^(127-e), ties to the even code, sign kept on zero.
+ * INT4:  for r in {6/7, 0.9, 0.95, 1.0, 1.05, 1.1}: s = amax*r/7 (amax >= 1e-8), q = clamp(rint(w/s), -8, 7);
+ *        keep the first r with the smallest fp32 sum of (w - q*s)^2; scale stored as bf16(s) (the model card's
+ *        "FP4 -> INT4 conversion", step 2).
+ * Q2_K:  per 16-weight group lo = min(0, min w), s_g = (max w - lo)/3, o_g = -lo; d = fp16(max s_g / 15),
+ *        dmin = fp16(max o_g / 15); sc = rint(s_g/d), m = rint(o_g/dmin) clamped to [0,15];
+ *        q = clamp(rint((w + dmin*m)/(d*sc)), 0, 3) (the pages give no encoder; this is the library's own).
+ * All arithmetic fp32 round-to-nearest-even; bit-identical to the CPU oracle. k must be a multiple of the block
+ * size. src and dst device pointers; dst 16-byte aligned is not required. */
+moe_status_t moe_encode_blocks(moe_format_t fmt, const float* src, int64_t rows, int64_t k, void* dst, void* stream);
+
+/* Pack weights into the device layout.
+ *   kind GATE_UP: src_a = Gate, src_b = Up, each [n_experts, I, H];  kind DOWN: src_a = Down [n_experts, H, I],
+ *   src_b unused. With src_kind BLOCKS the sources are canonical blocks, with F32 they are fp32 weights that are
+ *   encoded on the fly exactly as moe_encode_blocks does.
+ *   dst must be 16-byte aligned and hold moe_packed_bytes(...) bytes.
+ * Shapes: H and I multiples of 256 (and of the block size), 256 <= H, I <= 4096.
+ * Layout MOE_LAYOUT_PREFILL is MXFP4 only. */
+moe_status_t moe_pack_weights(moe_format_t fmt, moe_src_t src_kind, moe_layout_t layout, moe_matrix_t kind,
+                              int64_t n_experts, int64_t H, int64_t I, const void* src_a, const void* src_b,
+                              void* dst, size_t dst_bytes, void* stream);
+
+/* One layer's packed experts. */
+typedef struct {
+  moe_format_t fmt;
+  moe_layout_t layout;
+  int32_t H;              /* hidden size */
+  int32_t I;              /* expert intermediate size */
+  int32_t E;              /* number of routed experts */
+  const void* gate_up;    /* moe_packed_bytes(fmt, layout, MOE_MAT_GATE_UP, E, H, I) bytes */
+  const void* down;       /* moe_packed_bytes(fmt, layout, MOE_MAT_DOWN, E, H, I) bytes */
+} moe_layer_t;
+
+/* ---------------------------------------------------------------- routing ---------------------------------------- */
+
+/* Router for T tokens.
+ *   Softmax mode (token_ids == NULL): logits[t,e] = sum_h W_r[e,h] * x[t,h] (fp16 x bf16 products, fp32 sums),
+ *     idx[t, 0..k) = the k largest logits in decreasing order, ties to the lower expert index,
+ *     weights[t, r] = exp(l_r - l_0) / sum_j exp(l_j - l_0) over the k chosen (fp32).
+ *   Hash mode (token_ids != NULL): idx[t, r] = tid2eid[token_ids[t] * k + r], weights = 1/k.
+ * router_w_f16 [E, H] fp16; x_bf16 [T, H] bf16; idx [T, k] int32; weights [T, k] fp32.
+ * Limits: 1 <= k <= 8, k <= E <= 1024, H multiple of 256 and <= 8192, T >= 1.
+ * Token ids outside [0, V) return MOE_ERR_INVALID_ARG only if checked on the host: they are device data, so
+ * the kernel clamps nothing and the caller must pass valid ids. */
+moe_status_t moe_route_topk(const void* router_w_f16, const void* x_bf16, int32_t T, int32_t H, int32_t E,
+                            int32_t k, const int32_t* token_ids, const int32_t* tid2eid, int32_t V, int32_t* idx,
+                            float* weights, void* stream);
+
+/* ---------------------------------------------------------------- expert FFN ------------------------------------- */
+
+/* Workspace (device scratch owned by the caller) for decode / verify of up to T_max tokens with top-k.
+ * It must be zeroed once with moe_workspace_init() before first use; the kernels leave it zeroed. */
+size_t moe_workspace_bytes(const moe_layer_t* layer, int32_t T_max, int32_t k);
+moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
+/* Synchronises `stream`, returns the device status word (MOE_OK or MOE_ERR_DEVICE_TIMEOUT) and clears it. */
+moe_status_t moe_get_device_status(void* ws, void* stream);
+
+/* Decode, one token: y[H] (=, or += if accumulate) sum_r w[r] * FFN_{idx[r]}(x).
+ *   x_bf16 [H] bf16; idx [k] int32 (expert ids < E); w [k] fp32; y [H] fp32; y_bf16 [H] bf16 or NULL
+ *   (round-to-nearest-even copy of y). Equivalent to moe_expert_ffn_verify with T = 1.
+ * Numerics: x is rescaled per token by a power of two and held in binary16 (exact for every element within
+ * 2^-28 of the token's largest |x|); weights are exact; h is fp32, rescaled per (expert, token) by a power of two
+ * into binary16 for the down projection; sums are fp32 on tensor cores. */
+moe_status_t moe_expert_ffn_decode(const moe_layer_t* layer, const void* x_bf16, const int32_t* idx, const float* w,
+                                   int32_t k, float* y, void* y_bf16, int32_t accumulate, void* ws, size_t ws_bytes,
+                                   void* stream);
+
+/* Verify, T tokens (1 <= T <= 8) sharing one sweep of the union of their experts' weights.
+ * Row t of y is bit-identical to moe_expert_ffn_decode of token t with the same idx/w rows.
+ *   x_bf16 [T, H]; idx [T, k]; w [T, k]; y [T, H]; y_bf16 [T, H] or NULL. */
+moe_status_t moe_expert_ffn_verify(const moe_layer_t* layer, const void* x_bf16, int32_t T, const int32_t* idx,
+                                   const float* w, int32_t k, float* y, void* y_bf16, int32_t accumulate, void* ws,
+                                   size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------- debug (tests only) ----------------------------- */
+
+/* Unpack expert `expert` of a packed matrix back to fp32 values [rows, K] (rows = I for each of gate and up,
+ * written as [2, I, H]; rows = H for down, [H, I]). For bit-exact checks of the layout. */
+moe_status_t moe_debug_unpack(moe_format_t fmt, moe_layout_t layout, moe_matrix_t kind, const void* packed,
+                              int64_t H, int64_t I, int64_t expert, float* out, void* stream);
+
+/* Runs a one-CTA kernel that waits on a flag nothing sets, with a limit of `limit_us` microseconds, then records
+ * MOE_ERR_DEVICE_TIMEOUT in the workspace status word and returns. Tests the bounded-wait path. */
+moe_status_t moe_debug_timeout_probe(void* ws, size_t ws_bytes, int32_t limit_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BIT_MOE_DECODE_GB300_MOE_H */

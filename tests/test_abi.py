@@ -1,0 +1,84 @@
+"""The C-ABI library builds, loads and exports every symbol include/moe.h declares; host-side logic (sizes, status
+strings, argument checks, fault injection) works without a GPU."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def m():
+    from bit_moe_decode_gb300 import build
+    build.build()
+    import bit_moe_decode_gb300 as mod
+    mod.lib()
+    return mod
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(m):
+    names = _declared()
+    assert len(names) >= 15
+    L = C.CDLL(m.LIB_PATH)
+    for n in names:
+        assert hasattr(L, n), n
+    assert sorted(m.EXPORTS) == names
+
+
+def test_status_strings_and_version(m):
+    assert m.moe_status_string(0) == "ok"
+    assert "timed" in m.moe_status_string(7) or "time" in m.moe_status_string(7)
+    assert m.moe_version() >= 100
+
+
+def test_sizes_host_only(m):
+    # canonical bytes: 17 B / 32, 18 B / 32, 84 B / 256
+    assert m.moe_canonical_bytes(1, 2048, 4096) == 2048 * 128 * 17
+    assert m.moe_canonical_bytes(2, 2048, 4096) == 2048 * 128 * 18
+    assert m.moe_canonical_bytes(3, 2048, 4096) == 2048 * 16 * 84
+    assert m.moe_canonical_bytes(3, 2048, 4000) == 0
+    # packed layout holds exactly the canonical bytes
+    for f in (1, 2, 3):
+        assert m.moe_packed_bytes(f, 0, 0, 256, 4096, 2048) == 256 * 2 * m.moe_canonical_bytes(f, 2048, 4096)
+        assert m.moe_packed_bytes(f, 0, 1, 256, 4096, 2048) == 256 * m.moe_canonical_bytes(f, 4096, 2048)
+    # active bytes per token-layer at top-6
+    per_tok = {f: 6 * (m.moe_packed_bytes(f, 0, 0, 1, 4096, 2048) + m.moe_packed_bytes(f, 0, 1, 1, 4096, 2048))
+               for f in (1, 2, 3)}
+    assert per_tok == {1: 80216064, 2: 84934656, 3: 49545216}
+    # unsupported shapes
+    assert m.moe_packed_bytes(1, 0, 0, 1, 4096 + 128, 2048) == 0
+    assert m.moe_packed_bytes(1, 0, 0, 1, 8192, 2048) == 0
+
+
+def test_workspace_bytes(m):
+    class FakeLayer:
+        pass
+    lay = FakeLayer()
+    lay.c = m.moe_layer_t(1, 0, 4096, 2048, 256, None, None)
+    one = m.moe_workspace_bytes(lay, 1, 6)
+    eight = m.moe_workspace_bytes(lay, 8, 6)
+    assert one == 4096 + 6 * 8 * 2048 * 4 + 6 * 4096 * 8 * 4
+    assert eight == 4096 + 48 * 8 * 2048 * 4 + 48 * 4096 * 8 * 4
+    assert m.moe_workspace_bytes(lay, 9, 6) == 0
+
+
+def test_fault_injection_and_argument_checks(m, monkeypatch):
+    L = m.lib()
+    monkeypatch.setenv("MOE_FAULT", "decode,pack")
+    assert L.moe_pack_weights(1, 0, 0, 0, 1, 512, 256, None, None, None, 0, None) == 8
+    lay = m.moe_layer_t(1, 0, 512, 256, 8, None, None)
+    assert L.moe_expert_ffn_decode(C.byref(lay), None, None, None, 2, None, None, 0, None, 0, None) == 8
+    # a call not named still runs its own checks: null pointers are rejected before any launch
+    assert L.moe_expert_ffn_verify(C.byref(lay), None, 1, None, None, 2, None, None, 0, None, 0, None) == 1
+    monkeypatch.setenv("MOE_FAULT", "")
+    assert L.moe_pack_weights(1, 0, 0, 0, 1, 512, 256, None, None, None, 0, None) == 1
+    assert L.moe_pack_weights(9, 0, 0, 0, 1, 512, 256, None, None, None, 0, None) == 3
+    assert L.moe_route_topk(None, None, 1, 4096, 256, 6, None, None, 0, None, None, None) == 1
