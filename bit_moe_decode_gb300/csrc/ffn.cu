@@ -30,8 +30,8 @@
 
 namespace moe {
 
-constexpr int kCW = 8;                 // consumer warps
-constexpr int kThreads = (kCW + 1) * 32;
+constexpr int kMaxCW = 16;             // consumer warps (tensor-core mat-vec), at most
+constexpr int kNR = 4;                 // reduction slots between consumers and the epilogue warp
 constexpr int kMaxT = 8;
 constexpr int kMaxK = 8;
 constexpr int kMaxU = kMaxT * kMaxK;   // 64
@@ -62,12 +62,16 @@ struct FfnArgs {
 
 template <int FMT> struct Cfg {
   using F = Fmt<FMT>;
+  // Warp roles: CW consumer warps (each owns a K slice of every tile), one producer warp (bulk copies), one
+  // epilogue warp (cross-warp sums, outputs, signals, combine).
+  static constexpr int CW = FMT == MOE_FMT_Q2K ? 8 : 16;
+  static constexpr int PROD = CW, EPI = CW + 1, THREADS = (CW + 2) * 32;
   static constexpr int SB = F::CPS * F::CB;                                // stage bytes (2048 columns)
   static constexpr int NS = FMT == MOE_FMT_Q2K ? 13 : 8;                   // ring stages
-  static constexpr int NCH = 4096 / F::CK / kCW;                           // max chunks per warp per tile
-  static constexpr int NPS = F::CPS / kCW;                                 // chunks per warp per stage
-  static constexpr int SXF = FMT == MOE_FMT_Q2K ? kCW * NCH * F::STEPS * kMaxT : 0;  // group sums of x (floats)
-  static constexpr int RED = 2 * kCW * 32 * 4;                             // double-buffered reduction (floats)
+  static constexpr int NCH = 4096 / F::CK / CW;                            // max chunks per warp per tile
+  static constexpr int NPS = F::CPS / CW;                                  // chunks per warp per stage
+  static constexpr int SXF = FMT == MOE_FMT_Q2K ? CW * NCH * F::STEPS * kMaxT : 0;   // group sums of x (floats)
+  static constexpr int RED = kNR * CW * 32 * 4;                            // reduction slots (floats)
   static constexpr size_t SMEM = (size_t)NS * SB + (size_t)(RED + SXF) * 4;
 };
 
@@ -181,7 +185,7 @@ __device__ __forceinline__ bool consume_tile(uint8_t* ring, uint64_t* full, uint
       const uint32_t par = ((it + s) / C::NS) & 1;
       if (*abort || !mbar_wait(&full[slot], par, wait_ns)) ok = false;
     }
-    const int c = warp + kCW * n;
+    const int c = warp + C::CW * n;
     if (ok && c < nchunks) {
       const uint8_t* cp = ring + (size_t)slot * C::SB + (size_t)(c - s * F::CPS) * F::CB;
       chunk_mma<FMT>(cp, lane, b[n], sxw ? sxw + n * F::STEPS * kMaxT : nullptr, acc);
@@ -195,25 +199,70 @@ __device__ __forceinline__ bool consume_tile(uint8_t* ring, uint64_t* full, uint
   return ok;
 }
 
+// Loads the warp's B fragments of expert u's h (rescaled per token into fp16) after its G tiles are all done.
 template <int FMT>
-__global__ void __launch_bounds__(kThreads, 1) ffn_kernel(const FfnArgs a) {
+__device__ __forceinline__ void load_h_fragments(const FfnArgs& a, int u, int ncd, int warp, int lane,
+                                                 uint32_t (&bh)[Cfg<FMT>::NCH][Fmt<FMT>::STEPS][2], float* sxw) {
+  using C = Cfg<FMT>;
+  using F = Fmt<FMT>;
+  const int col = lane >> 2, q = lane & 3, T = a.T, I = a.I;
+  const float am = col < T ? __uint_as_float(__ldcg(&a.amax_h[u * kMaxT + col])) : 0.f;
+  const float sc = exp2i(rescale_exponent(am));
+#pragma unroll
+  for (int n = 0; n < C::NCH; ++n) {
+    const int c = warp + C::CW * n;
+#pragma unroll
+    for (int j = 0; j < F::STEPS; ++j) {
+      uint32_t v[2] = {0u, 0u};
+      if (c < ncd && col < T) {
+        const float* hr = a.hbuf + ((size_t)u * kMaxT + col) * I + c * F::CK + 16 * j + 2 * q;
+        const float2 p0 = __ldcg(reinterpret_cast<const float2*>(hr));
+        const float2 p1 = __ldcg(reinterpret_cast<const float2*>(hr + 8));
+        const __half2 h0 = __floats2half2_rn(p0.x * sc, p0.y * sc);
+        const __half2 h1 = __floats2half2_rn(p1.x * sc, p1.y * sc);
+        v[0] = *reinterpret_cast<const uint32_t*>(&h0);
+        v[1] = *reinterpret_cast<const uint32_t*>(&h1);
+      }
+      bh[n][j][0] = v[0];
+      bh[n][j][1] = v[1];
+    }
+  }
+  if constexpr (FMT == MOE_FMT_Q2K) {
+#pragma unroll
+    for (int n = 0; n < C::NCH; ++n)
+#pragma unroll
+      for (int j = 0; j < F::STEPS; ++j) {
+        const __half2 h0 = *reinterpret_cast<const __half2*>(&bh[n][j][0]);
+        const __half2 h1 = *reinterpret_cast<const __half2*>(&bh[n][j][1]);
+        float s = (__low2float(h0) + __high2float(h0)) + (__low2float(h1) + __high2float(h1));
+        s += __shfl_xor_sync(0xffffffffu, s, 1);
+        s += __shfl_xor_sync(0xffffffffu, s, 2);
+        if (q == 0) sxw[(n * F::STEPS + j) * kMaxT + col] = s;
+      }
+    __syncwarp();
+  }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(Cfg<FMT>::THREADS, 1) ffn_kernel(const FfnArgs a) {
   using C = Cfg<FMT>;
   using F = Fmt<FMT>;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
-  float* red = reinterpret_cast<float*>(smem + (size_t)C::NS * C::SB);
+  float* red = reinterpret_cast<float*>(smem + (size_t)C::NS * C::SB);   // [kNR][C::CW warps][32 lanes][4]
   float* sx = red + C::RED;
-  __shared__ __align__(8) uint64_t full[C::NS], empty[C::NS];
+  __shared__ __align__(8) uint64_t full[C::NS], empty[C::NS], redfull[kNR], redempty[kNR];
   __shared__ int s_val[kMaxU], s_first[kMaxU], s_slot[kMaxU], s_union[kMaxU];
-  __shared__ float s_wsum[kMaxT][kMaxU];        // per token: summed router weight of each union expert
   __shared__ int s_routed[kMaxT][kMaxU];        // per token: does it route to this union expert
+  __shared__ float s_wsum[kMaxT][kMaxU];        // per token: summed router weight of each union expert
   __shared__ int s_nu[kMaxT];                   // per token: its union experts in ascending order ...
   __shared__ int s_ulist[kMaxT][kMaxK];
   __shared__ float s_uw[kMaxT][kMaxK];          // ... and their summed weights
-  __shared__ int s_U;
+  __shared__ int s_U, s_last;
   __shared__ volatile int s_abort;
   __shared__ int s_sig[kMaxT];
-  __shared__ float s_colmax[kCW][kMaxT];
+  __shared__ float s_colmax[kMaxCW][kMaxT];
+  __shared__ float s_hinv[kMaxT];               // epilogue warp: 2^-sigma of the current D expert, per token
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = a.T, k = a.k, H = a.H, I = a.I;
@@ -221,7 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_kernel(const FfnArgs a) {
 
   // ---------------- prologue: barriers, union of the tokens' experts (sorted, deduplicated), weight sums
   if (tid == 0) {
-    for (int s = 0; s < C::NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], kCW); }
+    for (int s = 0; s < C::NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], C::CW); }
+    for (int s = 0; s < kNR; ++s) { mbar_init(&redfull[s], C::CW); mbar_init(&redempty[s], 1); }
     fence_mbar_init();
     s_abort = 0;
   }
@@ -241,30 +291,35 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_kernel(const FfnArgs a) {
   __syncthreads();
   if (tid < n_ent) {
     const int v = s_val[tid];
-    int rank = 0;
-    for (int j = 0; j < n_ent; ++j) rank += (s_first[j] && s_val[j] < v) ? 1 : 0;
+    int rank = 0, nfirst = 0;
+    for (int j = 0; j < n_ent; ++j) {
+      rank += (s_first[j] && s_val[j] < v) ? 1 : 0;
+      nfirst += s_first[j];
+    }
     s_slot[tid] = rank;
     if (s_first[tid]) s_union[rank] = v;
-  }
-  if (tid == 0) {
-    int u = 0;
-    for (int j = 0; j < n_ent; ++j) u += s_first[j];
-    s_U = u;
-  }
-  __syncthreads();
-  if (tid < T) {  // rank order, so a token's sums do not depend on the other tokens
-    for (int r = 0; r < k; ++r) {
-      const int u = s_slot[tid * k + r];
-      s_wsum[tid][u] += __ldg(&a.w[tid * k + r]);
-      s_routed[tid][u] = 1;
+    if (tid == 0) s_U = nfirst;
+    // rank order, so a token's weight sums do not depend on the other tokens
+    if (tid % k == 0) {
+      const int t = tid / k;
+      for (int r = 0; r < k; ++r) {
+        int rr = 0;
+        const int vv = s_val[t * k + r];
+        for (int j = 0; j < n_ent; ++j) rr += (s_first[j] && s_val[j] < vv) ? 1 : 0;
+        s_wsum[t][rr] += __ldg(&a.w[t * k + r]);
+        s_routed[t][rr] = 1;
+      }
     }
-    int n = 0;
-    for (int u = 0; u < s_U; ++u)
-      if (s_routed[tid][u]) { s_ulist[tid][n] = u; s_uw[tid][n] = s_wsum[tid][u]; ++n; }
-    s_nu[tid] = n;
   }
   __syncthreads();
   const int U = s_U;
+  if (tid < T) {
+    int n = 0;
+    for (int u = 0; u < U; ++u)
+      if (s_routed[tid][u]) { s_ulist[tid][n] = u; s_uw[tid][n] = s_wsum[tid][u]; ++n; }
+    s_nu[tid] = n;
+  }
+  // (s_nu / s_ulist are read only by the epilogue warp after the grid barrier, far below)
   const int G = gridDim.x, bid = blockIdx.x;
   const int gt = I / 8, dt = H / 16;  // tiles per expert
   const int64_t NG = (int64_t)U * gt, ND = (int64_t)U * dt;
@@ -275,8 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_kernel(const FfnArgs a) {
   const int64_t tbg = tile_bytes(FMT, H), tbd = tile_bytes(FMT, I);
   const int64_t sgu = gate_up_stride(FMT, H, I), sdn = down_stride(FMT, H, I);
 
-  if (warp == kCW) {
-    // ================= producer: G tiles of the CTA's range, then for each union expert its D tiles [m0, m1)
+  if (warp == C::PROD) {
+    // ================= producer: G tiles of the CTA's range, then its D tiles (expert-major)
     if (lane == 0 && !s_abort) {
       const uint64_t pol = policy_evict_first();
       uint32_t it = 0;
@@ -309,12 +364,122 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_kernel(const FfnArgs a) {
         for (uint32_t i = lo; i < it; ++i) mbar_wait(&full[i % C::NS], (i / C::NS) & 1, a.wait_ns);
       }
     }
+  } else if (warp == C::EPI) {
+    // ================= epilogue warp: per unit, sum the 8 warps' partials in warp order, then
+    //   G: h = SiLU(g) * u -> h buffer (fp32) and the per-(expert, token) max |h|
+    //   D: d = down partial of the unit's expert -> d buffer
+    // then the grid barrier and the combine of the CTA's output rows.
+    uint32_t ri = 0;
+    auto wait_red = [&](uint32_t r) -> const float* {
+      const int slot = (int)(r % kNR);
+      if (s_abort || !mbar_wait(&redfull[slot], (r / kNR) & 1, a.wait_ns)) {
+        record_error(&a.hdr->status, MOE_ERR_DEVICE_TIMEOUT);
+        s_abort = 1;
+      }
+      return red + (size_t)slot * (C::CW * 32 * 4);
+    };
+    auto release_red = [&](uint32_t r) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&redempty[r % kNR]);
+    };
+    int pend_u = -1, pend_n = 0;  // G tiles done but not yet published, for one expert
+    for (int64_t gu = g0; gu < g1; ++gu, ++ri) {
+      const int u = (int)(gu / gt), jt = (int)(gu % gt);
+      const float* rb = wait_red(ri);
+#pragma unroll
+      for (int pp = 0; pp < 2; ++pp) {
+        // output pair p -> fragment lane fl, column slot cc: g from c[cc] (row fl/4), u from c[cc+2] (row fl/4+8)
+        const int p = lane + 32 * pp, fl = p >> 1, cc = p & 1;
+        const int r = fl >> 2, tc = 2 * (fl & 3) + cc;
+        if (tc < T) {
+          float gs = 0.f, us = 0.f;
+#pragma unroll
+          for (int w = 0; w < C::CW; ++w) {
+            gs += rb[(w * 32 + fl) * 4 + cc];
+            us += rb[(w * 32 + fl) * 4 + cc + 2];
+          }
+          const float inv = exp2i_neg(s_sig[tc]);
+          const float g = gs * inv, uu = us * inv;
+          const float h = g * __frcp_rn(1.0f + __expf(-g)) * uu;   // SiLU(g) * u
+          a.hbuf[((size_t)u * kMaxT + tc) * I + (size_t)jt * 8 + r] = h;
+          atomicMax(&a.amax_h[u * kMaxT + tc], __float_as_uint(fabsf(h)));
+        }
+      }
+      release_red(ri);
+      // publish per expert: when the expert changes and after the CTA's last G tile
+      if (pend_u != u) {
+        if (pend_u >= 0 && lane == 0) { __threadfence(); atomicAdd(&a.cnt_g[pend_u], (uint32_t)pend_n); }
+        pend_u = u;
+        pend_n = 0;
+      }
+      ++pend_n;
+    }
+    if (pend_u >= 0 && lane == 0) { __threadfence(); atomicAdd(&a.cnt_g[pend_u], (uint32_t)pend_n); }
+    int hu = -1;
+    for (int64_t du = d0; du < d1; ++du, ++ri) {
+      const int u = (int)(du / dt), m = (int)(du % dt);
+      const float* rb = wait_red(ri);
+      if (u != hu) {  // the consumers waited for this expert's G tiles before handing over this unit
+        if (lane < T) s_hinv[lane] = exp2i_neg(rescale_exponent(__uint_as_float(__ldcg(&a.amax_h[u * kMaxT + lane]))));
+        __syncwarp();
+        hu = u;
+      }
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp) {
+        const int p = lane + 32 * pp, fl = p >> 2, cc = p & 3;
+        const int row = (fl >> 2) + 8 * (cc >> 1), tc = 2 * (fl & 3) + (cc & 1);
+        if (tc < T && s_routed[tc][u]) {
+          float ds = 0.f;
+#pragma unroll
+          for (int w = 0; w < C::CW; ++w) ds += rb[(w * 32 + fl) * 4 + cc];
+          a.dbuf[((size_t)u * H + (size_t)m * 16 + row) * kMaxT + tc] = ds * s_hinv[tc];
+        }
+      }
+      release_red(ri);
+    }
+    // ---- grid-wide barrier, then the CTA combines its output rows: y_t = sum over the token's own experts, in
+    //      ascending expert id, of w * d (fp32 fma), so the result does not depend on the other tokens
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence();
+      atomicAdd(&a.hdr->gbar, 1u);
+      if (!s_abort && !wait_counter(&a.hdr->gbar, (uint32_t)G, a.wait_ns)) {
+        record_error(&a.hdr->status, MOE_ERR_DEVICE_TIMEOUT);
+        s_abort = 1;
+      }
+    }
+    __syncwarp();
+    for (int i = lane; i < (m1 - m0) * 16 * T; i += 32) {
+      const int tok = i % T, row = (i / T) % 16, mi = i / T / 16;
+      const size_t hrow = (size_t)(m0 + mi) * 16 + row;
+      const int nu = s_nu[tok];
+      float acc2 = 0.f;
+      for (int j = 0; j < nu; ++j)
+        acc2 = fmaf(s_uw[tok][j], __ldcg(&a.dbuf[((size_t)s_ulist[tok][j] * H + hrow) * kMaxT + tok]), acc2);
+      const size_t yi = (size_t)tok * H + hrow;
+      const float yv = a.accumulate ? a.y[yi] + acc2 : acc2;
+      a.y[yi] = yv;
+      if (a.y_bf16) a.y_bf16[yi] = __bfloat16_as_ushort(__float2bfloat16_rn(yv));
+    }
   } else {
-    // ================= consumers
-    uint32_t it = 0;
+    // ================= consumers (warps 0..7): tensor-core mat-vec over their K slices
+    uint32_t it = 0, ri = 0;
     const int col = lane >> 2, q = lane & 3;
     float* sxw = (FMT == MOE_FMT_Q2K) ? sx + warp * (C::NCH * F::STEPS * kMaxT) : nullptr;
-    int bufsel = 0;
+    auto hand_over = [&](const float (&acc)[4]) {
+      const int slot = (int)(ri % kNR);
+      if (ri >= (uint32_t)kNR) {
+        if (s_abort || !mbar_wait(&redempty[slot], ((ri / kNR) - 1) & 1, a.wait_ns)) {
+          record_error(&a.hdr->status, MOE_ERR_DEVICE_TIMEOUT);
+          s_abort = 1;
+        }
+      }
+      float* rb = red + (size_t)slot * (C::CW * 32 * 4);
+      *reinterpret_cast<float4*>(rb + (warp * 32 + lane) * 4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&redfull[slot]);
+      ++ri;
+    };
 
     // ---- phase G: B fragments = x of the T tokens, rescaled per token into fp16
     {
@@ -322,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_kernel(const FfnArgs a) {
       float mx = 0.f;
 #pragma unroll
       for (int n = 0; n < C::NCH; ++n) {
-        const int c = warp + kCW * n;
+        const int c = warp + C::CW * n;
 #pragma unroll
         for (int j = 0; j < F::STEPS; ++j) {
           uint32_t v0 = 0, v1 = 0;
@@ -341,12 +506,12 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_kernel(const FfnArgs a) {
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
       if (q == 0) s_colmax[warp][col] = mx;
-      named_bar(1, kCW * 32);
+      named_bar(1, C::CW * 32);
       float cm = 0.f;
 #pragma unroll
-      for (int w = 0; w < kCW; ++w) cm = fmaxf(cm, s_colmax[w][col]);
+      for (int w = 0; w < C::CW; ++w) cm = fmaxf(cm, s_colmax[w][col]);
       const int sig = rescale_exponent(cm);
-      if (warp == 0 && q == 0) s_sig[col] = sig;
+      if (warp == 0 && q == 0) s_sig[col] = sig;   // read by the epilogue warp after the first hand-over
       const float sc = exp2i(sig);
 #pragma unroll
       for (int n = 0; n < C::NCH; ++n)
@@ -373,59 +538,23 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_kernel(const FfnArgs a) {
           }
         __syncwarp();
       }
-      named_bar(1, kCW * 32);
 
       for (int64_t gu = g0; gu < g1; ++gu) {
-        const int u = (int)(gu / gt), jt = (int)(gu % gt);
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         if (!consume_tile<FMT>(ring, full, empty, it, ncg, warp, lane, bx, sxw, acc, a.wait_ns, &s_abort)) {
           record_error(&a.hdr->status, MOE_ERR_DEVICE_TIMEOUT);
           s_abort = 1;
         }
-        float* rb = red + bufsel * (kCW * 32 * 4);
-        *reinterpret_cast<float4*>(rb + (warp * 32 + lane) * 4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        named_bar(1, kCW * 32);
-        if (tid < 64) {
-          // thread -> (fragment lane fl, column slot cc): g from c[cc], u from c[cc+2]; warps summed in order
-          const int fl = tid >> 1, cc = tid & 1;
-          float gs = 0.f, us = 0.f;
-#pragma unroll
-          for (int w = 0; w < kCW; ++w) {
-            gs += rb[(w * 32 + fl) * 4 + cc];
-            us += rb[(w * 32 + fl) * 4 + cc + 2];
-          }
-          const int r = fl >> 2, tc = 2 * (fl & 3) + cc;
-          if (tc < T) {
-            const float inv = exp2i_neg(s_sig[tc]);
-            const float g = gs * inv, uu = us * inv;
-            const float h = g / (1.0f + expf(-g)) * uu;
-            a.hbuf[((size_t)u * kMaxT + tc) * I + (size_t)jt * 8 + r] = h;
-            atomicMax(&a.amax_h[u * kMaxT + tc], __float_as_uint(fabsf(h)));
-          }
-        }
-        bufsel ^= 1;
-      }
-      // publish this CTA's G tiles: one release per expert it touched
-      named_bar(1, kCW * 32);
-      if (tid == 0 && g1 > g0) {
-        __threadfence();
-        int64_t gu = g0;
-        while (gu < g1) {
-          const int u = (int)(gu / gt);
-          const int64_t end = min(g1, (int64_t)(u + 1) * gt);
-          atomicAdd(&a.cnt_g[u], (uint32_t)(end - gu));
-          gu = end;
-        }
+        hand_over(acc);
       }
     }
 
-    // ---- phase D: the CTA's range of down tiles (expert-major, so it loads the h of one or two experts);
-    //      B fragments = the expert's h rescaled per token into fp16; partial outputs go to d [U, H, 8]
+    // ---- phase D: the CTA's range of down tiles (expert-major, so it loads the h of one or two experts)
     {
       uint32_t bh[C::NCH][F::STEPS][2];
       int loaded = -1;
       for (int64_t du = d0; du < d1; ++du) {
-        const int u = (int)(du / dt), m = (int)(du % dt);
+        const int u = (int)(du / dt);
         if (u != loaded) {
           if (lane == 0 && !s_abort) {
             if (!wait_counter(&a.cnt_g[u], (uint32_t)gt, a.wait_ns)) {
@@ -434,41 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_kernel(const FfnArgs a) {
             }
           }
           __syncwarp();
-          const float am = col < T ? __uint_as_float(__ldcg(&a.amax_h[u * kMaxT + col])) : 0.f;
-          const float sc = exp2i(rescale_exponent(am));
-#pragma unroll
-          for (int n = 0; n < C::NCH; ++n) {
-            const int c = warp + kCW * n;
-#pragma unroll
-            for (int j = 0; j < F::STEPS; ++j) {
-              uint32_t v[2] = {0u, 0u};
-              if (c < ncd && col < T) {
-                const float* hr = a.hbuf + ((size_t)u * kMaxT + col) * I + c * F::CK + 16 * j + 2 * q;
-                const float2 p0 = __ldcg(reinterpret_cast<const float2*>(hr));
-                const float2 p1 = __ldcg(reinterpret_cast<const float2*>(hr + 8));
-                const __half2 h0 = __floats2half2_rn(p0.x * sc, p0.y * sc);
-                const __half2 h1 = __floats2half2_rn(p1.x * sc, p1.y * sc);
-                v[0] = *reinterpret_cast<const uint32_t*>(&h0);
-                v[1] = *reinterpret_cast<const uint32_t*>(&h1);
-              }
-              bh[n][j][0] = v[0];
-              bh[n][j][1] = v[1];
-            }
-          }
-          if constexpr (FMT == MOE_FMT_Q2K) {
-#pragma unroll
-            for (int n = 0; n < C::NCH; ++n)
-#pragma unroll
-              for (int j = 0; j < F::STEPS; ++j) {
-                const __half2 h0 = *reinterpret_cast<const __half2*>(&bh[n][j][0]);
-                const __half2 h1 = *reinterpret_cast<const __half2*>(&bh[n][j][1]);
-                float s = (__low2float(h0) + __high2float(h0)) + (__low2float(h1) + __high2float(h1));
-                s += __shfl_xor_sync(0xffffffffu, s, 1);
-                s += __shfl_xor_sync(0xffffffffu, s, 2);
-                if (q == 0) sxw[(n * F::STEPS + j) * kMaxT + col] = s;
-              }
-            __syncwarp();
-          }
+          load_h_fragments<FMT>(a, u, ncd, warp, lane, bh, sxw);
           loaded = u;
         }
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -476,53 +571,13 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_kernel(const FfnArgs a) {
           record_error(&a.hdr->status, MOE_ERR_DEVICE_TIMEOUT);
           s_abort = 1;
         }
-        float* rb = red + bufsel * (kCW * 32 * 4);
-        *reinterpret_cast<float4*>(rb + (warp * 32 + lane) * 4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        named_bar(1, kCW * 32);
-        if (tid < 128) {
-          const int fl = tid >> 2, cc = tid & 3;
-          const int row = (fl >> 2) + 8 * (cc >> 1), tc = 2 * (fl & 3) + (cc & 1);
-          if (tc < T && s_routed[tc][u]) {
-            float ds = 0.f;
-#pragma unroll
-            for (int w = 0; w < kCW; ++w) ds += rb[(w * 32 + fl) * 4 + cc];
-            const float am2 = __uint_as_float(__ldcg(&a.amax_h[u * kMaxT + tc]));
-            a.dbuf[((size_t)u * H + (size_t)m * 16 + row) * kMaxT + tc] = ds * exp2i_neg(rescale_exponent(am2));
-          }
-        }
-        bufsel ^= 1;
+        hand_over(acc);
       }
-    }
-
-    // ---- grid-wide barrier, then each CTA combines its output rows: y_t = sum over the token's own experts, in
-    //      ascending expert id, of w * d (fp32 fma), so the result does not depend on the other tokens
-    named_bar(1, kCW * 32);
-    if (tid == 0) {
-      __threadfence();
-      atomicAdd(&a.hdr->gbar, 1u);
-      if (!s_abort && !wait_counter(&a.hdr->gbar, (uint32_t)G, a.wait_ns)) {
-        record_error(&a.hdr->status, MOE_ERR_DEVICE_TIMEOUT);
-        s_abort = 1;
-      }
-    }
-    named_bar(1, kCW * 32);
-    for (int i = tid; i < (m1 - m0) * 16 * T; i += kCW * 32) {
-      const int tok = i % T, row = (i / T) % 16, mi = i / T / 16;
-      const size_t hrow = (size_t)(m0 + mi) * 16 + row;
-      const int nu = s_nu[tok];
-      float acc2 = 0.f;
-      for (int j = 0; j < nu; ++j)
-        acc2 = fmaf(s_uw[tok][j], __ldcg(&a.dbuf[((size_t)s_ulist[tok][j] * H + hrow) * kMaxT + tok]), acc2);
-      const size_t yi = (size_t)tok * H + hrow;
-      const float yv = a.accumulate ? a.y[yi] + acc2 : acc2;
-      a.y[yi] = yv;
-      if (a.y_bf16) a.y_bf16[yi] = __bfloat16_as_ushort(__float2bfloat16_rn(yv));
     }
   }
 
   // ---------------- epilogue: the last CTA to finish clears the per-call counters
   __syncthreads();
-  __shared__ int s_last;
   if (tid == 0) {
     __threadfence();
     const uint32_t prev = atomicAdd(&a.hdr->done, 1u);
@@ -567,7 +622,7 @@ static moe_status_t launch_ffn(const FfnArgs& a, cudaStream_t s) {
   if (nsm <= 0) return MOE_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(nsm);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(C::THREADS);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
