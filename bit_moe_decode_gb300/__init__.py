@@ -29,7 +29,7 @@ BLOCK = {MOE_FMT_MXFP4: (32, 17), MOE_FMT_INT4G32: (32, 18), MOE_FMT_Q2K: (256, 
 EXPORTS = ["moe_status_string", "moe_version", "moe_check_device", "moe_canonical_bytes", "moe_packed_bytes",
            "moe_encode_blocks", "moe_pack_weights", "moe_route_topk", "moe_workspace_bytes", "moe_workspace_init",
            "moe_get_device_status", "moe_expert_ffn_decode", "moe_expert_ffn_verify", "moe_debug_unpack",
-           "moe_debug_timeout_probe"]
+           "moe_debug_timeout_probe", "moe_expert_ffn_decode_static"]
 
 
 class MoeError(RuntimeError):
@@ -71,6 +71,7 @@ def lib() -> C.CDLL:
             "moe_expert_ffn_verify": (C.c_int, [LP, P, i32, P, P, i32, P, P, i32, P, sz, P]),
             "moe_debug_unpack": (C.c_int, [C.c_int, C.c_int, C.c_int, P, i64, i64, i64, P, P]),
             "moe_debug_timeout_probe": (C.c_int, [P, sz, i32, P]),
+            "moe_expert_ffn_decode_static": (C.c_int, [LP, P, P, P, i32, P, P, i32, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -160,6 +161,15 @@ def moe_expert_ffn_verify(layer: "Layer", x_bf16, T: int, idx, w, k: int, y, y_b
     _check(lib().moe_expert_ffn_verify(C.byref(layer.c), _ptr(x_bf16), T, _ptr(idx), _ptr(w), k, _ptr(y),
                                        _ptr(y_bf16), int(accumulate), _ptr(ws), ws.numel() * ws.element_size(),
                                        _stream(stream)), "moe_expert_ffn_verify")
+
+
+def moe_expert_ffn_decode_static(layer: "Layer", x_bf16, idx, w, k: int, y, y_bf16=None, accumulate: bool = False,
+                                 stream=None):
+    """Decode one token without a workspace: the library uses its own fixed scratch array (for callers that
+    cannot allocate device memory). See include/moe.h for the limits and the first-call set-up."""
+    _check(lib().moe_expert_ffn_decode_static(C.byref(layer.c), _ptr(x_bf16), _ptr(idx), _ptr(w), k, _ptr(y),
+                                              _ptr(y_bf16), int(accumulate), _stream(stream)),
+           "moe_expert_ffn_decode_static")
 
 
 def moe_debug_unpack(fmt: int, layout: int, kind: int, packed: torch.Tensor, H: int, I: int, expert: int,

@@ -24,6 +24,8 @@
 //   * Handoff G -> D: per-expert counters (acquire/release); D units wait (bounded) for all G tiles of their
 //     expert. The combine for a 16-row output tile is done by the CTA that finishes its last expert (counter),
 //     so no floating-point atomics are used anywhere. The last CTA to finish clears the counters.
+#include <mutex>
+
 #include "common.cuh"
 #include "layout.cuh"
 #include "api_internal.h"
@@ -684,4 +686,48 @@ extern "C" moe_status_t moe_expert_ffn_verify(const moe_layer_t* L, const void* 
                                               const float* w, int32_t k, float* y, void* y_bf16, int32_t accumulate,
                                               void* ws, size_t ws_bytes, void* stream) {
   return ffn_common("verify", L, x_bf16, T, idx, w, k, y, y_bf16, accumulate, ws, ws_bytes, stream);
+}
+
+// ------------------------------------------------------------------------------------------------------------------
+// Decode without a caller-provided workspace.
+//
+// Some callers cannot allocate device memory: a plugin whose host hands it only the input and output buffers, code
+// that runs under a device-memory budget owned by another allocator, or code that must not allocate while a stream
+// is being captured. For them moe_expert_ffn_decode_static() runs the same decode kernel with its scratch in the
+// file-scope array below instead of a workspace. The array is sized for one token with k <= 8 and H, I <= 4096:
+// kStaticScratchBytes = 4096 (counters) + 8 * 8 * 4096 * 4 (h) + 8 * 4096 * 8 * 4 (d) = 2,101,248 bytes, held by
+// every GPU that loads this library until the process exits.
+// ------------------------------------------------------------------------------------------------------------------
+namespace {
+constexpr size_t kStaticScratchBytes = kWsCounters + (size_t)kMaxK * kMaxT * 4096 * 4 + (size_t)kMaxK * 4096 * kMaxT * 4;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+std::mutex g_static_mu;
+void* g_static_ptr[64];  // device address of g_static_scratch, per device, looked up once
+}  // namespace
+
+extern "C" moe_status_t moe_expert_ffn_decode_static(const moe_layer_t* L, const void* x_bf16, const int32_t* idx,
+                                                     const float* w, int32_t k, float* y, void* y_bf16,
+                                                     int32_t accumulate, void* stream) {
+  if (moe_internal::fault("decode")) return MOE_ERR_FAULT_INJECTED;
+  if (!L || !x_bf16 || !idx || !w || !y) return MOE_ERR_INVALID_ARG;
+  if (k < 1 || k > kMaxK || !moe_internal::shape_ok(L->H, L->I)) return MOE_ERR_SHAPE;
+  if (ws_needed(L, 1, k) > kStaticScratchBytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  moe_status_t st = moe_check_device();
+  if (st != MOE_OK) return st;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    if (!g_static_ptr[dev]) {
+      // host code only sees a stand-in for the symbol; the kernel needs its device address
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+      g_static_ptr[dev] = p;
+    }
+    scratch = g_static_ptr[dev];
+  }
+  // every call shares the array: clear the counters and status word the kernel expects to start at zero
+  if (cudaMemsetAsync(scratch, 0, kWsCounters, (cudaStream_t)stream) != cudaSuccess) return MOE_ERR_CUDA;
+  return ffn_common("decode", L, x_bf16, 1, idx, w, k, y, y_bf16, accumulate, scratch, kStaticScratchBytes, stream);
 }

@@ -159,6 +159,20 @@ moe_status_t moe_expert_ffn_verify(const moe_layer_t* layer, const void* x_bf16,
                                    const float* w, int32_t k, float* y, void* y_bf16, int32_t accumulate, void* ws,
                                    size_t ws_bytes, void* stream);
 
+/* Decode of one token exactly like moe_expert_ffn_decode, but without a workspace argument: its scratch is a
+ * fixed array of 2,101,248 bytes inside the library (one per GPU that loads it, kept until the process exits).
+ * The pages have no counterpart; it exists for callers that cannot allocate device memory (a plugin given only
+ * its input and output buffers, code under a memory budget owned by another allocator).
+ *   Limits: k <= 8 and H, I <= 4096 (MOE_ERR_WORKSPACE_TOO_SMALL / MOE_ERR_SHAPE otherwise). It calls no
+ *   allocation routine. The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ *   with that device current; make that first call before any stream capture.
+ *   Every call shares the array and clears its counters and status word first (an asynchronous memset on
+ *   `stream`), so device-side errors of a call are not kept for later inspection. Calls that overlap on the GPU
+ *   (other streams, other threads) race on the array and must be serialised by the caller. */
+moe_status_t moe_expert_ffn_decode_static(const moe_layer_t* layer, const void* x_bf16, const int32_t* idx,
+                                          const float* w, int32_t k, float* y, void* y_bf16, int32_t accumulate,
+                                          void* stream);
+
 /* ---------------------------------------------------------------- debug (tests only) ----------------------------- */
 
 /* Unpack expert `expert` of a packed matrix back to fp32 values [rows, K] (rows = I for each of gate and up,
