@@ -37,7 +37,6 @@ constexpr int kNR = 4;                 // reduction slots between consumers and 
 constexpr int kMaxT = 8;
 constexpr int kMaxK = 8;
 constexpr int kMaxU = kMaxT * kMaxK;   // 64
-constexpr int kMaxRowTiles = 4096 / 16;
 
 // workspace: [header 256][cnt_g 64 u32][amax_h 64*8 u32] -> 4096 bytes, then h [U, 8, I] and d [U, H, 8] fp32
 constexpr size_t kWsCounters = 4096;
@@ -270,58 +269,85 @@ __global__ void __launch_bounds__(Cfg<FMT>::THREADS, 1) ffn_kernel(const FfnArgs
   const int T = a.T, k = a.k, H = a.H, I = a.I;
   const int n_ent = T * k;
 
-  // ---------------- prologue: barriers, union of the tokens' experts (sorted, deduplicated), weight sums
+  // ---------------- prologue
+  // Consumers start fetching their x fragments at once (they do not depend on the routing); the producer warp
+  // forms the union of the tokens' experts (sorted, deduplicated) and the per-token weight sums meanwhile.
+  uint32_t bx[C::NCH][F::STEPS][2];
+  float xmax = 0.f;
+  if (warp < C::CW) {
+    const int col = lane >> 2, q = lane & 3, ncg0 = H / F::CK;
+#pragma unroll
+    for (int n = 0; n < C::NCH; ++n) {
+      const int c = warp + C::CW * n;
+#pragma unroll
+      for (int j = 0; j < F::STEPS; ++j) {
+        uint32_t v0 = 0, v1 = 0;
+        if (c < ncg0 && col < T) {
+          const int k0 = c * F::CK + 16 * j + 2 * q;
+          const uint16_t* xr = a.x + (size_t)col * H;
+          v0 = __ldg(reinterpret_cast<const uint32_t*>(xr + k0));
+          v1 = __ldg(reinterpret_cast<const uint32_t*>(xr + k0 + 8));
+        }
+        bx[n][j][0] = v0;
+        bx[n][j][1] = v1;
+      }
+    }
+  }
   if (tid == 0) {
     for (int s = 0; s < C::NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], C::CW); }
     for (int s = 0; s < kNR; ++s) { mbar_init(&redfull[s], C::CW); mbar_init(&redempty[s], 1); }
     fence_mbar_init();
     s_abort = 0;
   }
-  for (int i = tid; i < kMaxT * kMaxU; i += blockDim.x) {
-    (&s_wsum[0][0])[i] = 0.f;
-    (&s_routed[0][0])[i] = 0;
-  }
-  if (tid < n_ent) s_val[tid] = a.idx[tid];
-  __syncthreads();
-  if (tid < n_ent) {
-    const int v = s_val[tid];
-    int first = 1;
-    for (int j = 0; j < tid; ++j) first &= (s_val[j] != v);
-    s_first[tid] = first;
-    if (v < 0 || v >= a.E) { s_abort = 1; if (blockIdx.x == 0) record_error(&a.hdr->status, MOE_ERR_INVALID_ARG); }
-  }
-  __syncthreads();
-  if (tid < n_ent) {
-    const int v = s_val[tid];
-    int rank = 0, nfirst = 0;
-    for (int j = 0; j < n_ent; ++j) {
-      rank += (s_first[j] && s_val[j] < v) ? 1 : 0;
-      nfirst += s_first[j];
+  if (warp == C::PROD) {
+    int bad = 0;
+    for (int i = lane; i < n_ent; i += 32) {
+      const int v = a.idx[i];
+      s_val[i] = v;
+      bad |= (v < 0 || v >= a.E);
     }
-    s_slot[tid] = rank;
-    if (s_first[tid]) s_union[rank] = v;
-    if (tid == 0) s_U = nfirst;
-    // rank order, so a token's weight sums do not depend on the other tokens
-    if (tid % k == 0) {
-      const int t = tid / k;
+    for (int i = lane; i < T * kMaxU; i += 32) {
+      (&s_wsum[0][0])[i] = 0.f;
+      (&s_routed[0][0])[i] = 0;
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    __syncwarp();
+    for (int i = lane; i < n_ent; i += 32) {
+      const int v = s_val[i];
+      int first = 1;
+      for (int j = 0; j < i; ++j) first &= (s_val[j] != v);
+      s_first[i] = first;
+    }
+    __syncwarp();
+    int nfirst = 0;
+    for (int i = lane; i < n_ent; i += 32) {
+      const int v = s_val[i];
+      int rank = 0;
+      for (int j = 0; j < n_ent; ++j) rank += (s_first[j] && s_val[j] < v) ? 1 : 0;
+      s_slot[i] = rank;
+      if (s_first[i]) s_union[rank] = v;
+      nfirst += s_first[i];
+    }
+    nfirst = __reduce_add_sync(0xffffffffu, nfirst);
+    __syncwarp();
+    if (lane < T) {  // rank order, so a token's weight sums do not depend on the other tokens
       for (int r = 0; r < k; ++r) {
-        int rr = 0;
-        const int vv = s_val[t * k + r];
-        for (int j = 0; j < n_ent; ++j) rr += (s_first[j] && s_val[j] < vv) ? 1 : 0;
-        s_wsum[t][rr] += __ldg(&a.w[t * k + r]);
-        s_routed[t][rr] = 1;
+        const int u = s_slot[lane * k + r];
+        s_wsum[lane][u] += __ldg(&a.w[lane * k + r]);
+        s_routed[lane][u] = 1;
       }
+      int n = 0;
+      for (int u = 0; u < nfirst; ++u)
+        if (s_routed[lane][u]) { s_ulist[lane][n] = u; s_uw[lane][n] = s_wsum[lane][u]; ++n; }
+      s_nu[lane] = n;
+    }
+    if (lane == 0) {
+      s_U = nfirst;
+      if (bad) { s_abort = 1; if (blockIdx.x == 0) record_error(&a.hdr->status, MOE_ERR_INVALID_ARG); }
     }
   }
   __syncthreads();
   const int U = s_U;
-  if (tid < T) {
-    int n = 0;
-    for (int u = 0; u < U; ++u)
-      if (s_routed[tid][u]) { s_ulist[tid][n] = u; s_uw[tid][n] = s_wsum[tid][u]; ++n; }
-    s_nu[tid] = n;
-  }
-  // (s_nu / s_ulist are read only by the epilogue warp after the grid barrier, far below)
   const int G = gridDim.x, bid = blockIdx.x;
   const int gt = I / 8, dt = H / 16;  // tiles per expert
   const int64_t NG = (int64_t)U * gt, ND = (int64_t)U * dt;
@@ -483,28 +509,17 @@ __global__ void __launch_bounds__(Cfg<FMT>::THREADS, 1) ffn_kernel(const FfnArgs
       ++ri;
     };
 
-    // ---- phase G: B fragments = x of the T tokens, rescaled per token into fp16
+    // ---- phase G: B fragments = x of the T tokens (fetched in the prologue), rescaled per token into fp16
     {
-      uint32_t bx[C::NCH][F::STEPS][2];
-      float mx = 0.f;
+      float mx = xmax;
 #pragma unroll
-      for (int n = 0; n < C::NCH; ++n) {
-        const int c = warp + C::CW * n;
+      for (int n = 0; n < C::NCH; ++n)
 #pragma unroll
         for (int j = 0; j < F::STEPS; ++j) {
-          uint32_t v0 = 0, v1 = 0;
-          if (c < ncg && col < T) {
-            const int k0 = c * F::CK + 16 * j + 2 * q;
-            const uint16_t* xr = a.x + (size_t)col * H;
-            v0 = __ldg(reinterpret_cast<const uint32_t*>(xr + k0));
-            v1 = __ldg(reinterpret_cast<const uint32_t*>(xr + k0 + 8));
-          }
-          bx[n][j][0] = v0;
-          bx[n][j][1] = v1;
+          const uint32_t v0 = bx[n][j][0], v1 = bx[n][j][1];
           mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf16_bits_to_f32(v0 & 0xFFFFu)), fabsf(bf16_bits_to_f32(v0 >> 16))),
                                fmaxf(fabsf(bf16_bits_to_f32(v1 & 0xFFFFu)), fabsf(bf16_bits_to_f32(v1 >> 16)))));
         }
-      }
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
       if (q == 0) s_colmax[warp][col] = mx;

@@ -54,24 +54,35 @@ route_kernel(const uint16_t* __restrict__ wr, const uint16_t* __restrict__ x, in
 #pragma unroll
     for (int t = 0; t < kRouteTPC; ++t) acc[t] = 0.f;
     const uint16_t* row = wr + (size_t)e * H;
-    for (int h = lane * 8; h < H; h += 256) {
-      const uint4 wv = __ldg(reinterpret_cast<const uint4*>(row + h));
-      const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
-      float wf[8];
+    // the row's 16-byte pieces for this lane, fetched in batches of 8 so the loads are in flight together
+    for (int h0 = lane * 8; h0 < H; h0 += 256 * 8) {
+      uint4 wv[8];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        wf[2 * j] = __half2float(__ushort_as_half((unsigned short)(ww[j] & 0xFFFFu)));
-        wf[2 * j + 1] = __half2float(__ushort_as_half((unsigned short)(ww[j] >> 16)));
+      for (int b = 0; b < 8; ++b) {
+        const int h = h0 + 256 * b;
+        wv[b] = h < H ? __ldg(reinterpret_cast<const uint4*>(row + h)) : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
-      for (int t = 0; t < kRouteTPC; ++t) {
-        if (t < nt) {
-          const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)t * H + h);
-          const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
+      for (int b = 0; b < 8; ++b) {
+        const int h = h0 + 256 * b;
+        if (h >= H) break;
+        const uint32_t ww[4] = {wv[b].x, wv[b].y, wv[b].z, wv[b].w};
+        float wf[8];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            acc[t] = fmaf(wf[2 * j], __uint_as_float(xx[j] << 16), acc[t]);
-            acc[t] = fmaf(wf[2 * j + 1], __uint_as_float(xx[j] & 0xFFFF0000u), acc[t]);
+        for (int j = 0; j < 4; ++j) {
+          wf[2 * j] = __half2float(__ushort_as_half((unsigned short)(ww[j] & 0xFFFFu)));
+          wf[2 * j + 1] = __half2float(__ushort_as_half((unsigned short)(ww[j] >> 16)));
+        }
+#pragma unroll
+        for (int t = 0; t < kRouteTPC; ++t) {
+          if (t < nt) {
+            const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)t * H + h);
+            const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              acc[t] = fmaf(wf[2 * j], __uint_as_float(xx[j] << 16), acc[t]);
+              acc[t] = fmaf(wf[2 * j + 1], __uint_as_float(xx[j] & 0xFFFF0000u), acc[t]);
+            }
           }
         }
       }
