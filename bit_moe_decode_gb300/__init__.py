@@ -29,7 +29,8 @@ BLOCK = {MOE_FMT_MXFP4: (32, 17), MOE_FMT_INT4G32: (32, 18), MOE_FMT_Q2K: (256, 
 EXPORTS = ["moe_status_string", "moe_version", "moe_check_device", "moe_canonical_bytes", "moe_packed_bytes",
            "moe_encode_blocks", "moe_pack_weights", "moe_route_topk", "moe_workspace_bytes", "moe_workspace_init",
            "moe_get_device_status", "moe_expert_ffn_decode", "moe_expert_ffn_verify", "moe_debug_unpack",
-           "moe_debug_timeout_probe", "moe_expert_ffn_decode_static"]
+           "moe_debug_timeout_probe", "moe_expert_ffn_decode_static", "moe_prefill_workspace_bytes",
+           "moe_expert_grouped_gemm_prefill", "moe_debug_prefill"]
 
 
 class MoeError(RuntimeError):
@@ -72,6 +73,9 @@ def lib() -> C.CDLL:
             "moe_debug_unpack": (C.c_int, [C.c_int, C.c_int, C.c_int, P, i64, i64, i64, P, P]),
             "moe_debug_timeout_probe": (C.c_int, [P, sz, i32, P]),
             "moe_expert_ffn_decode_static": (C.c_int, [LP, P, P, P, i32, P, P, i32, P]),
+            "moe_prefill_workspace_bytes": (sz, [LP, i32, i32]),
+            "moe_expert_grouped_gemm_prefill": (C.c_int, [LP, P, i32, P, P, i32, P, P, P, sz, P]),
+            "moe_debug_prefill": (C.c_int, [LP, P, i32, P, P, i32, P, P, P, sz, P, P, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -172,6 +176,30 @@ def moe_expert_ffn_decode_static(layer: "Layer", x_bf16, idx, w, k: int, y, y_bf
            "moe_expert_ffn_decode_static")
 
 
+def moe_prefill_workspace_bytes(layer: "Layer", T_max: int, k: int) -> int:
+    return lib().moe_prefill_workspace_bytes(C.byref(layer.c), T_max, k)
+
+
+def moe_expert_grouped_gemm_prefill(layer: "Layer", x_bf16, T: int, idx, w, k: int, y, y_bf16=None, ws=None,
+                                    stream=None):
+    _check(lib().moe_expert_grouped_gemm_prefill(C.byref(layer.c), _ptr(x_bf16), T, _ptr(idx), _ptr(w), k, _ptr(y),
+                                                 _ptr(y_bf16), _ptr(ws), ws.numel() * ws.element_size(),
+                                                 _stream(stream)), "moe_expert_grouped_gemm_prefill")
+
+
+PREFILL_OFFSETS = ("rows_max", "tiles_max", "n_tiles", "tile_first", "pair_row", "xq", "xsf", "hq", "hsf", "dout")
+
+
+def moe_debug_prefill(layer: "Layer", x_bf16, T: int, idx, w, k: int, y, y_bf16=None, ws=None, gu_dump=None,
+                      stream=None) -> dict:
+    """The prefill call with test hooks; returns the workspace layout (see include/moe.h)."""
+    off = (C.c_int64 * 10)()
+    _check(lib().moe_debug_prefill(C.byref(layer.c), _ptr(x_bf16), T, _ptr(idx), _ptr(w), k, _ptr(y), _ptr(y_bf16),
+                                   _ptr(ws), ws.numel() * ws.element_size(), _ptr(gu_dump), off, _stream(stream)),
+           "moe_debug_prefill")
+    return dict(zip(PREFILL_OFFSETS, list(off)))
+
+
 def moe_debug_unpack(fmt: int, layout: int, kind: int, packed: torch.Tensor, H: int, I: int, expert: int,
                      out: torch.Tensor, stream=None):
     _check(lib().moe_debug_unpack(fmt, layout, kind, _ptr(packed), H, I, expert, _ptr(out), _stream(stream)),
@@ -208,7 +236,11 @@ class Layer:
         moe_pack_weights(self.fmt, src_kind, self.layout, MOE_MAT_DOWN, n, self.H, self.I, down, None, dsl, stream)
 
     def workspace(self, T_max: int, k: int, stream=None) -> torch.Tensor:
-        nbytes = moe_workspace_bytes(self, T_max, k)
+        """Decode/verify workspace for DECODE-layout layers, prefill workspace for PREFILL-layout layers."""
+        if self.layout == MOE_LAYOUT_PREFILL:
+            nbytes = moe_prefill_workspace_bytes(self, T_max, k)
+        else:
+            nbytes = moe_workspace_bytes(self, T_max, k)
         if nbytes == 0:
             raise MoeError(2, "moe_workspace_bytes")
         ws = torch.empty(nbytes + 256, dtype=torch.uint8, device=self.gate_up.device)

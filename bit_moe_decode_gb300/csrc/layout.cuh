@@ -1,4 +1,6 @@
-// layout.cuh -- the packed device layout of expert weights (MOE_LAYOUT_DECODE).
+// layout.cuh -- the packed device layouts of expert weights.
+//
+// ---- MOE_LAYOUT_DECODE (all three formats; the mat-vec kernels of ffn.cu)
 //
 // A matrix is cut into TILES of 16 rows x K and each tile into CHUNKS of 16 rows x CK columns along K.
 //   Gate/Up: tile j holds gate rows 8j..8j+7 (tile rows 0..7) and up rows 8j..8j+7 (tile rows 8..15), so one
@@ -67,6 +69,39 @@ __host__ __device__ inline CodePos code_pos(int fmt, int tr, int k) {
   p.reg = (tr >= 8 ? 1 : 0) + (ks >= 8 ? 2 : 0);
   p.lane = (tr % 8) * 4 + q;
   return p;
+}
+
+// ---- MOE_LAYOUT_PREFILL (MXFP4; operands of the block-scaled tcgen05 MMA, loaded by TMA tensor copies)
+// Per expert, a matrix of R rows x K is stored as
+//   codes  [R][K/2] bytes: element k of a row in byte k/2, even k in the LOW nibble (the order in which the TMA
+//          engine's 16U4_ALIGN16B type unpacks E2M1 codes into the MMA's shared-memory operand);
+//   scales [R/128][K/128][512] bytes: for each 128-row x 128-column tile, the 4 x 128 E8M0 exponents permuted so
+//          that byte (l*16 + c*4 + kb) is the exponent of tile row (l + 32c), 32-block kb; tcgen05.cp
+//          .32x128b.warpx4 copies this block into the four TMEM scale columns the MMA reads.
+//   GATE_UP: R = 2I, K = H; 128-row tile b = gate rows 64b..64b+63 followed by up rows 64b..64b+63, so one
+//            128-column accumulator tile holds g and u of the same 64 intermediate indices.
+//   DOWN:    R = H, K = I.
+// The per-expert stride R*K*17/32 equals the canonical size (same bits per weight).
+struct TcGeom {
+  int64_t R, K, codes, stride;  // rows, columns, bytes of codes, bytes per expert
+};
+__host__ __device__ inline TcGeom tc_geom(int kind, int64_t H, int64_t I) {
+  TcGeom g;
+  g.R = kind == MOE_MAT_GATE_UP ? 2 * I : H;
+  g.K = kind == MOE_MAT_GATE_UP ? H : I;
+  g.codes = g.R * g.K / 2;
+  g.stride = g.codes + g.R * g.K / 32;
+  return g;
+}
+// storage row of canonical row `row` of matrix mi (0 = gate / down, 1 = up)
+__host__ __device__ inline int64_t tc_row(int kind, int mi, int64_t row) {
+  if (kind != MOE_MAT_GATE_UP) return row;
+  return (row / 64) * 128 + mi * 64 + row % 64;
+}
+// byte offset (inside one expert) of the exponent of storage row r, 32-block blk
+__host__ __device__ inline int64_t tc_scale_off(const TcGeom& g, int64_t r, int64_t blk) {
+  const int64_t tile = r / 128, rr = r % 128, kg = blk / 4, kb = blk % 4;
+  return g.codes + (tile * (g.K / 128) + kg) * 512 + (rr % 32) * 16 + (rr / 32) * 4 + kb;
 }
 
 }  // namespace moe

@@ -270,6 +270,52 @@ __global__ void unpack_kernel(moe_matrix_t kind, int64_t H, int64_t I, const uin
   }
 }
 
+// Tensor-core layout (MXFP4 only): one thread per canonical block writes its 16 code bytes (nibbles swapped to
+// even-k-low) and its exponent; every byte of the destination is written exactly once.
+__global__ void pack_tc_kernel(moe_src_t skind, moe_matrix_t kind, int64_t n_e, int64_t H, int64_t I,
+                               const void* src_a, const void* src_b, uint8_t* dst) {
+  const TcGeom g = tc_geom(kind, H, I);
+  const int64_t K = g.K, rows = kind == MOE_MAT_GATE_UP ? I : H, nmat = kind == MOE_MAT_GATE_UP ? 2 : 1;
+  const int64_t bpr = K / 32;
+  const int64_t total = n_e * nmat * rows * bpr;
+  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total; t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t bk = t % bpr, row = (t / bpr) % rows, mi = (t / bpr / rows) % nmat, e = t / bpr / rows / nmat;
+    uint8_t blk[17];
+    get_block<MOE_FMT_MXFP4>(mi == 0 ? src_a : src_b, skind, (e * rows + row) * bpr + bk, blk);
+    uint8_t* base = dst + e * g.stride;
+    const int64_t r = tc_row(kind, (int)mi, row);
+    uint32_t words[4];
+    for (int w = 0; w < 4; ++w) {
+      uint32_t v = 0;
+      for (int b = 0; b < 4; ++b) {
+        const uint32_t c = blk[1 + w * 4 + b];
+        v |= (((c >> 4) | ((c & 15) << 4)) & 255u) << (8 * b);  // canonical: even k high -> here: even k low
+      }
+      words[w] = v;
+    }
+    *reinterpret_cast<uint4*>(base + r * (K / 2) + bk * 16) = make_uint4(words[0], words[1], words[2], words[3]);
+    base[tc_scale_off(g, r, bk)] = blk[0];
+  }
+}
+
+__global__ void unpack_tc_kernel(moe_matrix_t kind, int64_t H, int64_t I, const uint8_t* packed, int64_t e, float* out) {
+  const TcGeom g = tc_geom(kind, H, I);
+  const int64_t K = g.K, rows = kind == MOE_MAT_GATE_UP ? I : H, nmat = kind == MOE_MAT_GATE_UP ? 2 : 1;
+  const int64_t total = nmat * rows * K;
+  const uint8_t* base = packed + e * g.stride;
+  const float tab[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
+  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total; t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t k = t % K, row = (t / K) % rows, mi = t / K / rows;
+    const int64_t r = tc_row(kind, (int)mi, row);
+    const uint8_t byte = base[r * (K / 2) + k / 2];
+    const int code = (k % 2 == 0) ? (byte & 15) : (byte >> 4);
+    const uint8_t ex = base[tc_scale_off(g, r, k / 32)];
+    const float s = ex == 255 ? __int_as_float(0x7fc00000) : __uint_as_float((uint32_t)ex << 23);
+    const float m = tab[code & 7] * s;
+    out[t] = (code & 8) ? -m : m;
+  }
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -283,7 +329,10 @@ extern "C" size_t moe_packed_bytes(moe_format_t fmt, moe_layout_t layout, moe_ma
                                    int64_t I) {
   if (fmt < MOE_FMT_MXFP4 || fmt > MOE_FMT_Q2K || n_e < 0) return 0;
   if (!moe_internal::shape_ok(H, I)) return 0;
-  if (layout == MOE_LAYOUT_PREFILL) return moe_internal::prefill_packed_bytes(fmt, kind, n_e, H, I);
+  if (layout == MOE_LAYOUT_PREFILL) {
+    if (fmt != MOE_FMT_MXFP4 || (kind != MOE_MAT_GATE_UP && kind != MOE_MAT_DOWN)) return 0;
+    return (size_t)(n_e * tc_geom(kind, H, I).stride);
+  }
   if (layout != MOE_LAYOUT_DECODE) return 0;
   int64_t s = kind == MOE_MAT_GATE_UP ? gate_up_stride(fmt, H, I) : down_stride(fmt, H, I);
   return (size_t)(n_e * s);
@@ -326,15 +375,18 @@ extern "C" moe_status_t moe_pack_weights(moe_format_t fmt, moe_src_t src_kind, m
   if (!src_a || !dst || (kind == MOE_MAT_GATE_UP && !src_b)) return MOE_ERR_INVALID_ARG;
   if (((uintptr_t)dst & 15) != 0) return MOE_ERR_INVALID_ARG;
   if (n_e < 1 || !moe_internal::shape_ok(H, I)) return MOE_ERR_SHAPE;
-  if (layout == MOE_LAYOUT_PREFILL) {
-    return moe_internal::pack_prefill(fmt, src_kind, kind, n_e, H, I, src_a, src_b, dst, dst_bytes, stream);
-  }
-  if (layout != MOE_LAYOUT_DECODE) return MOE_ERR_INVALID_ARG;
+  if (layout != MOE_LAYOUT_DECODE && layout != MOE_LAYOUT_PREFILL) return MOE_ERR_INVALID_ARG;
+  if (layout == MOE_LAYOUT_PREFILL && fmt != MOE_FMT_MXFP4) return MOE_ERR_UNSUPPORTED_FORMAT;
   size_t need = moe_packed_bytes(fmt, layout, kind, n_e, H, I);
   if (dst_bytes < need) return MOE_ERR_INVALID_ARG;
   moe_status_t st = moe_check_device();
   if (st != MOE_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
+  if (layout == MOE_LAYOUT_PREFILL) {
+    const int64_t nblk = n_e * (kind == MOE_MAT_GATE_UP ? 2 * I * (H / 32) : H * (I / 32));
+    pack_tc_kernel<<<grid_for(nblk, 128), 128, 0, s>>>(src_kind, kind, n_e, H, I, src_a, src_b, (uint8_t*)dst);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  }
   if (cudaMemsetAsync(dst, 0, need, s) != cudaSuccess) return MOE_ERR_CUDA;
   int64_t K = kind == MOE_MAT_GATE_UP ? H : I, rows = kind == MOE_MAT_GATE_UP ? I : H;
   int64_t nmat = kind == MOE_MAT_GATE_UP ? 2 : 1;
@@ -359,12 +411,17 @@ extern "C" moe_status_t moe_debug_unpack(moe_format_t fmt, moe_layout_t layout, 
   if (fmt < MOE_FMT_MXFP4 || fmt > MOE_FMT_Q2K) return MOE_ERR_UNSUPPORTED_FORMAT;
   if (!packed || !out || expert < 0) return MOE_ERR_INVALID_ARG;
   if (!moe_internal::shape_ok(H, I)) return MOE_ERR_SHAPE;
-  if (layout == MOE_LAYOUT_PREFILL) return moe_internal::unpack_prefill(fmt, kind, packed, H, I, expert, out, stream);
+  if (layout != MOE_LAYOUT_DECODE && layout != MOE_LAYOUT_PREFILL) return MOE_ERR_INVALID_ARG;
+  if (layout == MOE_LAYOUT_PREFILL && fmt != MOE_FMT_MXFP4) return MOE_ERR_UNSUPPORTED_FORMAT;
   moe_status_t st = moe_check_device();
   if (st != MOE_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
   int64_t total = (kind == MOE_MAT_GATE_UP ? 2 * I * H : H * I);
   int thr = 256;
+  if (layout == MOE_LAYOUT_PREFILL) {
+    unpack_tc_kernel<<<grid_for(total, thr), thr, 0, s>>>(kind, H, I, (const uint8_t*)packed, expert, out);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  }
   switch (fmt) {
     case MOE_FMT_MXFP4: unpack_kernel<MOE_FMT_MXFP4><<<grid_for(total, thr), thr, 0, s>>>(kind, H, I, (const uint8_t*)packed, expert, out); break;
     case MOE_FMT_INT4G32: unpack_kernel<MOE_FMT_INT4G32><<<grid_for(total, thr), thr, 0, s>>>(kind, H, I, (const uint8_t*)packed, expert, out); break;

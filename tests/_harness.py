@@ -43,9 +43,9 @@ class Weights:
         return oracle.encode(fmt, self.f32(e, which))
 
 
-def make_layer(m, fmt: int, W: Weights, E: int, experts, dev) -> "m.Layer":
+def make_layer(m, fmt: int, W: Weights, E: int, experts, dev, layout: int = 0) -> "m.Layer":
     """Device layer with E expert slots; the listed experts are packed from fp32 on the GPU."""
-    layer = m.Layer(fmt, W.H, W.I, E, device=dev)
+    layer = m.Layer(fmt, W.H, W.I, E, layout=layout, device=dev)
     for e in sorted(set(int(v) for v in experts)):
         g = torch.from_numpy(W.f32(e, 0)).to(dev)[None]
         u = torch.from_numpy(W.f32(e, 1)).to(dev)[None]
