@@ -38,6 +38,9 @@ def parse():
     p.add_argument("--seed", type=int, default=1)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
+    p.add_argument("--experts", type=int, default=E, help="expert slots of the layer (smaller only for profiling)")
+    p.add_argument("--prefill-tokens", type=int, default=4096,
+                   help="tokens of the prefill grouped-GEMM measurement (MXFP4 only; 0 = skip)")
     return p.parse_args()
 
 
@@ -119,9 +122,12 @@ def run_ours(args):
         raise RuntimeError("libmoe: device is not sm_103")
     fmt = FMT_IDS[args.fmt]
     T = args.tokens
+    E = args.experts
+    do_prefill = args.prefill_tokens > 0 and fmt == 1
 
     # ---- weights: seeded fp32 -> packed on the GPU by the library's encoder (replica per rank, same weights)
     layer = m.Layer(fmt, H, I, E, device=dev)
+    layer_p = m.Layer(fmt, H, I, E, layout=m.MOE_LAYOUT_PREFILL, device=dev) if do_prefill else None
     t0 = time.time()
     batch = 16
     pool = cf.ThreadPoolExecutor(2)
@@ -135,8 +141,10 @@ def run_ours(args):
         g, u, d = fut.result()
         if e0 + batch < E:
             fut = pool.submit(gen, e0 + batch)
-        layer.pack(m.MOE_SRC_F32, torch.from_numpy(g).to(dev), torch.from_numpy(u).to(dev),
-                   torch.from_numpy(d).to(dev), e0=e0)
+        gd, ud, dd = torch.from_numpy(g).to(dev), torch.from_numpy(u).to(dev), torch.from_numpy(d).to(dev)
+        layer.pack(m.MOE_SRC_F32, gd, ud, dd, e0=e0)
+        if layer_p is not None:
+            layer_p.pack(m.MOE_SRC_F32, gd, ud, dd, e0=e0)
     torch.cuda.synchronize()
     setup_s = time.time() - t0
 
@@ -278,6 +286,8 @@ def run_ours(args):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_ms = float(tt.item())
 
+    prefill = bench_prefill(m, torch, args, dev, stream, layer_p, E) if do_prefill else None
+
     out = None
     if rank == 0:
         peaks = measured_peaks()
@@ -310,12 +320,66 @@ def run_ours(args):
             "e2e": {"value": round(world * T / (e2e_ms * 1e-3), 1), "unit": "tok/s",
                     "h2d_bytes_per_step": int(T * H * 2), "d2h_bytes_per_step": int(T * H * 4)},
             "clocks": clk,
+            "prefill": prefill,
             "setup_s": round(setup_s, 1),
             "cuda_graph": use_graph,
         }
     if dist:
         dist.destroy_process_group()
     return out
+
+
+def bench_prefill(m, torch, args, dev, stream, layer_p, E):
+    """Prefill grouped GEMM: args.prefill_tokens tokens, top-6 with Zipf(1.1) expert popularity, one call per step.
+    Tensor roofline: useful FLOPs (pairs x 3 matrices x 2 H I) / call time against the fp8-rate tensor peak
+    (measured bf16 dense peak x 2, the nominal fp8 / bf16 ratio; mxf8f6f4 MMAs run at the fp8 rate)."""
+    from moe_inputs import x_bf16_bits, zipf_routing
+    Tp = args.prefill_tokens
+    xp = torch.from_numpy(x_bf16_bits(args.seed + 17, range(Tp), H).view(np.int16)).to(dev)
+    ip, wp = zipf_routing(args.seed, Tp, E, K_TOP)
+    idx_p = torch.from_numpy(ip).to(dev)
+    w_p = torch.from_numpy(wp).to(dev)
+    ws_p = layer_p.workspace(Tp, K_TOP, stream=stream)
+    y_p = torch.empty((Tp, H), dtype=torch.float32, device=dev)
+    yb_p = torch.empty((Tp, H), dtype=torch.int16, device=dev)
+
+    def call():
+        m.moe_expert_grouped_gemm_prefill(layer_p, xp, Tp, idx_p, w_p, K_TOP, y_p, yb_p, ws_p, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        call()
+    stream.synchronize()
+    if m.moe_get_device_status(ws_p, stream) != 0:
+        raise RuntimeError("device status after prefill warm-up")
+    reps = max(3, args.steps)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        call()
+    e1.record(stream)
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    if m.moe_get_device_status(ws_p, stream) != 0:
+        raise RuntimeError("device status after prefill")
+    counts = np.bincount(ip.reshape(-1), minlength=E)
+    pairs = int(counts.sum())
+    flops = pairs * 3 * 2.0 * H * I
+    wbytes = int(np.count_nonzero(counts)) * (m.moe_packed_bytes(1, 1, 0, 1, H, I) + m.moe_packed_bytes(1, 1, 1, 1, H, I))
+    peaks = measured_peaks()
+    bf16 = float(peaks["bf16_tflops"]) if peaks and "bf16_tflops" in peaks else None
+    peak = 2.0 * bf16 if bf16 else 3800.0
+    hbm = float(peaks["hbm_gbs"]) if peaks else 6800.0
+    tflops = flops / (ms * 1e-3) / 1e12
+    return {"workload": "prefill of %d tokens, top-6, Zipf(1.1) expert popularity over %d experts (%d pairs, "
+                        "%d tiles of 128)" % (Tp, E, pairs, int(np.sum((counts + 127) // 128))),
+            "tok_s": round(Tp / (ms * 1e-3), 1), "ms_per_call": round(ms, 4), "calls": reps,
+            "gpu_launches_per_call": 7,
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
+                         "frac": round(tflops / peak, 4), "traffic": None,
+                         "peak_source": ("MEASURED_PEAKS.json bf16_tflops x 2 (fp8 rate; of measured)" if bf16
+                                         else "fallback 1900 bf16 x 2")},
+            "weight_bytes": wbytes, "weight_gbs": round(wbytes / (ms * 1e-3) / 1e9, 1),
+            "weight_frac_of_hbm": round(wbytes / (ms * 1e-3) / 1e9 / hbm, 4)}
 
 
 # ------------------------------------------------------------------------------------------------ CPU oracle

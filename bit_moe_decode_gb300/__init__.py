@@ -16,7 +16,8 @@ LIB_PATH = os.path.join(_HERE, "libmoe.so")
 
 MOE_FMT_MXFP4, MOE_FMT_INT4G32, MOE_FMT_Q2K = 1, 2, 3
 MOE_SRC_BLOCKS, MOE_SRC_F32 = 0, 1
-MOE_LAYOUT_DECODE, MOE_LAYOUT_PREFILL = 0, 1
+MOE_LAYOUT_DECODE, MOE_LAYOUT_TC = 0, 1
+MOE_LAYOUT_PREFILL = MOE_LAYOUT_TC
 MOE_MAT_GATE_UP, MOE_MAT_DOWN = 0, 1
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_SHAPE", 3: "MOE_ERR_UNSUPPORTED_FORMAT",
@@ -187,13 +188,13 @@ def moe_expert_grouped_gemm_prefill(layer: "Layer", x_bf16, T: int, idx, w, k: i
                                                  _stream(stream)), "moe_expert_grouped_gemm_prefill")
 
 
-PREFILL_OFFSETS = ("rows_max", "tiles_max", "n_tiles", "tile_first", "pair_row", "xq", "xsf", "hq", "hsf", "dout")
+PREFILL_OFFSETS = ("rows_max", "tiles_max", "n_tiles", "tile_first", "pair_row", "xq", "hq", "dout")
 
 
 def moe_debug_prefill(layer: "Layer", x_bf16, T: int, idx, w, k: int, y, y_bf16=None, ws=None, gu_dump=None,
                       stream=None) -> dict:
     """The prefill call with test hooks; returns the workspace layout (see include/moe.h)."""
-    off = (C.c_int64 * 10)()
+    off = (C.c_int64 * 8)()
     _check(lib().moe_debug_prefill(C.byref(layer.c), _ptr(x_bf16), T, _ptr(idx), _ptr(w), k, _ptr(y), _ptr(y_bf16),
                                    _ptr(ws), ws.numel() * ws.element_size(), _ptr(gu_dump), off, _stream(stream)),
            "moe_debug_prefill")

@@ -71,26 +71,29 @@ __host__ __device__ inline CodePos code_pos(int fmt, int tr, int k) {
   return p;
 }
 
-// ---- MOE_LAYOUT_PREFILL (MXFP4; operands of the block-scaled tcgen05 MMA, loaded by TMA tensor copies)
-// Per expert, a matrix of R rows x K is stored as
-//   codes  [R][K/2] bytes: element k of a row in byte k/2, even k in the LOW nibble (the order in which the TMA
+// ---- MOE_LAYOUT_TC (MXFP4; operands of the block-scaled tcgen05 MMA, used by prefill, decode and verify)
+// A matrix of R rows x K per expert is cut into 128 x 128 tiles, stored tile-major (row tile rt, then column
+// tile kt); every tile is one contiguous run of 8704 bytes:
+//   codes  [128 rows][64 B]: element k of a row in byte k/2, even k in the LOW nibble (the order in which the TMA
 //          engine's 16U4_ALIGN16B type unpacks E2M1 codes into the MMA's shared-memory operand);
-//   scales [R/128][K/128][512] bytes: for each 128-row x 128-column tile, the 4 x 128 E8M0 exponents permuted so
-//          that byte (l*16 + c*4 + kb) is the exponent of tile row (l + 32c), 32-block kb; tcgen05.cp
-//          .32x128b.warpx4 copies this block into the four TMEM scale columns the MMA reads.
-//   GATE_UP: R = 2I, K = H; 128-row tile b = gate rows 64b..64b+63 followed by up rows 64b..64b+63, so one
+//   scales [512 B] at +8192: the 4 x 128 E8M0 exponents permuted so that byte (l*16 + c*4 + kb) is the exponent of
+//          tile row (l + 32c), 32-block kb; tcgen05.cp .32x128b.warpx4 copies it into four TMEM scale columns.
+// One pipeline stage of the GEMM kernels reads exactly one tile, so weight reads are 8.5 KB sequential runs.
+//   GATE_UP: R = 2I, K = H; row tile b = gate rows 64b..64b+63 followed by up rows 64b..64b+63, so one
 //            128-column accumulator tile holds g and u of the same 64 intermediate indices.
 //   DOWN:    R = H, K = I.
 // The per-expert stride R*K*17/32 equals the canonical size (same bits per weight).
+constexpr int64_t kTcTileBytes = 8704;
 struct TcGeom {
-  int64_t R, K, codes, stride;  // rows, columns, bytes of codes, bytes per expert
+  int64_t R, K, RT, KT, stride;  // rows, columns, row tiles, column tiles, bytes per expert
 };
 __host__ __device__ inline TcGeom tc_geom(int kind, int64_t H, int64_t I) {
   TcGeom g;
   g.R = kind == MOE_MAT_GATE_UP ? 2 * I : H;
   g.K = kind == MOE_MAT_GATE_UP ? H : I;
-  g.codes = g.R * g.K / 2;
-  g.stride = g.codes + g.R * g.K / 32;
+  g.RT = g.R / 128;
+  g.KT = g.K / 128;
+  g.stride = g.RT * g.KT * kTcTileBytes;
   return g;
 }
 // storage row of canonical row `row` of matrix mi (0 = gate / down, 1 = up)
@@ -98,10 +101,17 @@ __host__ __device__ inline int64_t tc_row(int kind, int mi, int64_t row) {
   if (kind != MOE_MAT_GATE_UP) return row;
   return (row / 64) * 128 + mi * 64 + row % 64;
 }
-// byte offset (inside one expert) of the exponent of storage row r, 32-block blk
-__host__ __device__ inline int64_t tc_scale_off(const TcGeom& g, int64_t r, int64_t blk) {
-  const int64_t tile = r / 128, rr = r % 128, kg = blk / 4, kb = blk % 4;
-  return g.codes + (tile * (g.K / 128) + kg) * 512 + (rr % 32) * 16 + (rr / 32) * 4 + kb;
+// byte offset (inside one expert) of the tile holding storage row r, column k
+__host__ __device__ inline int64_t tc_tile_off(const TcGeom& g, int64_t r, int64_t k) {
+  return ((r / 128) * g.KT + k / 128) * kTcTileBytes;
+}
+// byte offset of the code byte of (storage row r, column k) and of the exponent of (r, 32-block of k)
+__host__ __device__ inline int64_t tc_code_off(const TcGeom& g, int64_t r, int64_t k) {
+  return tc_tile_off(g, r, k) + (r % 128) * 64 + (k % 128) / 2;
+}
+__host__ __device__ inline int64_t tc_scale_off(const TcGeom& g, int64_t r, int64_t k) {
+  const int64_t rr = r % 128, kb = (k % 128) / 32;
+  return tc_tile_off(g, r, k) + 8192 + (rr % 32) * 16 + (rr / 32) * 4 + kb;
 }
 
 }  // namespace moe

@@ -293,8 +293,8 @@ __global__ void pack_tc_kernel(moe_src_t skind, moe_matrix_t kind, int64_t n_e, 
       }
       words[w] = v;
     }
-    *reinterpret_cast<uint4*>(base + r * (K / 2) + bk * 16) = make_uint4(words[0], words[1], words[2], words[3]);
-    base[tc_scale_off(g, r, bk)] = blk[0];
+    *reinterpret_cast<uint4*>(base + tc_code_off(g, r, bk * 32)) = make_uint4(words[0], words[1], words[2], words[3]);
+    base[tc_scale_off(g, r, bk * 32)] = blk[0];
   }
 }
 
@@ -307,9 +307,9 @@ __global__ void unpack_tc_kernel(moe_matrix_t kind, int64_t H, int64_t I, const 
   for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total; t += (int64_t)gridDim.x * blockDim.x) {
     const int64_t k = t % K, row = (t / K) % rows, mi = t / K / rows;
     const int64_t r = tc_row(kind, (int)mi, row);
-    const uint8_t byte = base[r * (K / 2) + k / 2];
+    const uint8_t byte = base[tc_code_off(g, r, k)];
     const int code = (k % 2 == 0) ? (byte & 15) : (byte >> 4);
-    const uint8_t ex = base[tc_scale_off(g, r, k / 32)];
+    const uint8_t ex = base[tc_scale_off(g, r, k)];
     const float s = ex == 255 ? __int_as_float(0x7fc00000) : __uint_as_float((uint32_t)ex << 23);
     const float m = tab[code & 7] * s;
     out[t] = (code & 8) ? -m : m;

@@ -42,6 +42,7 @@ constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;       // accumulators at columns 0 and 128, scale columns from 256
 constexpr uint32_t SF_COL0 = 256;
 constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+constexpr int ACT_TILE = A_BYTES + SF_BYTES;  // one 128-row x 128-column activation tile: codes, then exponents
 constexpr int PLACE_CHUNK = 256;          // pairs per CTA of the counting sort
 constexpr int MAX_E = 1024;
 
@@ -50,7 +51,7 @@ enum { GATE_UP = 0, DOWN = 1 };
 // ------------------------------------------------------------------ workspace layout (byte offsets)
 struct Plan {
   int64_t npairs, tiles_max, rows_max, nchunks;
-  int64_t o_cnt, o_tstart, o_chist, o_tile_e, o_tile_n, o_tile_c0, o_pslot, o_xq, o_xsf, o_hq, o_hsf, o_dout, total;
+  int64_t o_cnt, o_tstart, o_chist, o_tile_e, o_tile_n, o_tile_c0, o_pslot, o_xq, o_hq, o_dout, total;
 };
 // header (status word) 0..255; n_tiles at byte 256
 constexpr int64_t kNTilesOff = 256;
@@ -71,10 +72,8 @@ inline Plan make_plan(int64_t T, int64_t k, int64_t E, int64_t H, int64_t I) {
   p.o_tile_n = o; o = al(o + p.tiles_max * 4);
   p.o_tile_c0 = o; o = al(o + p.tiles_max * 4);
   p.o_pslot = o;  o = al(o + p.npairs * 4);
-  p.o_xq = o;     o = al(o + p.rows_max * H);
-  p.o_xsf = o;    o = al(o + p.tiles_max * (H / 128) * 512);
-  p.o_hq = o;     o = al(o + p.rows_max * I);
-  p.o_hsf = o;    o = al(o + p.tiles_max * (I / 128) * 512);
+  p.o_xq = o;     o = al(o + p.tiles_max * (H / 128) * ACT_TILE);
+  p.o_hq = o;     o = al(o + p.tiles_max * (I / 128) * ACT_TILE);
   p.o_dout = o;   o = al(o + p.npairs * H * 4);
   p.total = o;
   return p;
@@ -117,6 +116,9 @@ __device__ __forceinline__ int quant_block32(const float (&v)[32], uint32_t (&co
 }
 // byte offset of (tile row r, 32-block kb of a 128-column group) inside a permuted 512-byte scale block
 __device__ __forceinline__ int sf_byte(int r, int kb) { return (r & 31) * 16 + (r >> 5) * 4 + kb; }
+// Sorted activation buffers (x, then h) are tile-major like the weights: tile (row tile, 128-column group) is
+// 16 KB of E4M3 codes [128 rows][128] followed by its 512-byte permuted exponent block.
+__device__ __forceinline__ int64_t act_tile(int64_t tile, int KG, int kg) { return (tile * KG + kg) * (int64_t)ACT_TILE; }
 
 // ------------------------------------------------------------------ 1. counting sort of (token, rank) pairs
 __global__ void bucket_hist(const int32_t* idx, int64_t npairs, int E, int32_t* chist, int32_t* status) {
@@ -200,8 +202,7 @@ __global__ void bucket_place(const int32_t* idx, int64_t npairs, int E, const in
 
 // ------------------------------------------------------------------ 2. MXFP8 activations of every pair
 // One warp per pair; lane j quantises 32-blocks j, j+32, ...
-__global__ void quant_x(const uint16_t* x, int k, int64_t npairs, int H, const int32_t* pslot, uint8_t* xq,
-                        uint8_t* xsf) {
+__global__ void quant_x(const uint16_t* x, int k, int64_t npairs, int H, const int32_t* pslot, uint8_t* xq) {
   const int64_t p = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (p >= npairs) return;
@@ -224,25 +225,25 @@ __global__ void quant_x(const uint16_t* x, int k, int64_t npairs, int H, const i
     }
     uint32_t c[8];
     const int e = quant_block32(v, c);
-    uint4* dst = reinterpret_cast<uint4*>(xq + (int64_t)row * H + b * 32);
+    uint8_t* at = xq + act_tile(tile, KG, b / 4);
+    uint4* dst = reinterpret_cast<uint4*>(at + r * 128 + (b % 4) * 32);
     dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
     dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
-    xsf[((int64_t)tile * KG + b / 4) * 512 + sf_byte(r, b % 4)] = (uint8_t)e;
+    at[A_BYTES + sf_byte(r, b % 4)] = (uint8_t)e;
   }
 }
 
 // ------------------------------------------------------------------ 3, 4. the grouped GEMM
 struct GemmArgs {
   const uint8_t* w;           // packed weights of the layer (tensor-core layout)
-  int64_t wstride, wcodes;    // bytes per expert, bytes of codes per expert
+  int64_t wstride;            // bytes per expert
   int K, NB;                  // reduction size; 128-row weight blocks per expert
-  const uint8_t* asf;         // activation scale blocks [tiles][K/128][512]
+  const uint8_t* act;         // sorted activations, tile-major with exponent blocks
   const int32_t* tile_e;
   const int32_t* tile_n;
   const int32_t* tile_c0;
   const uint32_t* n_tiles;
-  uint8_t* hq;                // GATE_UP: MXFP8 h rows [rows][I] and scale blocks [tiles][I/128][512]
-  uint8_t* hsf;
+  uint8_t* hq;                // GATE_UP: MXFP8 h, tile-major like the activations
   float* gu_dump;             // GATE_UP, tests only: fp32 g and u [rows][2I] (NULL in the product path)
   int I;
   float* dout;                // DOWN: fp32 rows [pairs][H] (compact pair order)
@@ -304,16 +305,16 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
       for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         const int tile = (int)(u / a.NB), nb = (int)(u % a.NB);
         const int e = a.tile_e[tile];
-        const uint8_t* wsf = a.w + (int64_t)e * a.wstride + a.wcodes + (int64_t)nb * KG * SF_BYTES;
-        const uint8_t* asf = a.asf + (int64_t)tile * KG * SF_BYTES;
+        const uint8_t* wt = a.w + (int64_t)e * a.wstride + (int64_t)nb * KG * kTcTileBytes;
         for (int kg = 0; kg < KG; ++kg) {
           if (!pf_wait(&empty[stage], ph ^ 1, s_abort, lim)) { ok = false; break; }
           uint8_t* st = smem + stage * STAGE_BYTES;
           mbar_arrive_expect_tx(&full[stage], STAGE_TX);
-          tma_load_2d(st, &tmA, kg * BK, tile * BM, &full[stage]);
-          tma_load_3d(st + A_BYTES, &tmB, kg * BK, nb * BN, e, &full[stage]);
-          bulk_g2s_plain(st + A_BYTES + B_BYTES, asf + kg * SF_BYTES, SF_BYTES, &full[stage]);
-          bulk_g2s_plain(st + A_BYTES + B_BYTES + SF_BYTES, wsf + kg * SF_BYTES, SF_BYTES, &full[stage]);
+          tma_load_3d(st, &tmA, 0, 0, tile * KG + kg, &full[stage]);
+          tma_load_4d(st + A_BYTES, &tmB, 0, 0, nb * KG + kg, e, &full[stage]);
+          bulk_g2s_plain(st + A_BYTES + B_BYTES, a.act + act_tile(tile, KG, kg) + A_BYTES, SF_BYTES, &full[stage]);
+          bulk_g2s_plain(st + A_BYTES + B_BYTES + SF_BYTES, wt + (int64_t)kg * kTcTileBytes + 8192, SF_BYTES,
+                         &full[stage]);
           issued[stage] = (int)ph;
           if (++stage == STAGES) { stage = 0; ph ^= 1; }
         }
@@ -398,10 +399,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
           const int e = quant_block32(h, codes);
           if (valid) {
             const int i0 = nb * 64 + hb * 32;
-            uint4* dst = reinterpret_cast<uint4*>(a.hq + row * a.I + i0);
+            uint8_t* at = a.hq + act_tile(tile, a.I / 128, i0 / 128);
+            uint4* dst = reinterpret_cast<uint4*>(at + r * 128 + i0 % 128);
             dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
             dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-            a.hsf[((int64_t)tile * (a.I / 128) + i0 / 128) * SF_BYTES + sf_byte(r, (i0 % 128) / 32)] = (uint8_t)e;
+            at[A_BYTES + sf_byte(r, (i0 % 128) / 32)] = (uint8_t)e;
             if (a.gu_dump) {
               float* gd = a.gu_dump + row * 2 * a.I;
               for (int c = 0; c < 32; ++c) {
@@ -479,20 +481,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D map over E4M3 rows [rows][K]
-bool map_act(CUtensorMap* m, const void* base, int64_t K, int64_t rows) {
-  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows}, strides[1] = {(cuuint64_t)K};
-  cuuint32_t box[2] = {BK, BM}, es[2] = {1, 1};
-  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+// 3-D map over tile-major E4M3 activations: [n tiles][128 rows][128 B], tile stride ACT_TILE
+bool map_act(CUtensorMap* m, const void* base, int64_t ntiles) {
+  cuuint64_t dims[3] = {128, 128, (cuuint64_t)ntiles}, strides[2] = {128, (cuuint64_t)ACT_TILE};
+  cuuint32_t box[3] = {BK, BM, 1}, es[3] = {1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-// 3-D map over the packed E2M1 codes [E][R][K] (expert stride includes the scale blocks)
-bool map_wgt(CUtensorMap* m, const void* base, int64_t K, int64_t R, int64_t E, int64_t estride) {
-  cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)R, (cuuint64_t)E};
-  cuuint64_t strides[2] = {(cuuint64_t)(K / 2), (cuuint64_t)estride};
-  cuuint32_t box[3] = {BK, BN, 1}, es[3] = {1, 1, 1};
-  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void*>(base), dims, strides, box, es,
+// 4-D map over the E2M1 code tiles of a tensor-core layout matrix: [E][RT*KT tiles][128 rows][64 B]
+bool map_wgt(CUtensorMap* m, const void* base, const TcGeom& g, int64_t E) {
+  cuuint64_t dims[4] = {128, 128, (cuuint64_t)(g.RT * g.KT), (cuuint64_t)E};
+  cuuint64_t strides[3] = {64, (cuuint64_t)kTcTileBytes, (cuuint64_t)g.stride};
+  cuuint32_t box[4] = {BK, BN, 1, 1}, es[4] = {1, 1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4, const_cast<void*>(base), dims, strides, box, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -534,8 +536,8 @@ moe_status_t run(const moe_layer_t* L, const void* x_bf16, int32_t T, const int3
   // tensor maps (host encodes; they travel as __grid_constant__ kernel parameters)
   const TcGeom ggu = tc_geom(MOE_MAT_GATE_UP, H, I), gdn = tc_geom(MOE_MAT_DOWN, H, I);
   CUtensorMap mx, mgu, mh, mdn;
-  if (!map_act(&mx, B + P.o_xq, H, P.rows_max) || !map_wgt(&mgu, L->gate_up, H, ggu.R, E, ggu.stride) ||
-      !map_act(&mh, B + P.o_hq, I, P.rows_max) || !map_wgt(&mdn, L->down, I, gdn.R, E, gdn.stride))
+  if (!map_act(&mx, B + P.o_xq, P.tiles_max * (H / 128)) || !map_wgt(&mgu, L->gate_up, ggu, E) ||
+      !map_act(&mh, B + P.o_hq, P.tiles_max * (I / 128)) || !map_wgt(&mdn, L->down, gdn, E))
     return MOE_ERR_CUDA;
 
   static std::once_flag attr_once;
@@ -553,21 +555,19 @@ moe_status_t run(const moe_layer_t* L, const void* x_bf16, int32_t T, const int3
   bucket_scan<<<1, 1024, 0, s>>>(E, P.nchunks, chist, cnt, tstart, tile_e, tile_n, tile_c0, n_tiles);
   bucket_place<<<nch, PLACE_CHUNK, 0, s>>>(idx, P.npairs, E, chist, tstart, pslot);
   quant_x<<<(int)((P.npairs * 32 + 255) / 256), 256, 0, s>>>((const uint16_t*)x_bf16, k, P.npairs, H, pslot,
-                                                             B + P.o_xq, B + P.o_xsf);
+                                                             B + P.o_xq);
   const int grid = moe_internal::num_sms();
   GemmArgs ga{};
   ga.w = (const uint8_t*)L->gate_up;
   ga.wstride = ggu.stride;
-  ga.wcodes = ggu.codes;
   ga.K = H;
   ga.NB = (int)(ggu.R / BN);
-  ga.asf = B + P.o_xsf;
+  ga.act = B + P.o_xq;
   ga.tile_e = tile_e;
   ga.tile_n = tile_n;
   ga.tile_c0 = tile_c0;
   ga.n_tiles = n_tiles;
   ga.hq = B + P.o_hq;
-  ga.hsf = B + P.o_hsf;
   ga.gu_dump = gu_dump;
   ga.I = I;
   ga.dout = reinterpret_cast<float*>(B + P.o_dout);
@@ -578,10 +578,9 @@ moe_status_t run(const moe_layer_t* L, const void* x_bf16, int32_t T, const int3
   GemmArgs gd = ga;
   gd.w = (const uint8_t*)L->down;
   gd.wstride = gdn.stride;
-  gd.wcodes = gdn.codes;
   gd.K = I;
   gd.NB = (int)(gdn.R / BN);
-  gd.asf = B + P.o_hsf;
+  gd.act = B + P.o_hq;
   gd.gu_dump = nullptr;
   gemm_kernel<DOWN><<<grid, THREADS, SMEM, s>>>(mh, mdn, gd);
   dim3 cg(T, (H / 4 + 255) / 256);
@@ -612,9 +611,8 @@ extern "C" moe_status_t moe_debug_prefill(const moe_layer_t* layer, const void* 
   if (offsets) {
     if (!layer || T < 1 || k < 1) return MOE_ERR_INVALID_ARG;
     const pf::Plan P = pf::make_plan(T, k, layer->E, layer->H, layer->I);
-    const int64_t o[10] = {P.rows_max, P.tiles_max, pf::kNTilesOff, P.o_tile_c0, P.o_pslot,
-                           P.o_xq,     P.o_xsf,     P.o_hq,         P.o_hsf,     P.o_dout};
-    for (int i = 0; i < 10; ++i) offsets[i] = o[i];
+    const int64_t o[8] = {P.rows_max, P.tiles_max, pf::kNTilesOff, P.o_tile_c0, P.o_pslot, P.o_xq, P.o_hq, P.o_dout};
+    for (int i = 0; i < 8; ++i) offsets[i] = o[i];
   }
   return pf::run(layer, x_bf16, T, idx, w, k, y, y_bf16, ws, ws_bytes, gu_dump, stream);
 }

@@ -69,7 +69,9 @@ moe_status_t moe_check_device(void);
 /* ---------------------------------------------------------------- weights ---------------------------------------- */
 
 typedef enum { MOE_SRC_BLOCKS = 0, MOE_SRC_F32 = 1 } moe_src_t;
-typedef enum { MOE_LAYOUT_DECODE = 0, MOE_LAYOUT_PREFILL = 1 } moe_layout_t;
+/* DECODE: the mat-vec layout of the decode / verify kernels (all formats). TC: the tensor-core tile layout (MXFP4
+ * only) read by the prefill grouped GEMM; PREFILL is its older name. */
+typedef enum { MOE_LAYOUT_DECODE = 0, MOE_LAYOUT_TC = 1, MOE_LAYOUT_PREFILL = 1 } moe_layout_t;
 typedef enum { MOE_MAT_GATE_UP = 0, MOE_MAT_DOWN = 1 } moe_matrix_t;
 
 /* Bytes of `rows` x `k` weights in the canonical block format (blocks run along k, row-major). */
@@ -102,10 +104,10 @@ moe_status_t moe_encode_blocks(moe_format_t fmt, const float* src, int64_t rows,
  *   encoded on the fly exactly as moe_encode_blocks does.
  *   dst must be 16-byte aligned and hold moe_packed_bytes(...) bytes.
  * Shapes: H and I multiples of 256 (and of the block size), 256 <= H, I <= 4096.
- * Layout MOE_LAYOUT_PREFILL is MXFP4 only: per expert, codes [R][K/2] (even k in the low nibble) followed by the
- * E8M0 exponents in 512-byte blocks per 128 rows x 128 columns (byte l*16 + c*4 + kb = row l + 32c, 32-block kb);
- * GATE_UP has R = 2I rows ordered in groups of 128 = 64 gate rows then the same 64 up rows, K = H; DOWN has
- * R = H, K = I. */
+ * Layout MOE_LAYOUT_TC is MXFP4 only: per expert, 128 x 128 tiles in (row tile, column tile) order, each 8704
+ * contiguous bytes: codes [128 rows][64 B] (even k in the low nibble), then the 512 E8M0 exponents permuted
+ * (byte l*16 + c*4 + kb = row l + 32c, 32-block kb); GATE_UP has R = 2I rows ordered in groups of 128 = 64 gate
+ * rows then the same 64 up rows, K = H; DOWN has R = H, K = I. */
 moe_status_t moe_pack_weights(moe_format_t fmt, moe_src_t src_kind, moe_layout_t layout, moe_matrix_t kind,
                               int64_t n_experts, int64_t H, int64_t I, const void* src_a, const void* src_b,
                               void* dst, size_t dst_bytes, void* stream);
@@ -191,7 +193,7 @@ size_t moe_prefill_workspace_bytes(const moe_layer_t* layer, int32_t T_max, int3
  *   integer such that amax <= 448 * 2^k, codes = E4M3 round-to-nearest-even of x * 2^(127 - e)); g and u are
  *   accumulated in fp32; h = SiLU(g) * u in fp32 is quantised the same way per 32 along I; the down projection
  *   accumulates in fp32; y sums the k expert outputs in rank order in fp32.
- *   layer: fmt MXFP4, layout MOE_LAYOUT_PREFILL, 1 <= E <= 1024. x_bf16 [T, H] bf16 (16-byte aligned);
+ *   layer: fmt MXFP4, layout MOE_LAYOUT_TC, 1 <= E <= 1024. x_bf16 [T, H] bf16 (16-byte aligned);
  *   idx [T, k] int32; w [T, k] fp32; 1 <= k <= 8. y [T, H] fp32 (16-byte aligned) and/or y_bf16 [T, H] bf16
  *   (8-byte aligned; round-to-nearest-even copy of y); either may be NULL, not both.
  *   ws: moe_prefill_workspace_bytes(layer, T_max >= T, k) bytes, 256-byte aligned.
@@ -215,11 +217,11 @@ moe_status_t moe_debug_timeout_probe(void* ws, size_t ws_bytes, int32_t limit_us
 
 /* moe_expert_grouped_gemm_prefill with test hooks: if gu_dump is not NULL, the gate/up GEMM also writes its fp32
  * accumulators g and u to gu_dump [rows_max][2I] (row = the pair's row in the sorted buffers, g then u); if
- * offsets is not NULL it receives 10 values describing the workspace: rows_max, tiles_max, and the byte offsets of
+ * offsets is not NULL it receives 8 values describing the workspace: rows_max, tiles_max, and the byte offsets of
  * n_tiles (uint32), tile_first (int32 [tiles]: compact index of each tile's first pair), pair_row (int32 [T*k]:
- * row of pair (t, r), -1 for an invalid id), xq (E4M3 [rows_max][H]), xsf (E8M0 [tiles][H/128][512], permuted as
- * in MOE_LAYOUT_PREFILL), hq ([rows_max][I]), hsf ([tiles][I/128][512]) and dout (fp32 [T*k][H], compact pair
- * order: tile_first[row / 128] + row % 128). */
+ * row of pair (t, r), -1 for an invalid id), xq, hq (the sorted MXFP8 x and h: for each 128-row tile and
+ * 128-column group, 16384 bytes of E4M3 codes [128 rows][128] then the 512-byte exponent block permuted as in
+ * MOE_LAYOUT_TC) and dout (fp32 [T*k][H], compact pair order: tile_first[row / 128] + row % 128). */
 moe_status_t moe_debug_prefill(const moe_layer_t* layer, const void* x_bf16, int32_t T, const int32_t* idx,
                                const float* w, int32_t k, float* y, void* y_bf16, void* ws, size_t ws_bytes,
                                float* gu_dump, int64_t* offsets, void* stream);

@@ -48,6 +48,14 @@ def _unpermute_sf(blocks, rows_in_tile):
     return b.transpose(0, 3, 2, 1, 4).reshape(tiles * 128, KG * 4)
 
 
+def _act_tiles(r, name, tiles, K):
+    """Tile-major MXFP8 buffer -> (codes [tiles*128, K], exponents [tiles*128, K/32])."""
+    KG = K // 128
+    a = _ws_view(r, name, np.uint8, tiles * KG * 16896, (tiles, KG, 16896))
+    codes = a[:, :, :16384].reshape(tiles, KG, 128, 128).transpose(0, 2, 1, 3).reshape(tiles * 128, K)
+    return codes, _unpermute_sf(np.ascontiguousarray(a[:, :, 16384:]), 128)
+
+
 def _rne_bf16_bits(y32):
     b = np.asarray(y32, np.float32).view(np.uint32).astype(np.uint64)
     return ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
@@ -86,10 +94,8 @@ def _stages(m, W, E, H, I, T, k, idx, w, x, r, sample):
     n_tiles = int(_ws_view(r, "n_tiles", np.uint32, 1)[0])
     pair_row = _ws_view(r, "pair_row", np.int32, T * k).reshape(T, k)
     tile_first = _ws_view(r, "tile_first", np.int32, tiles_max)
-    xq = _ws_view(r, "xq", np.uint8, rows_max * H, (rows_max, H))
-    xsf = _unpermute_sf(_ws_view(r, "xsf", np.uint8, tiles_max * (H // 128) * 512, (tiles_max, H // 128, 512)), 128)
-    hq = _ws_view(r, "hq", np.uint8, rows_max * I, (rows_max, I))
-    hsf = _unpermute_sf(_ws_view(r, "hsf", np.uint8, tiles_max * (I // 128) * 512, (tiles_max, I // 128, 512)), 128)
+    xq, xsf = _act_tiles(r, "xq", tiles_max, H)
+    hq, hsf = _act_tiles(r, "hq", tiles_max, I)
     dout = _ws_view(r, "dout", np.float32, T * k * H, (T * k, H))
     # bucketing: rows are distinct, inside the used tiles, grouped by expert in (token, rank) order
     rows = pair_row.reshape(-1)
