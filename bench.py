@@ -39,6 +39,9 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--experts", type=int, default=E, help="expert slots of the layer (smaller only for profiling)")
+    p.add_argument("--layout", default="auto", choices=["auto", "tc", "decode"],
+                   help="weight layout of the decode path: tc (MXFP4, tcgen05 kernels) or decode (mat-vec kernels); "
+                        "auto = tc for MXFP4, decode otherwise")
     p.add_argument("--prefill-tokens", type=int, default=4096,
                    help="tokens of the prefill grouped-GEMM measurement (MXFP4 only; 0 = skip)")
     return p.parse_args()
@@ -124,10 +127,12 @@ def run_ours(args):
     T = args.tokens
     E = args.experts
     do_prefill = args.prefill_tokens > 0 and fmt == 1
+    use_tc = fmt == 1 and args.layout != "decode"
 
     # ---- weights: seeded fp32 -> packed on the GPU by the library's encoder (replica per rank, same weights)
-    layer = m.Layer(fmt, H, I, E, device=dev)
-    layer_p = m.Layer(fmt, H, I, E, layout=m.MOE_LAYOUT_PREFILL, device=dev) if do_prefill else None
+    layer_tc = m.Layer(fmt, H, I, E, layout=m.MOE_LAYOUT_TC, device=dev) if (use_tc or do_prefill) else None
+    layer = layer_tc if use_tc else m.Layer(fmt, H, I, E, device=dev)
+    layer_p = layer_tc if do_prefill else None
     t0 = time.time()
     batch = 16
     pool = cf.ThreadPoolExecutor(2)
@@ -143,8 +148,8 @@ def run_ours(args):
             fut = pool.submit(gen, e0 + batch)
         gd, ud, dd = torch.from_numpy(g).to(dev), torch.from_numpy(u).to(dev), torch.from_numpy(d).to(dev)
         layer.pack(m.MOE_SRC_F32, gd, ud, dd, e0=e0)
-        if layer_p is not None:
-            layer_p.pack(m.MOE_SRC_F32, gd, ud, dd, e0=e0)
+        if layer_tc is not None and layer_tc is not layer:
+            layer_tc.pack(m.MOE_SRC_F32, gd, ud, dd, e0=e0)
     torch.cuda.synchronize()
     setup_s = time.time() - t0
 
@@ -262,7 +267,8 @@ def run_ours(args):
     # routing alone
     idx_np = idx.cpu().numpy()
     uniq = np.mean([len(set(r)) for r in idx_np])
-    per_expert = m.moe_packed_bytes(fmt, 0, 0, 1, H, I) + m.moe_packed_bytes(fmt, 0, 1, 1, H, I)
+    lay = 1 if use_tc else 0
+    per_expert = m.moe_packed_bytes(fmt, lay, 0, 1, H, I) + m.moe_packed_bytes(fmt, lay, 1, 1, H, I)
     alg_bytes = float(np.mean([len(set(r)) for r in idx_np])) * per_expert
 
     # ---- end to end through the public API with host buffers (pinned), copies inside the timed region
@@ -299,10 +305,12 @@ def run_ours(args):
             "metric": "routed-MoE decode tok/s and HBM GB/s (% of 8 TB/s), MXFP4/Q2_K/INT4 experts",
             "value": round(value, 1), "unit": "tok/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": {1: "mxfp4", 2: "int4g32", 3: "q2k"}[fmt] + " weights, bf16 x, fp16/fp32 mma",
+            "dtype": {1: "mxfp4", 2: "int4g32", 3: "q2k"}[fmt] + " weights, bf16 x, " +
+                     ("E4M3-part activations, block-scaled tcgen05, fp32 accumulate" if use_tc else "fp16/fp32 mma"),
             "data": "synthetic (seeded N(0,0.02) weights quantised on the GPU, N(0,1) bf16 tokens)",
             "config": {"workload": "DS4-Flash routed-MoE layer decode, batch 1, %d independent tokens" % T,
                        "H": H, "I": I, "experts": E, "top_k": K_TOP, "format": args.fmt,
+                       "layout": "tc" if use_tc else "decode",
                        "l2": "inputs larger than L2 (3.4 GB of experts, random routing)",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "gpu_launches": 2 * T * args.steps,
@@ -315,7 +323,8 @@ def run_ours(args):
             "mean_unique_experts": float(uniq),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": None,
-                         "kernel": "ffn_kernel<%s>" % args.fmt, "bytes_per_launch": alg_bytes,
+                         "kernel": "decode_kernel (tcgen05)" if use_tc else "ffn_kernel<%s>" % args.fmt,
+                         "bytes_per_launch": alg_bytes,
                          "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if peaks else "fallback"},
             "e2e": {"value": round(world * T / (e2e_ms * 1e-3), 1), "unit": "tok/s",
                     "h2d_bytes_per_step": int(T * H * 2), "d2h_bytes_per_step": int(T * H * 4)},
@@ -339,7 +348,7 @@ def bench_prefill(m, torch, args, dev, stream, layer_p, E):
     ip, wp = zipf_routing(args.seed, Tp, E, K_TOP)
     idx_p = torch.from_numpy(ip).to(dev)
     w_p = torch.from_numpy(wp).to(dev)
-    ws_p = layer_p.workspace(Tp, K_TOP, stream=stream)
+    ws_p = layer_p.prefill_workspace(Tp, K_TOP, stream=stream)
     y_p = torch.empty((Tp, H), dtype=torch.float32, device=dev)
     yb_p = torch.empty((Tp, H), dtype=torch.int16, device=dev)
 

@@ -237,13 +237,16 @@ class Layer:
         moe_pack_weights(self.fmt, src_kind, self.layout, MOE_MAT_DOWN, n, self.H, self.I, down, None, dsl, stream)
 
     def workspace(self, T_max: int, k: int, stream=None) -> torch.Tensor:
-        """Decode/verify workspace for DECODE-layout layers, prefill workspace for PREFILL-layout layers."""
-        if self.layout == MOE_LAYOUT_PREFILL:
-            nbytes = moe_prefill_workspace_bytes(self, T_max, k)
-        else:
-            nbytes = moe_workspace_bytes(self, T_max, k)
+        """Zeroed, 256-byte aligned workspace for decode / verify of up to T_max tokens."""
+        return self._ws(moe_workspace_bytes(self, T_max, k), stream)
+
+    def prefill_workspace(self, T_max: int, k: int, stream=None) -> torch.Tensor:
+        """Zeroed, 256-byte aligned workspace for the prefill grouped GEMM of up to T_max tokens (TC layout)."""
+        return self._ws(moe_prefill_workspace_bytes(self, T_max, k), stream)
+
+    def _ws(self, nbytes: int, stream) -> torch.Tensor:
         if nbytes == 0:
-            raise MoeError(2, "moe_workspace_bytes")
+            raise MoeError(2, "workspace size")
         ws = torch.empty(nbytes + 256, dtype=torch.uint8, device=self.gate_up.device)
         off = (-ws.data_ptr()) % 256
         ws = ws[off:off + nbytes]

@@ -3,6 +3,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
+
 #include "../../include/moe.h"
 
 namespace moe_internal {
@@ -13,5 +15,19 @@ bool fault(const char* site);
 bool shape_ok(int64_t H, int64_t I);
 // number of SMs of the current device (cached per device)
 int num_sms();
+
+// decode / verify of MXFP4 experts in MOE_LAYOUT_TC on tcgen05 (decode_tc.cu); arguments checked by the caller
+size_t tc_decode_workspace_bytes(const moe_layer_t* L, int T_max, int k);
+moe_status_t tc_decode(const moe_layer_t* L, const void* x, int T, const int32_t* idx, const float* w, int k, float* y,
+                       void* y_bf16, int accumulate, void* ws, size_t ws_bytes, void* stream);
+
+// TMA tensor maps (host-side encoding through the runtime's driver entry point; false if it is unavailable or
+// rejects the arguments). tmap_tc_weights: the E2M1 code tiles of a MOE_LAYOUT_TC matrix as a 4-D map
+// [E][row tiles * column tiles][128 rows][64 B] with a 128 x 128 box (16U4_ALIGN16B, 128-byte swizzle).
+// tmap_u8: a rank-2 or rank-3 byte tensor (dims innermost first, strides in bytes for dims 1..), 128-byte swizzle.
+bool tmap_available();
+bool tmap_tc_weights(CUtensorMap* m, const void* base, int kind, int64_t H, int64_t I, int64_t E);
+bool tmap_u8(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+             const uint32_t* box);
 
 }  // namespace moe_internal

@@ -621,6 +621,7 @@ static size_t ws_needed(const moe_layer_t* L, int T, int k) {
 extern "C" size_t moe_workspace_bytes(const moe_layer_t* L, int32_t T_max, int32_t k) {
   if (!L || T_max < 1 || T_max > kMaxT || k < 1 || k > kMaxK) return 0;
   if (!moe_internal::shape_ok(L->H, L->I)) return 0;
+  if (L->layout == MOE_LAYOUT_TC) return L->fmt == MOE_FMT_MXFP4 ? moe_internal::tc_decode_workspace_bytes(L, T_max, k) : 0;
   return ws_needed(L, T_max, k);
 }
 
@@ -657,12 +658,18 @@ static moe_status_t ffn_common(const char* site, const moe_layer_t* L, const voi
   if (moe_internal::fault(site)) return MOE_ERR_FAULT_INJECTED;
   if (!L || !x || !idx || !w || !y || !ws) return MOE_ERR_INVALID_ARG;
   if (L->fmt < MOE_FMT_MXFP4 || L->fmt > MOE_FMT_Q2K) return MOE_ERR_UNSUPPORTED_FORMAT;
-  if (L->layout != MOE_LAYOUT_DECODE) return MOE_ERR_UNSUPPORTED_FORMAT;
+  if (L->layout != MOE_LAYOUT_DECODE && L->layout != MOE_LAYOUT_TC) return MOE_ERR_UNSUPPORTED_FORMAT;
   if (!L->gate_up || !L->down || ((uintptr_t)L->gate_up & 15) || ((uintptr_t)L->down & 15)) return MOE_ERR_INVALID_ARG;
   if (((uintptr_t)x & 3) || ((uintptr_t)ws & 255) || ((uintptr_t)y & 3)) return MOE_ERR_INVALID_ARG;
   if (y_bf16 && ((uintptr_t)y_bf16 & 1)) return MOE_ERR_INVALID_ARG;
   if (T < 1 || T > kMaxT || k < 1 || k > kMaxK || L->E < 1) return MOE_ERR_SHAPE;
   if (!moe_internal::shape_ok(L->H, L->I)) return MOE_ERR_SHAPE;
+  if (L->layout == MOE_LAYOUT_TC) {
+    if (L->fmt != MOE_FMT_MXFP4) return MOE_ERR_UNSUPPORTED_FORMAT;
+    moe_status_t st = moe_check_device();
+    if (st != MOE_OK) return st;
+    return moe_internal::tc_decode(L, x, T, idx, w, k, y, y_bf16, accumulate, ws, ws_bytes, stream);
+  }
   if (ws_bytes < ws_needed(L, T, k)) return MOE_ERR_WORKSPACE_TOO_SMALL;
   moe_status_t st = moe_check_device();
   if (st != MOE_OK) return st;
@@ -726,6 +733,7 @@ extern "C" moe_status_t moe_expert_ffn_decode_static(const moe_layer_t* L, const
   if (moe_internal::fault("decode")) return MOE_ERR_FAULT_INJECTED;
   if (!L || !x_bf16 || !idx || !w || !y) return MOE_ERR_INVALID_ARG;
   if (k < 1 || k > kMaxK || !moe_internal::shape_ok(L->H, L->I)) return MOE_ERR_SHAPE;
+  if (L->layout != MOE_LAYOUT_DECODE) return MOE_ERR_UNSUPPORTED_FORMAT;  // the fixed scratch serves this layout
   if (ws_needed(L, 1, k) > kStaticScratchBytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
   moe_status_t st = moe_check_device();
   if (st != MOE_OK) return st;

@@ -13,11 +13,9 @@
 //   4. gemm<DOWN>: per (tile, 128 hidden indices) unit, D = H_tile * Down^T over K = I, fp32 rows per pair.
 //   5. combine: y[t] = sum_r w[t, r] * D[pair (t, r)] in rank order, fp32 and/or bf16 (round to nearest even).
 // The GEMM kernel is persistent (one CTA per SM) and warp-specialised: warp 0 issues TMA tensor copies into a
-// 6-stage shared-memory ring, warp 1 issues tcgen05.cp (scale factors) and tcgen05.mma into one of two TMEM
+// 6-stage shared-memory ring from 3 lanes, warp 1 issues tcgen05.cp (scale factors) and tcgen05.mma into one of two TMEM
 // accumulators, warps 2..5 drain the other accumulator with tcgen05.ld. Every wait is bounded (timeout ->
 // device status MOE_ERR_DEVICE_TIMEOUT, the CTA drains its own copies and frees TMEM).
-#include <cuda.h>
-#include <cudaTypedefs.h>
 #include <mutex>
 
 #include "common.cuh"
@@ -39,6 +37,7 @@ constexpr int SF_BYTES = 512;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES + 2 * SF_BYTES;  // 33 KB, a multiple of 1024
 constexpr uint32_t STAGE_TX = A_BYTES + B_TX + 2 * SF_BYTES;
 constexpr int THREADS = 192;
+constexpr int PRODUCERS = 3;             // TMA-issuing lanes of warp 0
 constexpr uint32_t TMEM_COLS = 512;       // accumulators at columns 0 and 128, scale columns from 256
 constexpr uint32_t SF_COL0 = 256;
 constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
@@ -295,35 +294,35 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
   const long long lim = a.wait_ns;
 
   if (warp == 0) {
-    // ---------------- TMA producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t ph = 0;
-      int issued[STAGES];
-      for (int s = 0; s < STAGES; ++s) issued[s] = -1;
+    // ---------------- TMA producer. One issuing thread completes about one wait-and-issue round per 330 ns on
+    // GB300 however many bytes it moves, so PRODUCERS lanes take turns: lane l issues all four copies of stages
+    // l, l + PRODUCERS, ... of this CTA's sequence of (unit, k-group) stages.
+    if (lane < PRODUCERS) {
+      int issued_slot = -1;
+      uint32_t issued_ph = 0;
       bool ok = true;
-      for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      for (int64_t g = lane;; g += PRODUCERS) {
+        const int64_t u = blockIdx.x + (g / KG) * gridDim.x;
+        if (u >= n_units) break;
+        const int kg = (int)(g % KG), s = (int)(g % STAGES);
+        const uint32_t ph = (uint32_t)((g / STAGES) & 1);
+        if (!pf_wait(&empty[s], ph ^ 1, s_abort, lim)) { ok = false; break; }
         const int tile = (int)(u / a.NB), nb = (int)(u % a.NB);
         const int e = a.tile_e[tile];
-        const uint8_t* wt = a.w + (int64_t)e * a.wstride + (int64_t)nb * KG * kTcTileBytes;
-        for (int kg = 0; kg < KG; ++kg) {
-          if (!pf_wait(&empty[stage], ph ^ 1, s_abort, lim)) { ok = false; break; }
-          uint8_t* st = smem + stage * STAGE_BYTES;
-          mbar_arrive_expect_tx(&full[stage], STAGE_TX);
-          tma_load_3d(st, &tmA, 0, 0, tile * KG + kg, &full[stage]);
-          tma_load_4d(st + A_BYTES, &tmB, 0, 0, nb * KG + kg, e, &full[stage]);
-          bulk_g2s_plain(st + A_BYTES + B_BYTES, a.act + act_tile(tile, KG, kg) + A_BYTES, SF_BYTES, &full[stage]);
-          bulk_g2s_plain(st + A_BYTES + B_BYTES + SF_BYTES, wt + (int64_t)kg * kTcTileBytes + 8192, SF_BYTES,
-                         &full[stage]);
-          issued[stage] = (int)ph;
-          if (++stage == STAGES) { stage = 0; ph ^= 1; }
-        }
+        const uint8_t* wt = a.w + (int64_t)e * a.wstride + ((int64_t)nb * KG + kg) * kTcTileBytes;
+        uint8_t* st = smem + s * STAGE_BYTES;
+        mbar_arrive_expect_tx(&full[s], STAGE_TX);
+        tma_load_3d(st, &tmA, 0, 0, tile * KG + kg, &full[s]);
+        tma_load_4d(st + A_BYTES, &tmB, 0, 0, nb * KG + kg, e, &full[s]);
+        bulk_g2s_plain(st + A_BYTES + B_BYTES, a.act + act_tile(tile, KG, kg) + A_BYTES, SF_BYTES, &full[s]);
+        bulk_g2s_plain(st + A_BYTES + B_BYTES + SF_BYTES, wt + 8192, SF_BYTES, &full[s]);
+        issued_slot = s;
+        issued_ph = ph;
       }
       if (!ok) {
         record_error(a.status, MOE_ERR_DEVICE_TIMEOUT);
-        // let the copies already issued land before the CTA's shared memory is released
-        for (int s = 0; s < STAGES; ++s)
-          if (issued[s] >= 0) mbar_wait(&full[s], (uint32_t)issued[s], 100000000LL);
+        // let the last stage this lane issued land before the CTA's shared memory is released
+        if (issued_slot >= 0) mbar_wait(&full[issued_slot], issued_ph, 100000000LL);
       }
     }
     __syncwarp();
@@ -468,35 +467,11 @@ __global__ void combine(const float* dout, const int32_t* pslot, const int32_t* 
 }
 
 // ------------------------------------------------------------------ host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    cudaDriverEntryPointQueryResult q;
-    void* p = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
 // 3-D map over tile-major E4M3 activations: [n tiles][128 rows][128 B], tile stride ACT_TILE
 bool map_act(CUtensorMap* m, const void* base, int64_t ntiles) {
-  cuuint64_t dims[3] = {128, 128, (cuuint64_t)ntiles}, strides[2] = {128, (cuuint64_t)ACT_TILE};
-  cuuint32_t box[3] = {BK, BM, 1}, es[3] = {1, 1, 1};
-  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-// 4-D map over the E2M1 code tiles of a tensor-core layout matrix: [E][RT*KT tiles][128 rows][64 B]
-bool map_wgt(CUtensorMap* m, const void* base, const TcGeom& g, int64_t E) {
-  cuuint64_t dims[4] = {128, 128, (cuuint64_t)(g.RT * g.KT), (cuuint64_t)E};
-  cuuint64_t strides[3] = {64, (cuuint64_t)kTcTileBytes, (cuuint64_t)g.stride};
-  cuuint32_t box[4] = {BK, BN, 1, 1}, es[4] = {1, 1, 1, 1};
-  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4, const_cast<void*>(base), dims, strides, box, es,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const uint64_t dims[3] = {128, 128, (uint64_t)ntiles}, strides[2] = {128, (uint64_t)ACT_TILE};
+  const uint32_t box[3] = {BK, BM, 1};
+  return moe_internal::tmap_u8(m, base, 3, dims, strides, box);
 }
 
 bool check_layer(const moe_layer_t* L) {
@@ -519,7 +494,7 @@ moe_status_t run(const moe_layer_t* L, const void* x_bf16, int32_t T, const int3
   if (ws_bytes < (size_t)P.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   moe_status_t st = moe_check_device();
   if (st != MOE_OK) return st;
-  if (!encode_fn()) return MOE_ERR_CUDA;
+  if (!moe_internal::tmap_available()) return MOE_ERR_CUDA;
   cudaStream_t s = (cudaStream_t)stream;
   uint8_t* B = (uint8_t*)ws;
   int32_t* status = reinterpret_cast<int32_t*>(B);
@@ -536,8 +511,8 @@ moe_status_t run(const moe_layer_t* L, const void* x_bf16, int32_t T, const int3
   // tensor maps (host encodes; they travel as __grid_constant__ kernel parameters)
   const TcGeom ggu = tc_geom(MOE_MAT_GATE_UP, H, I), gdn = tc_geom(MOE_MAT_DOWN, H, I);
   CUtensorMap mx, mgu, mh, mdn;
-  if (!map_act(&mx, B + P.o_xq, P.tiles_max * (H / 128)) || !map_wgt(&mgu, L->gate_up, ggu, E) ||
-      !map_act(&mh, B + P.o_hq, P.tiles_max * (I / 128)) || !map_wgt(&mdn, L->down, gdn, E))
+  if (!map_act(&mx, B + P.o_xq, P.tiles_max * (H / 128)) || !moe_internal::tmap_tc_weights(&mgu, L->gate_up, MOE_MAT_GATE_UP, H, I, E) ||
+      !map_act(&mh, B + P.o_hq, P.tiles_max * (I / 128)) || !moe_internal::tmap_tc_weights(&mdn, L->down, MOE_MAT_DOWN, H, I, E))
     return MOE_ERR_CUDA;
 
   static std::once_flag attr_once;

@@ -64,7 +64,7 @@ def _rne_bf16_bits(y32):
 def _run(m, layer, x, idx, w, k, gu=True):
     T, H = x.shape
     I = layer.I
-    ws = layer.workspace(T, k)
+    ws = layer.prefill_workspace(T, k)
     assert ws.numel() == m.moe_prefill_workspace_bytes(layer, T, k)
     y = torch.full((T, H), float("nan"), device=DEV)
     yb = torch.zeros((T, H), dtype=torch.int16, device=DEV)
@@ -241,7 +241,7 @@ def test_prefill_host_errors(m):
     E, H, I, k, T = 8, 512, 256, 2, 4
     dec = m.Layer(MXFP4, H, I, E, device=DEV)
     pre = m.Layer(MXFP4, H, I, E, layout=PREFILL, device=DEV)
-    ws = pre.workspace(T, k)
+    ws = pre.prefill_workspace(T, k)
     x = torch.zeros((T, H), dtype=torch.int16, device=DEV)
     idx = torch.zeros((T, k), dtype=torch.int32, device=DEV)
     w = torch.zeros((T, k), device=DEV)
