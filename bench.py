@@ -306,7 +306,7 @@ def run_ours(args):
             "value": round(value, 1), "unit": "tok/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": {1: "mxfp4", 2: "int4g32", 3: "q2k"}[fmt] + " weights, bf16 x, " +
-                     ("E4M3-part activations, block-scaled tcgen05, fp32 accumulate" if use_tc else "fp16/fp32 mma"),
+                     ("E2M1-part activations (6 parts), block-scaled tcgen05 kind::mxf4, fp32 accumulate" if use_tc else "fp16/fp32 mma"),
             "data": "synthetic (seeded N(0,0.02) weights quantised on the GPU, N(0,1) bf16 tokens)",
             "config": {"workload": "DS4-Flash routed-MoE layer decode, batch 1, %d independent tokens" % T,
                        "H": H, "I": I, "experts": E, "top_k": K_TOP, "format": args.fmt,

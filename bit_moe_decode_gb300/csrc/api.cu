@@ -37,15 +37,28 @@ bool tmap_tc_weights(CUtensorMap* m, const void* base, int kind, int64_t H, int6
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool tmap_tc_weights_packed(CUtensorMap* m, const void* base, int kind, int64_t H, int64_t I, int64_t E) {
+  if (!encode_fn()) return false;
+  const moe::TcGeom g = moe::tc_geom(kind, H, I);
+  cuuint64_t dims[4] = {64, 128, (cuuint64_t)(g.RT * g.KT), (cuuint64_t)E};
+  cuuint64_t strides[3] = {64, (cuuint64_t)moe::kTcTileBytes, (cuuint64_t)g.stride};
+  cuuint32_t box[4] = {64, 128, 1, 1}, es[4] = {1, 1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool tmap_u8(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
-             const uint32_t* box) {
+             const uint32_t* box, int swizzle_bytes) {
   if (!encode_fn() || rank < 2 || rank > 3) return false;
   cuuint64_t d[3], st[2];
   cuuint32_t b[3], es[3] = {1, 1, 1};
   for (int i = 0; i < rank; ++i) { d[i] = dims[i]; b[i] = box[i]; }
   for (int i = 0; i < rank - 1; ++i) st[i] = strides[i];
   return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank, const_cast<void*>(base), d, st, b, es,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

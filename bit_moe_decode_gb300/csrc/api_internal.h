@@ -24,10 +24,13 @@ moe_status_t tc_decode(const moe_layer_t* L, const void* x, int T, const int32_t
 // TMA tensor maps (host-side encoding through the runtime's driver entry point; false if it is unavailable or
 // rejects the arguments). tmap_tc_weights: the E2M1 code tiles of a MOE_LAYOUT_TC matrix as a 4-D map
 // [E][row tiles * column tiles][128 rows][64 B] with a 128 x 128 box (16U4_ALIGN16B, 128-byte swizzle).
-// tmap_u8: a rank-2 or rank-3 byte tensor (dims innermost first, strides in bytes for dims 1..), 128-byte swizzle.
+// tmap_u8: a rank-2 or rank-3 byte tensor (dims innermost first, strides in bytes for dims 1..), 128- or 64-byte
+// swizzle.
 bool tmap_available();
 bool tmap_tc_weights(CUtensorMap* m, const void* base, int kind, int64_t H, int64_t I, int64_t E);
+// the same tiles as packed bytes ([E][tiles][128 rows][64 B], box 64 x 128, 64-byte swizzle) for kind::mxf4
+bool tmap_tc_weights_packed(CUtensorMap* m, const void* base, int kind, int64_t H, int64_t I, int64_t E);
 bool tmap_u8(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
-             const uint32_t* box);
+             const uint32_t* box, int swizzle_bytes = 128);
 
 }  // namespace moe_internal

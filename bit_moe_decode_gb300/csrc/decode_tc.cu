@@ -1,28 +1,31 @@
 // decode_tc.cu -- decode and verify (1..8 tokens) of MXFP4 experts in the tensor-core layout on tcgen05.
 //
-// The work is a mat-vec per expert, so the block-scaled MMA runs with the weights as the 128-row operand A and a
-// handful of activation columns as operand B:
-//   gate/up: B = x split into two E4M3 parts per 32-block (x ~= p0 * 2^(e0-127) + p1 * 2^(e1-127), exact for
-//            bf16 x except far below the block's largest element), 2 columns per token, N = 16;
-//   down:    B = h split into three E4M3 parts the same way (about 12 significant bits), 3 columns per
-//            (expert, token), N = 32.
-// A token's result is the sum of its part columns; the MMA computes every column independently, so a token's
-// numbers do not depend on which other tokens share the sweep (verify row t == decode of token t).
+// The work is a mat-vec per expert, so the block-scaled MMA (kind::mxf4: E2M1 x E2M1, one UE8M0 exponent per 32,
+// K = 64 per instruction) runs with the weights as the 128-row operand A, read as PACKED codes straight from the
+// tensor-core tile layout (8 KB per 128 x 128 tile in shared memory, no unpacking), and a few activation columns as
+// operand B: x (gate/up) and h (down) are each split into PARTS = 6 E2M1 parts per 32-block (split_parts_n: part p
+// has exponent e0 - 2p and quantises what the earlier parts left; error below 1/3072 of the block's largest value).
+// Column t * PARTS + p holds part p of token t; N = 48 for every call. A token's result is the sum of its part
+// columns in part order; the MMA computes every column independently, so a token's numbers do not depend on which
+// other tokens share the sweep (verify row t == decode of token t).
 //
 // Work units (fixed for every T, so the arithmetic of a token never changes):
 //   G unit (expert u, 128-row tile rt of [Gate;Up], K segment ks): fp32 partial g/u of the tile's 64 gate and 64
 //     up rows over KS_G k-tiles, written to the workspace. The unit that completes the last segment of (u, rt)
-//     sums the segments in order, forms h = SiLU(g) * u and writes the three E4M3 parts of h for the D units.
+//     sums the segments in order, forms h = SiLU(g) * u and writes the E2M1 parts of h for the D units.
 //   D unit (expert u, 128-row tile jt of Down, segment ks): fp32 partial of Down * h. The unit that completes the
 //     last D unit of row tile jt (over all experts and segments) sums each (expert, token) in segment order and
 //     combines y[t] = sum_r w[t, r] * d_r in rank order.
 // Units are dealt round-robin to persistent CTAs (one per SM, cooperative launch), G units first (expert-major),
-// then D units. Inside a CTA, four independent pipelines (a TMA-issuing lane, an MMA-issuing thread, a two-slot
-// shared-memory ring and two TMEM accumulators each) take the CTA's units in turn, because one issuing thread
-// sustains only about one wait-and-issue round per 330 ns (TMA) or one 4-MMA stage plus commit per ~600 cycles
-// (tcgen05), while one SM must consume an 8.5 KB weight tile every ~180 ns to keep pace with HBM. Four epilogue
-// warps drain the accumulators. Cross-CTA dependencies (x parts ready, h of an expert ready) are global counters
-// with bounded waits; the last CTA to finish resets them.
+// then D units; the grid is a multiple of the number of gate/up segments, so all G units of a CTA share one K
+// segment and the CTA keeps that segment's x parts resident in shared memory (computed at kernel start).
+// Inside a CTA, three independent pipelines take the CTA's units as they free up. A pipeline is a weight-issuing
+// warp, an activation-issuing warp (h parts of D units, after their h is final), an MMA-issuing warp, a five-slot
+// shared-memory ring, two TMEM accumulators and a group of four epilogue warps. One issuing thread sustains only
+// about one wait-and-issue round per 330 ns (TMA) or one stage of MMAs plus commit per ~600 cycles (tcgen05),
+// while one SM must consume an 8.5 KB weight tile every ~180 ns to keep pace with HBM. Cross-CTA dependencies
+// (partials complete, h of an expert's K segment final) are global counters with bounded waits; the last CTA to
+// finish resets them.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <mutex>
@@ -35,22 +38,30 @@
 namespace moe {
 namespace dtc {
 
-constexpr int NPIPE = 4;                 // pipelines per CTA
-constexpr int RING = 2;                  // stage slots per pipeline
+constexpr int NPIPE = 3;                 // pipelines per CTA
+constexpr int RING = 5;                  // stage slots per pipeline
 constexpr int NSLOT = NPIPE * RING;
-constexpr int A_BYTES = 16384;           // 128 x 128 E2M1 weights as unpacked in shared memory
-constexpr int A_TX = 8192;               // bytes the TMA engine reads for them
-constexpr int B_BYTES = 4096;            // up to 32 rows x 128 E4M3 activation parts
-constexpr int SLOT_BYTES = A_BYTES + B_BYTES + 1024;  // + two 512-byte exponent blocks; 21 KB
+constexpr int PARTS = 6;                 // E2M1 parts per activation value
+constexpr int NB = 48;                   // B rows (MMA N): PARTS x 8 tokens
+constexpr int A_BYTES = 8192;            // 128 rows x 64 B of packed E2M1 weight codes
+constexpr int B_BYTES = NB * 64;         // 48 rows x 64 B of packed E2M1 activation parts
+constexpr int SLOT_BYTES = A_BYTES + B_BYTES + 1024;  // + two 512-byte exponent blocks; 12 KB
 constexpr int MAX_T = 8, MAX_K = 8, MAX_U = MAX_T * MAX_K;
-constexpr int XROWS = 16, HROWS = 32;    // B rows: 2 parts x 8 tokens; 3 parts x 8 tokens (padded)
-constexpr int EPI_WARP0 = 5;             // warps 0: producers, 1..4: MMA issuers, 5..20: epilogue
+constexpr int XROWS = NB, HROWS = NB;    // B rows of the x parts and of each expert's h parts
+constexpr int EPI_WARP0 = 3 * NPIPE;     // warps: 2 NPIPE producers, NPIPE MMA issuers, then the epilogue groups
+// (each issuing thread has a warp of its own: issuing lanes that share a warp diverge and run one after another)
 constexpr int NGRP = NPIPE;              // epilogue groups of 4 warps; group j drains pipeline j
-constexpr int QN = 4;                    // unit-id queue entries per pipeline
+constexpr int QN = 8;                    // unit-id queue entries per pipeline
 constexpr int THREADS = (EPI_WARP0 + 4 * NGRP) * 32;
-constexpr uint32_t TMEM_COLS = 512;      // accumulators: pipeline j, buffer a at 64 j + 32 a; scales from 256
-constexpr uint32_t SF_COL0 = 256;
-constexpr int SMEM = NSLOT * SLOT_BYTES + 1024;
+constexpr uint32_t TMEM_COLS = 512;      // accumulators: pipeline j, buffer a at 128 j + 64 a; scales from 384
+constexpr uint32_t SF_COL0 = 384;
+static_assert(128 * NPIPE <= (int)SF_COL0 && SF_COL0 + 8 * NSLOT <= TMEM_COLS, "TMEM budget");
+// Every gate/up unit of CTA b covers the same K segment (b mod S_G: the grid is a multiple of S_G), so the CTA keeps
+// that segment's x parts resident: 8 k-tiles x 48 rows x 64 B in the 64-byte-swizzled MMA layout, and their
+// exponent blocks.
+constexpr int XRES_TILE = NB * 64;       // 3 KB per k-tile
+constexpr int XRES_BYTES = 8 * XRES_TILE + 8 * 512;
+constexpr int SMEM = NSLOT * SLOT_BYTES + XRES_BYTES + 1024;
 
 // ------------------------------------------------------------------ geometry of one call
 struct Geo {
@@ -59,29 +70,30 @@ struct Geo {
   int RTD, KTD, KSD, SD;   // down
   int nG, nD;              // units
 };
-__host__ __device__ inline int ks_for(int kt) { return kt % 8 == 0 ? 8 : (kt % 4 == 0 ? 4 : 2); }
+// k-tiles per unit: gate/up 8 (or 4, 2), down 4 (or 2) -- shorter down units shorten the tail after the last h
+__host__ __device__ inline int ks_for_g(int kt) { return kt % 8 == 0 ? 8 : (kt % 4 == 0 ? 4 : 2); }
+__host__ __device__ inline int ks_for_d(int kt) { return kt % 4 == 0 ? 4 : 2; }
 
 // ------------------------------------------------------------------ workspace (byte offsets from the base)
 // [0, 256)       WsHeader (status word)
-// [256, 20736)   counters (uint32): x_ready, done, h_ready[64], g_cnt[64 * 64], d_cnt[32]
-// then xb [16][H] E4M3, xsf [H/128][512], hb [Umax * 32][I], hsf [Umax][I/128][512],
+// [256, ...)     counters (uint32): (unused), done, h_ready[64][16] (per expert and down K segment),
+//                g_cnt[64 * 64] (per expert and gate/up row tile), d_cnt[32] (per down row tile)
+// then hb [Umax * 48][I/2] packed E2M1 h parts, hsf [Umax][I/128][512] their exponents,
 //      gpart [Umax][2I/128][S_G][TS][128] fp32, dpart [Umax][H/128][S_D][TS][128] fp32
 // with Umax = T_max * k union experts and TS = T_max token columns of the partial buffers.
 constexpr int64_t kCnt = 256;
-constexpr int C_XREADY = 0, C_DONE = 1, C_HREADY = 2, C_G = C_HREADY + MAX_U, C_D = C_G + MAX_U * 64;
+constexpr int C_DONE = 1, C_HREADY = 2, C_G = C_HREADY + MAX_U * 16, C_D = C_G + MAX_U * 64;
 constexpr int C_END = C_D + 32;
 struct Ws {
-  int64_t xb, xsf, hb, hsf, gpart, dpart, total;
+  int64_t hb, hsf, gpart, dpart, total;
 };
 inline int64_t al1k(int64_t v) { return (v + 1023) & ~(int64_t)1023; }
 inline Ws ws_layout(int64_t H, int64_t I, int64_t Umax, int64_t TS) {
   Ws w;
   int64_t o = al1k(kCnt + (int64_t)C_END * 4);
   const int64_t RTG = 2 * I / 128, KTG = H / 128, RTD = H / 128, KTD = I / 128;
-  const int64_t SG = KTG / ks_for((int)KTG), SD = KTD / ks_for((int)KTD);
-  w.xb = o;    o = al1k(o + XROWS * H);
-  w.xsf = o;   o = al1k(o + KTG * 512);
-  w.hb = o;    o = al1k(o + Umax * HROWS * I);
+  const int64_t SG = KTG / ks_for_g((int)KTG), SD = KTD / ks_for_d((int)KTD);
+  w.hb = o;    o = al1k(o + Umax * HROWS * I / 2);
   w.hsf = o;   o = al1k(o + Umax * KTD * 512);
   w.gpart = o; o = al1k(o + Umax * RTG * SG * TS * 128 * 4);
   w.dpart = o; o = al1k(o + Umax * RTD * SD * TS * 128 * 4);
@@ -108,11 +120,12 @@ struct Args {
 };
 
 // ------------------------------------------------------------------ small helpers
-__device__ __forceinline__ int mx8_exp(float amax) {
+// Exponent of an E2M1 block: e = clamp(k + 127, 1, 254), k the smallest integer with amax <= 6 * 2^k.
+__device__ __forceinline__ int mx4_exp(float amax) {
   const uint32_t ab = __float_as_uint(amax) & 0x7FFFFFFFu;
   const int ef = (int)(ab >> 23);
   if (ef == 0) return 1;
-  const int e = ef - 8 + ((ab & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+  const int e = ef - 2 + ((ab & 0x7FFFFFu) > 0x400000u ? 1 : 0);
   return e < 1 ? 1 : (e > 254 ? 254 : e);
 }
 __device__ __forceinline__ float pow2_127m(int e) {  // 2^(127 - e), e in [1, 254]
@@ -121,32 +134,62 @@ __device__ __forceinline__ float pow2_127m(int e) {  // 2^(127 - e), e in [1, 25
 __device__ __forceinline__ float pow2_m127(int e) {  // 2^(e - 127), e in [1, 254]
   return __uint_as_float((uint32_t)e << 23);
 }
-__device__ __forceinline__ uint32_t e4m3_code(float v) {  // round to nearest even, saturating
+// E2M1 code of v (round to nearest even, saturating to +-6) in the low nibble
+__device__ __forceinline__ uint32_t e2m1_code(float v) {
   uint16_t d;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(0.0f), "f"(v));
-  return d & 0xFFu;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}" : "=h"(d) : "f"(0.0f), "f"(v));
+  return d & 15u;
 }
-__device__ __forceinline__ float e4m3_value(uint32_t code) {
-  uint32_t h2;
-  const uint16_t c = (uint16_t)code;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
-  return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+__device__ __forceinline__ float e2m1_value(uint32_t c) {
+  const float mag = (c & 4) ? ((c & 2) ? ((c & 1) ? 6.f : 4.f) : ((c & 1) ? 3.f : 2.f))
+                            : (float)(c & 3) * 0.5f;
+  return (c & 8) ? -mag : mag;
 }
 __device__ __forceinline__ float warp_amax(float v) {
   const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(v)));
   return __uint_as_float(m);
 }
-// Split v (one element per lane of a 32-block) into `np` E4M3 parts with per-block exponents. Lane writes its
-// codes to codes[p]; returns nothing else (exponents in exps[p], identical across the warp).
-__device__ __forceinline__ void split_parts(float v, int np, uint32_t* codes, int* exps) {
-  float r = v;
-  for (int p = 0; p < np; ++p) {
-    const int e = mx8_exp(warp_amax(r));
-    const uint32_t c = e4m3_code(r * pow2_127m(e));
-    codes[p] = c;
-    exps[p] = e;
-    r = r - e4m3_value(c) * pow2_m127(e);
+// Split v (lane l holds element l of a 32-block) into PARTS E2M1 parts: part 0 uses the block exponent e0 (largest
+// magnitude <= 6 * 2^(e0 - 127)); part p uses e0 - 2p (clamped at 1) and quantises what parts 0 .. p-1 left. After
+// a part the remainder is at most half an E2M1 step, <= 1 unit of its scale = 4 units of the next part's, so no
+// part saturates and each adds at least 2 bits: the final error is below 2^-10 of part 0's scale, i.e. below
+// 1/3072 of the block's largest magnitude. Only e0 needs a warp reduction. Even lanes get the packed byte of
+// elements (l, l + 1) of each part in bytes[p] (element l in the low nibble). A block holding NaN or infinity has
+// no E2M1 encoding: every part gets the E8M0 NaN exponent (255), which the block-scaled MMA turns into NaN.
+template <int NV>
+__device__ __forceinline__ void split_parts_n(const float (&v)[NV], const bool (&live)[NV], uint32_t (&bytes)[NV][PARTS],
+                                              int (&exps)[NV][PARTS]) {
+  const int lane = threadIdx.x & 31;
+  float r[NV], am[NV];
+#pragma unroll
+  for (int q = 0; q < NV; ++q) {
+    r[q] = v[q];
+    am[q] = live[q] ? warp_amax(v[q]) : 0.f;
   }
+#pragma unroll
+  for (int q = 0; q < NV; ++q) {
+    if (!live[q]) continue;
+    const bool nonfinite = !(am[q] <= 3.4028235e38f);
+    const int e0 = mx4_exp(am[q]);
+#pragma unroll
+    for (int p = 0; p < PARTS; ++p) {
+      const int e = nonfinite ? 255 : (e0 - 2 * p > 1 ? e0 - 2 * p : 1);
+      const uint32_t c = nonfinite ? 0u : e2m1_code(r[q] * pow2_127m(e));
+      const uint32_t hi = __shfl_down_sync(0xFFFFFFFFu, c, 1);
+      bytes[q][p] = (lane & 1) ? 0u : (c | (hi << 4));
+      exps[q][p] = e;
+      if (!nonfinite) r[q] = r[q] - e2m1_value(c) * pow2_m127(e);
+    }
+  }
+}
+__device__ __forceinline__ void split_parts(float v, uint32_t (&bytes)[PARTS], int (&exps)[PARTS]) {
+  const float vv[1] = {v};
+  const bool live[1] = {true};
+  uint32_t b[1][PARTS];
+  int e[1][PARTS];
+  split_parts_n<1>(vv, live, b, e);
+#pragma unroll
+  for (int p = 0; p < PARTS; ++p) { bytes[p] = b[0][p]; exps[p] = e[0][p]; }
 }
 __device__ __forceinline__ int sfb(int row, int kb) { return (row & 31) * 16 + (row >> 5) * 4 + kb; }
 
@@ -161,10 +204,13 @@ __device__ __forceinline__ bool wait_ge(const uint32_t* p, uint32_t target, vola
     if (globaltimer_ns() - t0 > lim) { *abort_flag = 1; return false; }
   }
 }
+// Spinning threads back off briefly between polls so that warps doing arithmetic on the same SM keep their issue
+// slots.
 __device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, long long lim) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = globaltimer_ns();
   while (true) {
+    __nanosleep(20);
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > lim) { *abort_flag = 1; return false; }
@@ -186,16 +232,39 @@ __device__ __forceinline__ uint32_t atom_acq_rel_add(uint32_t* p, uint32_t v) {
 struct Unit {
   int d, u, rt, ks;
 };
-__device__ __forceinline__ Unit unit_of(int v, const Geo& g) {
-  Unit r;
-  if (v < g.nG) {
-    const int per = g.RTG * g.SG;
-    r.d = 0; r.u = v / per; r.rt = (v % per) / g.SG; r.ks = v % g.SG;
-  } else {
-    v -= g.nG;
-    const int per = g.RTD * g.SD;
-    r.d = 1; r.u = v / per; r.rt = (v % per) / g.SD; r.ks = v % g.SD;
+// Global order of the work: blocks of units G(u) (all row tiles and segments of expert u's gate/up) and D(u); D(u)
+// is placed after G(u + LAG). With LAG = MAX_U every G block comes first (G0 .. G(U-1) D0 .. D(U-1)), which measured
+// best: a D block placed earlier waits for h of its expert while holding a pipeline.
+constexpr int LAG = MAX_U;
+struct Order {
+  int n;                       // blocks
+  int start[2 * MAX_U + 1];    // first unit of each block; start[n] = total units
+  int8_t d[2 * MAX_U], u[2 * MAX_U];
+};
+__device__ void build_order(Order& o, const Geo& g, int U) {
+  const int nGu = g.RTG * g.SG, nDu = g.RTD * g.SD;
+  int nb = 0, pos = 0;
+  auto add = [&](int d, int u) { o.start[nb] = pos; o.d[nb] = (int8_t)d; o.u[nb] = (int8_t)u; pos += d ? nDu : nGu; ++nb; };
+  for (int b = 0; b < U; ++b) {
+    add(0, b);
+    if (b >= LAG) add(1, b - LAG);
   }
+  for (int b = U > LAG ? U - LAG : 0; b < U; ++b) add(1, b);
+  o.start[nb] = pos;
+  o.n = nb;
+}
+__device__ __forceinline__ Unit unit_of(int v, const Geo& g, const Order& o) {
+  int lo = 0, hi = o.n - 1;  // last block with start <= v
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (o.start[mid] <= v) lo = mid; else hi = mid - 1;
+  }
+  Unit r;
+  r.d = o.d[lo];
+  r.u = o.u[lo];
+  const int rr = v - o.start[lo], S = r.d ? g.SD : g.SG;
+  r.rt = rr / S;
+  r.ks = rr % S;
   return r;
 }
 
@@ -229,35 +298,70 @@ __device__ void build_tables(Tables& tb, const int32_t* idx, int T, int k, int E
     }
 }
 
-// x of every token, k-tile kt, split into two E4M3 parts: B rows 2t + p, one exponent per (row, 32-block).
-// Run by the 4 epilogue warps of CTA kt: warp w takes the (token, 32-block) pairs w, w + 4, ...
-__device__ void split_x(const Args& a, const Geo& g, int kt, int ew) {
+// x of every token over the K segment ks0 (KSG k-tiles), split into PARTS E2M1 parts, written into the resident B
+// operand: k-tile kk at xres + kk * XRES_TILE, row PARTS * t + p, 64 bytes per row, 16-byte chunks swizzled as the
+// 64-byte TMA swizzle does (chunk c of row r at chunk c ^ ((r >> 1) & 3)); exponents into the permuted blocks at
+// xsf + kk * 512. Run by the 12 epilogue warps; warp ew takes the (token, 32-block) pairs ew, ew + 12, ...
+// The x values of the warp's first four pairs, loaded at kernel entry (before the weight stream saturates DRAM and
+// stretches load latency to microseconds).
+__device__ __forceinline__ void load_x4(const Args& a, const Geo& g, int ks0, int ew, int p0, float (&xs)[4]) {
   const int lane = threadIdx.x & 31;
-  uint8_t* xb = a.ws + a.L.xb;
-  uint8_t* xsf = a.ws + a.L.xsf + kt * 512;
-  for (int pr = ew; pr < 4 * g.T; pr += 4) {
-    const int t = pr / 4, blk = pr % 4;
-    const int i = kt * 128 + blk * 32 + lane;
-    const float xv = __uint_as_float((uint32_t)a.x[(int64_t)t * g.H + i] << 16);
-    uint32_t c[2];
-    int ex[2];
-    split_parts(xv, 2, c, ex);
+  const int nblk = 4 * g.KSG, npairs = nblk * g.T, step = 4 * NGRP;
 #pragma unroll
-    for (int p = 0; p < 2; ++p) {
-      xb[(int64_t)(2 * t + p) * g.H + i] = (uint8_t)c[p];
-      if (lane == 0) xsf[sfb(2 * t + p, blk)] = (uint8_t)ex[p];
+  for (int q = 0; q < 4; ++q) {
+    const int pr = p0 + q * step;
+    xs[q] = 0.f;
+    if (pr < npairs) {
+      const int t = pr / nblk, b = pr % nblk;
+      xs[q] = __uint_as_float((uint32_t)a.x[(int64_t)t * g.H + (ks0 * g.KSG + b / 4) * 128 + (b % 4) * 32 + lane] << 16);
+    }
+  }
+}
+
+__device__ void split_x_res(const Args& a, const Geo& g, int ks0, int ew, uint8_t* xres, uint8_t* xsf,
+                            const float (&xfirst)[4]) {
+  const int lane = threadIdx.x & 31;
+  const int nblk = 4 * g.KSG, npairs = nblk * g.T, step = 4 * NGRP;
+  for (int p0 = ew; p0 < npairs; p0 += 4 * step) {
+    float xs[4];
+    if (p0 == ew) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) xs[q] = xfirst[q];
+    } else {
+      load_x4(a, g, ks0, ew, p0, xs);
+    }
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {
+      const int pr = p0 + q * step;
+      if (pr >= npairs) break;
+      const int t = pr / nblk, b = pr % nblk, kk = b / 4, kb = b % 4;
+      // parts as in split_parts_n, stored as they are produced
+      float r = xs[q];
+      const float am = warp_amax(r);
+      const bool nonfinite = !(am <= 3.4028235e38f);
+      const int e0 = mx4_exp(am);
+#pragma unroll
+      for (int p = 0; p < PARTS; ++p) {
+        const int e = nonfinite ? 255 : (e0 - 2 * p > 1 ? e0 - 2 * p : 1);
+        const uint32_t c = nonfinite ? 0u : e2m1_code(r * pow2_127m(e));
+        const uint32_t hi = __shfl_down_sync(0xFFFFFFFFu, c, 1);
+        if (!nonfinite) r = r - e2m1_value(c) * pow2_m127(e);
+        const int n = PARTS * t + p;
+        if (!(lane & 1)) xres[kk * XRES_TILE + n * 64 + ((kb ^ ((n >> 1) & 3)) << 4) + (lane >> 1)] = (uint8_t)(c | (hi << 4));
+        if (lane == 0) xsf[kk * 512 + sfb(n, kb)] = (uint8_t)e;
+      }
     }
   }
 }
 
 // All G segments of (expert u, row tile rt) are in: g, u of the 64 intermediate indices rt*64 .. +63 (tile rows
-// 0..63 gate, 64..127 up), h = SiLU(g) * u, three E4M3 parts per 32-block into the D operand rows 3s + p of u.
+// 0..63 gate, 64..127 up), h = SiLU(g) * u, PARTS E2M1 parts per 32-block into the D operand rows PARTS * s + p.
 // Threads et < 64 (two whole warps, one 32-block each) do the work.
 __device__ void finalize_h(const Args& a, const Geo& g, const Tables& tb, int u, int rt, int et) {
   if (et >= 64) return;
   const float* gp = reinterpret_cast<const float*>(a.ws + a.L.gpart) + ((int64_t)u * g.RTG + rt) * g.SG * a.ts * 128;
   const int i = rt * 64 + et, kt = i / 128, kb = (i % 128) / 32;
-  uint8_t* hb = a.ws + a.L.hb + (int64_t)u * HROWS * g.I;
+  uint8_t* hb = a.ws + a.L.hb + (int64_t)u * HROWS * (g.I / 2);
   uint8_t* hsf = a.ws + a.L.hsf + ((int64_t)u * g.KTD + kt) * 512;
   const int nt = tb.ntok[u];
   for (int s = 0; s < nt; ++s) {
@@ -276,13 +380,13 @@ __device__ void finalize_h(const Args& a, const Geo& g, const Tables& tb, int u,
         if (k0 + q < g.SG) { gv += gl[q]; uv += ul[q]; }
     }
     const float h = gv / (1.0f + expf(-gv)) * uv;
-    uint32_t c[3];
-    int ex[3];
-    split_parts(h, 3, c, ex);
+    uint32_t c[PARTS];
+    int ex[PARTS];
+    split_parts(h, c, ex);
 #pragma unroll
-    for (int p = 0; p < 3; ++p) {
-      hb[(int64_t)(3 * s + p) * g.I + i] = (uint8_t)c[p];
-      if ((et & 31) == 0) hsf[sfb(3 * s + p, kb)] = (uint8_t)ex[p];
+    for (int p = 0; p < PARTS; ++p) {
+      if (!(et & 1)) hb[(int64_t)(PARTS * s + p) * (g.I / 2) + i / 2] = (uint8_t)c[p];
+      if ((et & 31) == 0) hsf[sfb(PARTS * s + p, kb)] = (uint8_t)ex[p];
     }
   }
 }
@@ -316,7 +420,7 @@ __device__ void combine_rows(const Args& a, const Geo& g, const Tables& tb, int 
   }
 }
 
-__device__ void epilogue(const Args& a, const Geo& g, const Tables& tb, uint32_t tbase, uint64_t (*acc_full)[2],
+__device__ void epilogue(const Args& a, const Geo& g, const Tables& tb, const Order& ord, uint32_t tbase, uint64_t (*acc_full)[2],
                          uint64_t (*acc_empty)[2], uint64_t (*uq_full)[QN], volatile int (*uq)[QN], uint32_t* cnt,
                          volatile int* s_last, volatile int* s_ok, volatile int* s_unit, volatile int* s_abort) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = warp & 3;
@@ -325,11 +429,6 @@ __device__ void epilogue(const Args& a, const Geo& g, const Tables& tb, uint32_t
   const int et = threadIdx.x - (EPI_WARP0 + 4 * grp) * 32;       // 0..127 inside the group
   const int m = q * 32 + lane;                                   // TMEM lane = weight row of the tile
   const long long lim = a.wait_ns;
-  if (grp == 0 && g.nG > 0 && (int)blockIdx.x < g.KTG) {
-    split_x(a, g, blockIdx.x, warp - EPI_WARP0);
-    named_bar(bar, 128);
-    if (et == 0) red_release_add(cnt + C_XREADY, 1u);
-  }
   float* gpart = reinterpret_cast<float*>(a.ws + a.L.gpart);
   float* dpart = reinterpret_cast<float*>(a.ws + a.L.dpart);
   // the units pipeline j = grp took, in order (each accumulator's phases in order)
@@ -350,12 +449,20 @@ __device__ void epilogue(const Args& a, const Geo& g, const Tables& tb, uint32_t
     if (s_ok[grp] != 1) break;
     tc_fence_after();
     const int i = s_unit[grp];
-    const Unit un = unit_of((int)blockIdx.x + i * (int)gridDim.x, g);
-    const uint32_t taddr = tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)(64 * j + 32 * ab);
-    uint32_t v0[16], v1[16];
-    tc_ld16(taddr, v0);
-    if (un.d) tc_ld16(taddr + 16, v1);
-    tc_wait_ld();
+    const Unit un = unit_of((int)blockIdx.x + i * (int)gridDim.x, g, ord);
+    const uint32_t taddr = tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)(128 * j + 64 * ab);
+    // column t * PARTS + p = part p of token (or slot) t; sum the parts of each column group in part order
+    float acc[MAX_T];
+#pragma unroll
+    for (int t = 0; t < MAX_T; ++t) acc[t] = 0.f;
+#pragma unroll
+    for (int cb = 0; cb < NB / 16; ++cb) {
+      uint32_t v[16];
+      tc_ld16(taddr + 16 * cb, v);
+      tc_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 16; ++c) acc[(16 * cb + c) / PARTS] += __uint_as_float(v[c]);
+    }
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(&acc_empty[j][ab]);
@@ -363,20 +470,13 @@ __device__ void epilogue(const Args& a, const Geo& g, const Tables& tb, uint32_t
       float* gp = gpart + (((int64_t)un.u * g.RTG + un.rt) * g.SG + un.ks) * a.ts * 128 + m;
 #pragma unroll
       for (int t = 0; t < MAX_T; ++t)
-        if (t < g.T) gp[t * 128] = __uint_as_float(v0[2 * t]) + __uint_as_float(v0[2 * t + 1]);
+        if (t < g.T) gp[t * 128] = acc[t];
     } else {
       float* dp = dpart + (((int64_t)un.u * g.RTD + un.rt) * g.SD + un.ks) * a.ts * 128 + m;
       const int nt = tb.ntok[un.u];
 #pragma unroll
-      for (int s = 0; s < MAX_T; ++s) {
-        if (s < nt) {
-          const int c0 = 3 * s;
-          const float p0 = __uint_as_float(c0 < 16 ? v0[c0] : v1[c0 - 16]);
-          const float p1 = __uint_as_float(c0 + 1 < 16 ? v0[c0 + 1] : v1[c0 + 1 - 16]);
-          const float p2 = __uint_as_float(c0 + 2 < 16 ? v0[c0 + 2] : v1[c0 + 2 - 16]);
-          dp[s * 128] = (p0 + p1) + p2;
-        }
-      }
+      for (int s = 0; s < MAX_T; ++s)
+        if (s < nt) dp[s * 128] = acc[s];
     }
     // count the unit; the one that completes a group of units does the group's follow-up work
     named_bar(bar, 128);
@@ -391,7 +491,7 @@ __device__ void epilogue(const Args& a, const Geo& g, const Tables& tb, uint32_t
       if (!un.d) {
         finalize_h(a, g, tb, un.u, un.rt, et);
         named_bar(bar, 128);
-        if (et == 0) red_release_add(cnt + C_HREADY + un.u, 1u);
+        if (et == 0) red_release_add(cnt + C_HREADY + un.u * 16 + (un.rt * 64) / (128 * g.KSD), 1u);
       } else {
         combine_rows(a, g, tb, un.rt, et);
       }
@@ -401,17 +501,19 @@ __device__ void epilogue(const Args& a, const Geo& g, const Tables& tb, uint32_t
 
 __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constant__ CUtensorMap tm_gu,
                                                             const __grid_constant__ CUtensorMap tm_dn,
-                                                            const __grid_constant__ CUtensorMap tm_x,
                                                             const __grid_constant__ CUtensorMap tm_h, const Args a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ __align__(8) uint64_t full[NSLOT], empty[NSLOT], acc_full[NPIPE][2], acc_empty[NPIPE][2], drain[NPIPE];
-  __shared__ __align__(8) uint64_t uq_full[NPIPE][QN];
+  __shared__ __align__(8) uint64_t uq_full[NPIPE][QN], xres_full;
+  uint8_t* xres = smem + NSLOT * SLOT_BYTES;    // resident x parts of this CTA's gate/up K segment
+  uint8_t* xres_sf = xres + 8 * XRES_TILE;
   __shared__ volatile int uq[NPIPE][QN];
   __shared__ int s_next;
   __shared__ Tables tb;
+  __shared__ Order ord;
   __shared__ uint32_t s_tmem;
-  __shared__ int s_units;
+  __shared__ int s_units, s_has_g;
   __shared__ volatile int s_abort, s_ok[NGRP], s_last[NGRP], s_unit[NGRP];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -419,21 +521,25 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
   uint32_t* cnt = reinterpret_cast<uint32_t*>(a.ws + kCnt);
   Geo g = a.g;
   const long long lim = a.wait_ns;
+  float xfirst[4] = {0.f, 0.f, 0.f, 0.f};
+  if (warp >= EPI_WARP0) load_x4(a, g, (int)blockIdx.x % g.SG, warp - EPI_WARP0, warp - EPI_WARP0, xfirst);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NSLOT; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int s = 0; s < NSLOT; ++s) { mbar_init(&full[s], 2); mbar_init(&empty[s], 1); }  // full: both producers arrive
     for (int j = 0; j < NPIPE; ++j) {
       mbar_init(&acc_full[j][0], 1); mbar_init(&acc_full[j][1], 1);
       mbar_init(&acc_empty[j][0], 4); mbar_init(&acc_empty[j][1], 4);  // the 4 warps of one epilogue group
       mbar_init(&drain[j], 1);
       for (int e = 0; e < QN; ++e) mbar_init(&uq_full[j][e], 1);
     }
+    mbar_init(&xres_full, 1);
     s_abort = 0;
     s_next = 0;
     fence_mbar_init();
     build_tables(tb, a.idx, g.T, g.k, a.E);
     if (tb.bad) { s_abort = 1; if (blockIdx.x == 0) record_error(&hdr->status, MOE_ERR_INVALID_ARG); }
     s_units = tb.bad ? 0 : tb.U * (g.RTG * g.SG + g.RTD * g.SD);
+    build_order(ord, g, tb.bad ? 0 : tb.U);
   }
   if (warp == 1) tc_alloc(&s_tmem, TMEM_COLS);
   tc_fence_before();
@@ -449,56 +555,69 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
   // next i from a shared counter when they start a unit, so a pipeline waiting for h does not hold up the rest;
   // each publishes the ids it took through its queue uq[j] to its MMA thread and epilogue group.
   const int my_units = nunits > (int)blockIdx.x ? (nunits - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  if (threadIdx.x == 0) {  // does any of this CTA's units need the resident x parts?
+    int hg = 0;
+    for (int i = 0; i < my_units && !hg; ++i) hg = unit_of((int)blockIdx.x + i * (int)gridDim.x, g, ord).d == 0;
+    s_has_g = hg;
+  }
+  __syncthreads();
+  const bool has_g = s_has_g != 0;
 
-  if (warp == 0) {
-    // ---------------- producers: lane j feeds pipeline j
-    if (lane < NPIPE) {
-      const int j = lane;
-      int n = 0;  // stages issued by this pipeline
-      bool ok = true, x_ok = false, partial = false;
+  if (warp < 2 * NPIPE) {
+    // ---------------- producers, two warps per pipeline j (lane 0 issues): warp j streams the weight tiles of
+    // every stage (no dependency, so weights keep flowing while activations are not ready), warp NPIPE + j adds
+    // the activation parts of each stage once they exist (x split done; h of the expert finalised). Each posts its
+    // own byte count on the stage's barrier.
+    const bool wprod = warp < NPIPE;
+    const int j = wprod ? warp : warp - NPIPE;
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int n = 0;  // stages of this pipeline
+      bool ok = true;
       int h_ok_u = -1;
       for (int c = 0; ok; ++c) {
-        const int i = atomicAdd(&s_next, 1);
-        // entry c % QN was last read for unit c - QN, which its epilogue group started before this pipeline's
-        // MMA could move past unit c - 2; the producer is at most RING stages ahead of the MMA
-        uq[j][c % QN] = i < my_units ? i : -1;
-        mbar_arrive(&uq_full[j][c % QN]);
-        if (i >= my_units) break;
-        const Unit un = unit_of((int)blockIdx.x + i * (int)gridDim.x, g);
+        int i;
+        if (wprod) {
+          i = atomicAdd(&s_next, 1);
+          // entry c % QN was last read for unit c - QN: the weight producer is at most RING stages ahead of the
+          // MMA, so (units having at least 2 stages) the MMA has started unit c - 3 and the epilogue group has
+          // finished unit c - 5; the activation producer is ahead of the MMA
+          uq[j][c % QN] = i < my_units ? i : -1;
+          mbar_arrive(&uq_full[j][c % QN]);
+        } else {
+          if (!bwait(&uq_full[j][c % QN], (uint32_t)((c / QN) & 1), &s_abort, lim)) { ok = false; break; }
+          i = uq[j][c % QN];
+        }
+        if (i < 0 || i >= my_units) break;
+        const Unit un = unit_of((int)blockIdx.x + i * (int)gridDim.x, g, ord);
         const int e = tb.ue[un.u];
         const int ks = un.d ? g.KSD : g.KSG;
+        const int KT = un.d ? g.KTD : g.KTG;
+        if (!wprod && un.d && h_ok_u != un.u * 16 + un.ks) {  // down: wait once for h of its K segment
+          const uint32_t* dep_cnt = cnt + C_HREADY + un.u * 16 + un.ks;
+          if (!wait_ge(dep_cnt, (uint32_t)(2 * g.KSD), &s_abort, lim)) { ok = false; break; }
+          asm volatile("fence.proxy.async.global;" ::: "memory");  // generic-proxy writes -> TMA reads
+          h_ok_u = un.u * 16 + un.ks;
+        }
         for (int kk = 0; kk < ks; ++kk, ++n) {
           const int slot = j * RING + (n % RING);
           const uint32_t ph = (uint32_t)((n / RING) & 1);
           if (!bwait(&empty[slot], ph ^ 1, &s_abort, lim)) { ok = false; break; }
           uint8_t* st = smem + slot * SLOT_BYTES;
-          if (!un.d) {
-            const int kt = un.ks * g.KSG + kk;
-            const int tile = un.rt * g.KTG + kt;
-            mbar_arrive_expect_tx(&full[slot], A_TX + XROWS * 128 + 1024);
-            tma_load_4d(st, &tm_gu, 0, 0, tile, e, &full[slot]);
-            bulk_g2s_plain(st + A_BYTES + B_BYTES, a.gu + (int64_t)e * a.gu_stride + (int64_t)tile * kTcTileBytes + 8192,
-                           512, &full[slot]);
-            if (!x_ok) {
-              if (!wait_ge(cnt + C_XREADY, (uint32_t)g.KTG, &s_abort, lim)) { ok = false; partial = true; break; }
-              asm volatile("fence.proxy.async.global;" ::: "memory");  // generic-proxy writes -> TMA reads
-              x_ok = true;
-            }
-            tma_load_2d(st + A_BYTES, &tm_x, kt * 128, 0, &full[slot]);
-            bulk_g2s_plain(st + A_BYTES + B_BYTES + 512, a.ws + a.L.xsf + kt * 512, 512, &full[slot]);
+          const int kt = un.ks * ks + kk;
+          if (wprod) {
+            const int tile = un.rt * KT + kt;
+            const uint8_t* wbase = un.d ? a.dn + (int64_t)e * a.dn_stride : a.gu + (int64_t)e * a.gu_stride;
+            // weights are read once per call: evict-first keeps them from displacing the instructions, partial
+            // sums and activation parts that the dependent steps read back through L2
+            mbar_arrive_expect_tx(&full[slot], A_BYTES + 512);
+            tma_load_4d_hint(st, un.d ? &tm_dn : &tm_gu, 0, 0, tile, e, &full[slot], pol);
+            bulk_g2s(st + A_BYTES + B_BYTES, wbase + (int64_t)tile * kTcTileBytes + 8192, 512, &full[slot], pol);
+          } else if (!un.d) {
+            mbar_arrive(&full[slot]);  // gate/up: the x parts are resident; nothing to copy
           } else {
-            const int kt = un.ks * g.KSD + kk;
-            const int tile = un.rt * g.KTD + kt;
-            mbar_arrive_expect_tx(&full[slot], A_TX + HROWS * 128 + 1024);
-            tma_load_4d(st, &tm_dn, 0, 0, tile, e, &full[slot]);
-            bulk_g2s_plain(st + A_BYTES + B_BYTES, a.dn + (int64_t)e * a.dn_stride + (int64_t)tile * kTcTileBytes + 8192,
-                           512, &full[slot]);
-            if (h_ok_u != un.u) {
-              if (!wait_ge(cnt + C_HREADY + un.u, (uint32_t)g.RTG, &s_abort, lim)) { ok = false; partial = true; break; }
-              asm volatile("fence.proxy.async.global;" ::: "memory");
-              h_ok_u = un.u;
-            }
-            tma_load_2d(st + A_BYTES, &tm_h, kt * 128, un.u * HROWS, &full[slot]);
+            mbar_arrive_expect_tx(&full[slot], B_BYTES + 512);
+            tma_load_2d(st + A_BYTES, &tm_h, kt * 64, un.u * HROWS, &full[slot]);
             bulk_g2s_plain(st + A_BYTES + B_BYTES + 512, a.ws + a.L.hsf + ((int64_t)un.u * g.KTD + kt) * 512, 512,
                            &full[slot]);
           }
@@ -506,50 +625,49 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
       }
       if (!ok) {
         record_error(&hdr->status, MOE_ERR_DEVICE_TIMEOUT);
-        // the weight copies of a stage whose activation copy never came leave the barrier short: wait (bounded)
-        // for what was issued so the shared memory is not released under a copy in flight
-        for (int q = 0; q < RING; ++q) {
-          const int m = n - 1 - q;
-          if (m >= 0) mbar_wait(&full[j * RING + (m % RING)], (uint32_t)((m / RING) & 1), 50000000LL);
-        }
-        if (partial) {  // stage n got its weight copies only: its barrier never completes, so give them 1 ms
-          const long long t0 = globaltimer_ns();
-          while (globaltimer_ns() - t0 < 1000000LL) __nanosleep(1000);
-        }
+        // a stage may hold the copies of one producer only, so its barrier never completes: give the copies this
+        // warp issued 1 ms to land before the CTA's shared memory is released
+        const long long t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 1000000LL) __nanosleep(1000);
       }
     }
     __syncwarp();
-  } else if (warp <= NPIPE) {
-    // ---------------- MMA issuers: warp 1 + j, lane 0, pipeline j
-    const int j = warp - 1;
+  } else if (warp < 3 * NPIPE) {
+    // ---------------- MMA issuers: lane 0 of warp 2 NPIPE + j, pipeline j
+    const int j = warp - 2 * NPIPE;
     if (lane == 0) {
       int n = 0, c = 0;
-      bool ok = true;
+      bool ok = true, xres_ok = false;
       const uint32_t sfa_col = tbase + SF_COL0;
       for (;; ++c) {
         if (!bwait(&uq_full[j][c % QN], (uint32_t)((c / QN) & 1), &s_abort, lim)) { ok = false; break; }
         const int i = uq[j][c % QN];
         if (i < 0) break;
-        const Unit un = unit_of((int)blockIdx.x + i * (int)gridDim.x, g);
+        const Unit un = unit_of((int)blockIdx.x + i * (int)gridDim.x, g, ord);
         const int ab = c & 1;
         if (!bwait(&acc_empty[j][ab], ((c >> 1) & 1) ^ 1, &s_abort, lim)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t d_tmem = tbase + (uint32_t)(64 * j + 32 * ab);
+        const uint32_t d_tmem = tbase + (uint32_t)(128 * j + 64 * ab);
         const int ks = un.d ? g.KSD : g.KSG;
-        const uint32_t N = un.d ? HROWS : XROWS;
+        if (!un.d && !xres_ok) {  // the resident x parts (built by the epilogue warps at start)
+          if (!bwait(&xres_full, 0, &s_abort, lim)) { ok = false; break; }
+          xres_ok = true;
+        }
         for (int kk = 0; kk < ks; ++kk, ++n) {
           const int slot = j * RING + (n % RING);
           if (!bwait(&full[slot], (uint32_t)((n / RING) & 1), &s_abort, lim)) { ok = false; break; }
           tc_fence_after();
           uint8_t* st = smem + slot * SLOT_BYTES;
           const uint32_t sfa = sfa_col + (uint32_t)(slot * 8), sfbc = sfa + 4;
+          // B: gate/up from the resident x parts (k-tile kk of the CTA's segment), down from the stage
+          const uint8_t* bsrc = un.d ? st + A_BYTES : xres + kk * XRES_TILE;
+          const uint8_t* bsf = un.d ? st + A_BYTES + B_BYTES + 512 : xres_sf + kk * 512;
           tc_cp_sf(sfa, umma_desc_sf(smem_u32(st + A_BYTES + B_BYTES)));
-          tc_cp_sf(sfbc, umma_desc_sf(smem_u32(st + A_BYTES + B_BYTES + 512)));
-          const uint64_t ad = umma_desc_sw128(smem_u32(st)), bd = umma_desc_sw128(smem_u32(st + A_BYTES));
+          tc_cp_sf(sfbc, umma_desc_sf(smem_u32(bsf)));
+          const uint64_t ad = umma_desc_sw64(smem_u32(st)), bd = umma_desc_sw64(smem_u32(bsrc));
 #pragma unroll
-          for (int kb = 0; kb < 4; ++kb)
-            tc_mma_mxf8f6f4(d_tmem, ad + 2 * kb, bd + 2 * kb, idesc_mxf8f6f4(5, 0, 128, N, kb, kb), sfa, sfbc,
-                            (kk | kb) != 0);
+          for (int kh = 0; kh < 2; ++kh)  // two K = 64 halves of the 128-column tile, scale bytes 2kh, 2kh + 1
+            tc_mma_mxf4(d_tmem, ad + 2 * kh, bd + 2 * kh, idesc_mxf4(128, NB, 2 * kh), sfa, sfbc, (kk | kh) != 0);
           tc_commit(&empty[slot]);
         }
         if (ok) tc_commit(&acc_full[j][ab]);
@@ -560,8 +678,14 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
     }
     __syncwarp();
   } else {
-    // ---------------- epilogue warps (see the second part of this file)
-    epilogue(a, g, tb, tbase, acc_full, acc_empty, uq_full, uq, cnt, s_last, s_ok, s_unit, &s_abort);
+    // ---------------- epilogue warps: first the resident x parts of the CTA's gate/up segment
+    if (has_g) {
+      split_x_res(a, g, (int)blockIdx.x % g.SG, warp - EPI_WARP0, xres, xres_sf, xfirst);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> MMA (async proxy) reads
+      named_bar(1 + NGRP, 4 * NGRP * 32);
+      if (warp == EPI_WARP0 && lane == 0) mbar_arrive(&xres_full);
+    }
+    epilogue(a, g, tb, ord, tbase, acc_full, acc_empty, uq_full, uq, cnt, s_last, s_ok, s_unit, &s_abort);
   }
   tc_fence_before();
   __syncthreads();
@@ -573,8 +697,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
     const uint32_t old = atomicAdd(cnt + C_DONE, 1u);
     if (old == gridDim.x - 1) {
       __threadfence();
-      cnt[C_XREADY] = 0;
-      for (int u = 0; u < tb.U; ++u) cnt[C_HREADY + u] = 0;
+      for (int q = 0; q < tb.U * 16; ++q) cnt[C_HREADY + q] = 0;
       for (int q = 0; q < tb.U * g.RTG; ++q) cnt[C_G + q] = 0;
       for (int q = 0; q < g.RTD; ++q) cnt[C_D + q] = 0;
       __threadfence();
@@ -601,7 +724,6 @@ moe_status_t run(const moe_layer_t* L, const void* x, int T, const int32_t* idx,
     if (ws_bytes >= workspace_bytes(L, tm, k)) { tmax = tm; break; }
   if (!tmax) return MOE_ERR_WORKSPACE_TOO_SMALL;
   if (!moe_internal::tmap_available()) return MOE_ERR_CUDA;
-  if (moe_internal::num_sms() < L->H / 128) return MOE_ERR_UNSUPPORTED_ARCH;  // x is split by CTAs 0 .. H/128 - 1
   Args a;
   a.gu = (const uint8_t*)L->gate_up;
   a.dn = (const uint8_t*)L->down;
@@ -621,17 +743,15 @@ moe_status_t run(const moe_layer_t* L, const void* x, int T, const int32_t* idx,
   a.wait_ns = kDefaultWaitNs;
   Geo& g = a.g;
   g.H = L->H; g.I = L->I; g.T = T; g.k = k; g.U = 0;
-  g.RTG = 2 * L->I / 128; g.KTG = L->H / 128; g.KSG = ks_for(g.KTG); g.SG = g.KTG / g.KSG;
-  g.RTD = L->H / 128;     g.KTD = L->I / 128; g.KSD = ks_for(g.KTD); g.SD = g.KTD / g.KSD;
+  g.RTG = 2 * L->I / 128; g.KTG = L->H / 128; g.KSG = ks_for_g(g.KTG); g.SG = g.KTG / g.KSG;
+  g.RTD = L->H / 128;     g.KTD = L->I / 128; g.KSD = ks_for_d(g.KTD); g.SD = g.KTD / g.KSD;
   g.nG = g.nD = 0;
-  CUtensorMap mgu, mdn, mx, mh;
-  const uint64_t xd[2] = {(uint64_t)L->H, (uint64_t)XROWS}, xs[1] = {(uint64_t)L->H};
-  const uint64_t hd[2] = {(uint64_t)L->I, (uint64_t)(umax * HROWS)}, hs[1] = {(uint64_t)L->I};
-  const uint32_t xbox[2] = {128, XROWS}, hbox[2] = {128, HROWS};
-  if (!moe_internal::tmap_tc_weights(&mgu, L->gate_up, MOE_MAT_GATE_UP, L->H, L->I, L->E) ||
-      !moe_internal::tmap_tc_weights(&mdn, L->down, MOE_MAT_DOWN, L->H, L->I, L->E) ||
-      !moe_internal::tmap_u8(&mx, a.ws + a.L.xb, 2, xd, xs, xbox) ||
-      !moe_internal::tmap_u8(&mh, a.ws + a.L.hb, 2, hd, hs, hbox))
+  CUtensorMap mgu, mdn, mh;
+  const uint64_t hd[2] = {(uint64_t)L->I / 2, (uint64_t)(umax * HROWS)}, hs[1] = {(uint64_t)L->I / 2};
+  const uint32_t hbox[2] = {64, HROWS};
+  if (!moe_internal::tmap_tc_weights_packed(&mgu, L->gate_up, MOE_MAT_GATE_UP, L->H, L->I, L->E) ||
+      !moe_internal::tmap_tc_weights_packed(&mdn, L->down, MOE_MAT_DOWN, L->H, L->I, L->E) ||
+      !moe_internal::tmap_u8(&mh, a.ws + a.L.hb, 2, hd, hs, hbox, 64))
     return MOE_ERR_CUDA;
   static std::once_flag once;
   static bool attr_ok = false;
@@ -640,7 +760,8 @@ moe_status_t run(const moe_layer_t* L, const void* x, int T, const int32_t* idx,
   });
   if (!attr_ok) return MOE_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(moe_internal::num_sms());
+  const int nsm = moe_internal::num_sms();
+  cfg.gridDim = dim3(nsm - nsm % g.SG);  // a multiple of S_G: every gate/up unit of a CTA has the same K segment
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = SMEM;
   cfg.stream = (cudaStream_t)stream;
@@ -649,7 +770,7 @@ moe_status_t run(const moe_layer_t* L, const void* x, int T, const int32_t* idx,
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, decode_kernel, mgu, mdn, mx, mh, a) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, decode_kernel, mgu, mdn, mh, a) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }
 

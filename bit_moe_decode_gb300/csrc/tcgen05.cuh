@@ -1,6 +1,6 @@
 // tcgen05.cuh -- 5th-generation tensor core (tcgen05 / TMEM) and TMA tensor-copy wrappers for sm_103a.
 //
-// Conventions established on GB300 and relied on by prefill.cu:
+// Conventions established on GB300 and relied on by prefill.cu and decode_tc.cu:
 //   * Operands in shared memory are K-major with the 128-byte swizzle (TMA CU_TENSOR_MAP_SWIZZLE_128B):
 //     rows of 128 bytes, 8-row atoms of 1024 bytes. FP4 (E2M1) weights are loaded with the TMA type 16U4_ALIGN16B,
 //     which expands every 16 packed codes (8 bytes, low nibble first) to 16 bytes; the transaction count is the
@@ -10,6 +10,9 @@
 //     operand reads lane m, column base + m/32; the four columns are replicated into every 32-lane quarter, which
 //     tcgen05.cp .32x128b.warpx4 does from a 512-byte block laid out as byte (l*16 + c*4 + kb) = scale of row
 //     (l + 32c), K-block kb.
+//   * Packed E2M1 (kind::mxf4, both operands FP4, K = 64 per instruction): rows of 64 bytes (128 codes, even k in
+//     the low nibble) loaded by byte-typed TMA with the 64-byte swizzle; the second K = 64 half starts 32 bytes
+//     further; scale_vec::2X reads scale bytes (0, 1) and (2, 3) of the same columns for the two halves.
 #pragma once
 #include <cstdint>
 
@@ -27,6 +30,8 @@ __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint
 }
 // K-major, 128-byte swizzle, 8-row atoms of 1024 bytes
 __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) { return umma_desc(saddr, 16, 1024, 2); }
+// K-major, 64-byte swizzle, 8-row atoms of 512 bytes (packed E2M1 operands of kind::mxf4: 128 codes per row)
+__device__ __forceinline__ uint64_t umma_desc_sw64(uint32_t saddr) { return umma_desc(saddr, 16, 512, 4); }
 // 32 rows x 16 bytes of scale factors, no swizzle (source of tcgen05.cp .32x128b)
 __device__ __forceinline__ uint64_t umma_desc_sf(uint32_t saddr) { return umma_desc(saddr, 16, 128, 0); }
 
@@ -36,6 +41,12 @@ __host__ __device__ __forceinline__ uint32_t idesc_mxf8f6f4(uint32_t a_fmt, uint
                                                             uint32_t a_sf_id, uint32_t b_sf_id) {
   return (b_sf_id << 4) | (a_fmt << 7) | (b_fmt << 10) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) |
          (a_sf_id << 29);
+}
+
+// Instruction descriptor, kind::mxf4 block-scaled (E2M1 x E2M1, format code 1), fp32 accumulate, K-major, UE8M0
+// scales with scale_vec::2X: one K = 64 instruction uses scale bytes sf_id and sf_id + 1 (sf_id 0 or 2).
+__host__ __device__ __forceinline__ uint32_t idesc_mxf4(uint32_t M, uint32_t N, uint32_t sf_id) {
+  return (sf_id << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) | (sf_id << 29);
 }
 
 __device__ __forceinline__ void tc_alloc(uint32_t* smem_dst, uint32_t ncols) {
@@ -53,6 +64,14 @@ __device__ __forceinline__ void tc_mma_mxf8f6f4(uint32_t d_tmem, uint64_t adesc,
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }
@@ -94,6 +113,15 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, int x, 
       "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(
           smem_u32(dst)),
       "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+      : "memory");
+}
+// the same with an L2 cache policy (e.g. evict-first for data read once)
+__device__ __forceinline__ void tma_load_4d_hint(void* dst, const void* tmap, int x, int y, int z, int w, uint64_t* bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3, %4, "
+      "%5}], [%6], %7;" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
 // plain 1-D bulk copy without an L2 hint
