@@ -322,7 +322,10 @@ def run_ours(args):
             "ffn_pct_of_8tbs": round(100 * alg_bytes / (ffn_us * 1e-6) / 8e12, 2),
             "mean_unique_experts": float(uniq),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": None,
+                         "frac": round(achieved / peak, 4),
+                         # dram__bytes_read + dram__bytes_write per launch from the ncu capture summarised in
+                         # profiles/decode_kernel_mxfp4_ds4_t1.md (the tensor-core MXFP4 kernel as it stands)
+                         "traffic": 82176000 if use_tc else None,
                          "kernel": "decode_kernel (tcgen05)" if use_tc else "ffn_kernel<%s>" % args.fmt,
                          "bytes_per_launch": alg_bytes,
                          "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if peaks else "fallback"},
