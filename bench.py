@@ -107,6 +107,11 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------------------------ GPU arm
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the tensor-core decode kernel as it stands, from the
+# ncu capture summarised in profiles/decode_kernel_mxfp4_ds4_t1.md (None until that capture matches the kernel)
+TC_TRAFFIC = None
+
+
 def run_ours(args):
     import torch
     import bit_moe_decode_gb300 as m
@@ -162,10 +167,15 @@ def run_ours(args):
     ws = layer.workspace(1, K_TOP)
     stream = torch.cuda.Stream(device=dev)
 
+    fused = use_tc and E <= 256   # router + FFN in one launch (the router's logits spread over the whole grid)
+
     def step_launch():
         for t in range(T):
-            m.moe_route_topk(wr, x[t], 1, H, E, K_TOP, None, None, 0, idx[t], w[t], stream=stream)
-            m.moe_expert_ffn_decode(layer, x[t], idx[t], w[t], K_TOP, y[t], None, False, ws, stream=stream)
+            if fused:
+                m.moe_route_expert_ffn(layer, wr, x[t], 1, K_TOP, idx[t], w[t], y[t], None, False, ws, stream=stream)
+            else:
+                m.moe_route_topk(wr, x[t], 1, H, E, K_TOP, None, None, 0, idx[t], w[t], stream=stream)
+                m.moe_expert_ffn_decode(layer, x[t], idx[t], w[t], K_TOP, y[t], None, False, ws, stream=stream)
 
     def ffn_only_launch():
         for t in range(T):
@@ -313,7 +323,8 @@ def run_ours(args):
                        "layout": "tc" if use_tc else "decode",
                        "l2": "inputs larger than L2 (3.4 GB of experts, random routing)",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
-            "gpu_launches": 2 * T * args.steps,
+            "gpu_launches": (1 if fused else 2) * T * args.steps,
+            "step_kernels": "moe_route_expert_ffn (router + FFN, one launch)" if fused else "moe_route_topk + moe_expert_ffn_decode",
             "hbm_gbs_step": round(alg_bytes * T / (ms_step * 1e-3) / 1e9, 1),
             "pct_of_8tbs_step": round(100 * alg_bytes * T / (ms_step * 1e-3) / 8e12, 2),
             "ffn_kernel_us": round(ffn_us, 3),
@@ -325,7 +336,7 @@ def run_ours(args):
                          "frac": round(achieved / peak, 4),
                          # dram__bytes_read + dram__bytes_write per launch from the ncu capture summarised in
                          # profiles/decode_kernel_mxfp4_ds4_t1.md (the tensor-core MXFP4 kernel as it stands)
-                         "traffic": 82176000 if use_tc else None,
+                         "traffic": TC_TRAFFIC if use_tc else None,
                          "kernel": "decode_kernel (tcgen05)" if use_tc else "ffn_kernel<%s>" % args.fmt,
                          "bytes_per_launch": alg_bytes,
                          "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if peaks else "fallback"},

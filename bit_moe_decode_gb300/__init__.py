@@ -29,8 +29,8 @@ BLOCK = {MOE_FMT_MXFP4: (32, 17), MOE_FMT_INT4G32: (32, 18), MOE_FMT_Q2K: (256, 
 # every symbol include/moe.h declares
 EXPORTS = ["moe_status_string", "moe_version", "moe_check_device", "moe_canonical_bytes", "moe_packed_bytes",
            "moe_encode_blocks", "moe_pack_weights", "moe_route_topk", "moe_workspace_bytes", "moe_workspace_init",
-           "moe_get_device_status", "moe_expert_ffn_decode", "moe_expert_ffn_verify", "moe_debug_unpack",
-           "moe_debug_timeout_probe", "moe_expert_ffn_decode_static", "moe_prefill_workspace_bytes",
+           "moe_get_device_status", "moe_expert_ffn_decode", "moe_expert_ffn_verify", "moe_route_expert_ffn",
+           "moe_debug_unpack", "moe_debug_timeout_probe", "moe_expert_ffn_decode_static", "moe_prefill_workspace_bytes",
            "moe_expert_grouped_gemm_prefill", "moe_debug_prefill"]
 
 
@@ -71,6 +71,7 @@ def lib() -> C.CDLL:
             "moe_get_device_status": (C.c_int, [P, P]),
             "moe_expert_ffn_decode": (C.c_int, [LP, P, P, P, i32, P, P, i32, P, sz, P]),
             "moe_expert_ffn_verify": (C.c_int, [LP, P, i32, P, P, i32, P, P, i32, P, sz, P]),
+            "moe_route_expert_ffn": (C.c_int, [LP, P, P, i32, i32, P, P, P, P, i32, P, sz, P]),
             "moe_debug_unpack": (C.c_int, [C.c_int, C.c_int, C.c_int, P, i64, i64, i64, P, P]),
             "moe_debug_timeout_probe": (C.c_int, [P, sz, i32, P]),
             "moe_expert_ffn_decode_static": (C.c_int, [LP, P, P, P, i32, P, P, i32, P]),
@@ -166,6 +167,15 @@ def moe_expert_ffn_verify(layer: "Layer", x_bf16, T: int, idx, w, k: int, y, y_b
     _check(lib().moe_expert_ffn_verify(C.byref(layer.c), _ptr(x_bf16), T, _ptr(idx), _ptr(w), k, _ptr(y),
                                        _ptr(y_bf16), int(accumulate), _ptr(ws), ws.numel() * ws.element_size(),
                                        _stream(stream)), "moe_expert_ffn_verify")
+
+
+def moe_route_expert_ffn(layer: "Layer", router_w_f16, x_bf16, T: int, k: int, idx, w, y, y_bf16=None,
+                         accumulate: bool = False, ws=None, stream=None):
+    """Router top-k and expert FFN in one launch (tensor-core layout, MXFP4, E <= 256): writes idx [T, k] and
+    w [T, k] (equal to moe_route_topk's) and y (equal to moe_expert_ffn_verify's with that routing)."""
+    _check(lib().moe_route_expert_ffn(C.byref(layer.c), _ptr(router_w_f16), _ptr(x_bf16), T, k, _ptr(idx), _ptr(w),
+                                      _ptr(y), _ptr(y_bf16), int(accumulate), _ptr(ws), ws.numel() * ws.element_size(),
+                                      _stream(stream)), "moe_route_expert_ffn")
 
 
 def moe_expert_ffn_decode_static(layer: "Layer", x_bf16, idx, w, k: int, y, y_bf16=None, accumulate: bool = False,

@@ -18,8 +18,11 @@ int num_sms();
 
 // decode / verify of MXFP4 experts in MOE_LAYOUT_TC on tcgen05 (decode_tc.cu); arguments checked by the caller
 size_t tc_decode_workspace_bytes(const moe_layer_t* L, int T_max, int k);
+// router_w != NULL: route inside the kernel (fp16 router [E][H], E <= 256), writing idx_out / w_out ([T][k]);
+// idx / w are then unused
 moe_status_t tc_decode(const moe_layer_t* L, const void* x, int T, const int32_t* idx, const float* w, int k, float* y,
-                       void* y_bf16, int accumulate, void* ws, size_t ws_bytes, void* stream);
+                       void* y_bf16, int accumulate, void* ws, size_t ws_bytes, void* stream,
+                       const void* router_w = nullptr, int32_t* idx_out = nullptr, float* w_out = nullptr);
 
 // TMA tensor maps (host-side encoding through the runtime's driver entry point; false if it is unavailable or
 // rejects the arguments). tmap_tc_weights: the E2M1 code tiles of a MOE_LAYOUT_TC matrix as a 4-D map

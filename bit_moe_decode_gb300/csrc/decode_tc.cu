@@ -33,6 +33,7 @@
 #include "common.cuh"
 #include "layout.cuh"
 #include "tcgen05.cuh"
+#include "route.cuh"
 #include "api_internal.h"
 
 namespace moe {
@@ -47,7 +48,7 @@ constexpr int A_BYTES = 8192;            // 128 rows x 64 B of packed E2M1 weigh
 constexpr int B_BYTES = NB * 64;         // 48 rows x 64 B of packed E2M1 activation parts
 constexpr int SLOT_BYTES = A_BYTES + B_BYTES + 1024;  // + two 512-byte exponent blocks; 12 KB
 constexpr int MAX_T = 8, MAX_K = 8, MAX_U = MAX_T * MAX_K;
-constexpr int XROWS = NB, HROWS = NB;    // B rows of the x parts and of each expert's h parts
+constexpr int HROWS = NB;                // B rows of each expert's h parts
 constexpr int EPI_WARP0 = 3 * NPIPE;     // warps: 2 NPIPE producers, NPIPE MMA issuers, then the epilogue groups
 // (each issuing thread has a warp of its own: issuing lanes that share a warp diverge and run one after another)
 constexpr int NGRP = NPIPE;              // epilogue groups of 4 warps; group j drains pipeline j
@@ -83,9 +84,10 @@ __host__ __device__ inline int ks_for_d(int kt) { return kt % 4 == 0 ? 4 : 2; }
 // with Umax = T_max * k union experts and TS = T_max token columns of the partial buffers.
 constexpr int64_t kCnt = 256;
 constexpr int C_DONE = 1, C_HREADY = 2, C_G = C_HREADY + MAX_U * 16, C_D = C_G + MAX_U * 64;
-constexpr int C_END = C_D + 32;
+constexpr int C_ROUTE = C_D + 32;      // experts whose logits are in (routing inside the kernel)
+constexpr int C_END = C_ROUTE + 1;
 struct Ws {
-  int64_t hb, hsf, gpart, dpart, total;
+  int64_t hb, hsf, gpart, dpart, lg, total;
 };
 inline int64_t al1k(int64_t v) { return (v + 1023) & ~(int64_t)1023; }
 inline Ws ws_layout(int64_t H, int64_t I, int64_t Umax, int64_t TS) {
@@ -97,6 +99,7 @@ inline Ws ws_layout(int64_t H, int64_t I, int64_t Umax, int64_t TS) {
   w.hsf = o;   o = al1k(o + Umax * KTD * 512);
   w.gpart = o; o = al1k(o + Umax * RTG * SG * TS * 128 * 4);
   w.dpart = o; o = al1k(o + Umax * RTD * SD * TS * 128 * 4);
+  w.lg = o;    o = al1k(o + (int64_t)kRouteTPC * kRouteMaxE * 4);  // router logits [token][expert]
   w.total = o;
   return w;
 }
@@ -106,8 +109,11 @@ struct Args {
   const uint8_t* dn;          // down weights
   int64_t gu_stride, dn_stride;
   const uint16_t* x;          // [T][H] bf16
-  const int32_t* idx;         // [T][k]
+  const int32_t* idx;         // [T][k] (routing given), or
   const float* w;             // [T][k]
+  const uint16_t* wr;         // [E][H] fp16 router: route inside the kernel, writing idx_out / w_out
+  int32_t* idx_out;
+  float* w_out;
   float* y;                   // [T][H]
   __nv_bfloat16* yb;          // [T][H] or NULL
   int accumulate;
@@ -276,16 +282,19 @@ struct Tables {
   int8_t tok[MAX_U][MAX_T];  // union expert, slot -> token
   int8_t pu[MAX_T][MAX_K];   // (t, r) -> union index
   int8_t ps[MAX_T][MAX_K];   // (t, r) -> slot
+  float w[MAX_T][MAX_K];     // routing weights
   int U;
   int bad;
 };
 
-__device__ void build_tables(Tables& tb, const int32_t* idx, int T, int k, int E) {
+__device__ void build_tables(Tables& tb, const int32_t (*idx)[MAX_K], const float (*w)[MAX_K], int T, int k, int E) {
   tb.U = 0;
   tb.bad = 0;
   for (int t = 0; t < T; ++t)
+    for (int r = 0; r < k; ++r) tb.w[t][r] = w[t][r];
+  for (int t = 0; t < T; ++t)
     for (int r = 0; r < k; ++r) {
-      const int e = idx[t * k + r];
+      const int e = idx[t][r];
       if (e < 0 || e >= E) { tb.bad = 1; tb.pu[t][r] = 0; tb.ps[t][r] = 0; continue; }
       int u = 0;
       while (u < tb.U && tb.ue[u] != e) ++u;
@@ -411,7 +420,7 @@ __device__ void combine_rows(const Args& a, const Geo& g, const Tables& tb, int 
         for (int q = 0; q < 4; ++q)
           if (k0 + q < g.SD) sum += pl[q];
       }
-      acc = fmaf(a.w[t * g.k + r], sum, acc);
+      acc = fmaf(tb.w[t][r], sum, acc);
     }
     float* yp = a.y + (int64_t)t * g.H + j;
     const float out = a.accumulate ? *yp + acc : acc;
@@ -465,7 +474,7 @@ __device__ void epilogue(const Args& a, const Geo& g, const Tables& tb, const Or
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&acc_empty[j][ab]);
+    if (lane == 0) mbar_arrive_relaxed(&acc_empty[j][ab]);  // TMEM read; no wait for the earlier global stores
     if (!un.d) {
       float* gp = gpart + (((int64_t)un.u * g.RTG + un.rt) * g.SG + un.ks) * a.ts * 128 + m;
 #pragma unroll
@@ -505,7 +514,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ __align__(8) uint64_t full[NSLOT], empty[NSLOT], acc_full[NPIPE][2], acc_empty[NPIPE][2], drain[NPIPE];
-  __shared__ __align__(8) uint64_t uq_full[NPIPE][QN], xres_full;
+  __shared__ __align__(8) uint64_t uq_full[NPIPE][QN], xres_full, tab_full;
   uint8_t* xres = smem + NSLOT * SLOT_BYTES;    // resident x parts of this CTA's gate/up K segment
   uint8_t* xres_sf = xres + 8 * XRES_TILE;
   __shared__ volatile int uq[NPIPE][QN];
@@ -513,7 +522,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
   __shared__ Tables tb;
   __shared__ Order ord;
   __shared__ uint32_t s_tmem;
-  __shared__ int s_units, s_has_g;
+  __shared__ int s_units;
   __shared__ volatile int s_abort, s_ok[NGRP], s_last[NGRP], s_unit[NGRP];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -524,6 +533,21 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
   float xfirst[4] = {0.f, 0.f, 0.f, 0.f};
   if (warp >= EPI_WARP0) load_x4(a, g, (int)blockIdx.x % g.SG, warp - EPI_WARP0, warp - EPI_WARP0, xfirst);
 
+  float* lgw = reinterpret_cast<float*>(a.ws + a.L.lg);  // router logits [token][expert]
+  if (a.wr && warp >= 2 && warp < 2 + 2 * NPIPE) {
+    // routing, phase 1 (at entry, while thread 0 and warp 1 set the CTA up): the logits of experts
+    // blockIdx.x + gridDim.x * (w + 2 NPIPE i), w = warp - 2, spread over the grid
+    for (int e = (int)blockIdx.x + (int)gridDim.x * (warp - 2); e < a.E; e += (int)gridDim.x * 2 * NPIPE) {
+      float acc[kRouteTPC];
+      route_row_logits<8>(a.wr + (size_t)e * g.H, g.H, g.T, [&](int t) { return a.x + (size_t)t * g.H; }, acc);
+      if (lane == 0)
+        for (int t = 0; t < g.T; ++t) __stcg(lgw + t * a.E + e, acc[t]);
+      __syncwarp();
+      if (lane == 0) red_release_add(cnt + C_ROUTE, 1u);
+    }
+  }
+  __shared__ int32_t s_idx[MAX_T][MAX_K];
+  __shared__ float s_wt[MAX_T][MAX_K];
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSLOT; ++s) { mbar_init(&full[s], 2); mbar_init(&empty[s], 1); }  // full: both producers arrive
     for (int j = 0; j < NPIPE; ++j) {
@@ -533,19 +557,61 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
       for (int e = 0; e < QN; ++e) mbar_init(&uq_full[j][e], 1);
     }
     mbar_init(&xres_full, 1);
+    mbar_init(&tab_full, 1);
     s_abort = 0;
     s_next = 0;
     fence_mbar_init();
-    build_tables(tb, a.idx, g.T, g.k, a.E);
-    if (tb.bad) { s_abort = 1; if (blockIdx.x == 0) record_error(&hdr->status, MOE_ERR_INVALID_ARG); }
-    s_units = tb.bad ? 0 : tb.U * (g.RTG * g.SG + g.RTD * g.SD);
-    build_order(ord, g, tb.bad ? 0 : tb.U);
   }
   if (warp == 1) tc_alloc(&s_tmem, TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = s_tmem;
+  if (warp >= EPI_WARP0) {
+    // the resident x parts of the CTA's gate/up segment (needed by its gate/up units; independent of the routing),
+    // while the other warps route and build the tables; then wait for the tables
+    split_x_res(a, g, (int)blockIdx.x % g.SG, warp - EPI_WARP0, xres, xres_sf, xfirst);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> MMA (async proxy) reads
+    named_bar(1 + NGRP, 4 * NGRP * 32);
+    if (warp == EPI_WARP0 && lane == 0) mbar_arrive(&xres_full);
+    if (!bwait(&tab_full, 0, &s_abort, lim) && threadIdx.x == EPI_WARP0 * 32) record_error(&hdr->status, MOE_ERR_DEVICE_TIMEOUT);
+  } else {
+    if (a.wr) {
+      // routing, phase 2: every CTA selects each token's experts from all the logits (one warp per token)
+      if (warp < g.T) {
+        bool ok = true;
+        if (lane == 0) ok = wait_ge(cnt + C_ROUTE, (uint32_t)a.E, &s_abort, lim);
+        ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+        int sid[8];
+        float sw[8];
+        if (ok) {
+          const float* row = lgw + warp * a.E;
+          route_topk_warp<kRouteMaxE / 32 / 4>([&](int e) { return __ldcg(row + e); }, a.E, g.k, sid, sw);
+        }
+        if (lane == 0)
+          for (int r = 0; r < g.k; ++r) {
+            s_idx[warp][r] = ok ? sid[r] : -1;
+            s_wt[warp][r] = ok ? sw[r] : 0.f;
+            if (blockIdx.x == 0 && ok) {
+              a.idx_out[warp * g.k + r] = sid[r];
+              a.w_out[warp * g.k + r] = sw[r];
+            }
+          }
+      }
+    } else if (threadIdx.x < g.T * g.k) {
+      s_idx[threadIdx.x / g.k][threadIdx.x % g.k] = a.idx[threadIdx.x];
+      s_wt[threadIdx.x / g.k][threadIdx.x % g.k] = a.w[threadIdx.x];
+    }
+    named_bar(2 + NGRP, EPI_WARP0 * 32);
+    if (threadIdx.x == 0) {
+      build_tables(tb, s_idx, s_wt, g.T, g.k, a.E);
+      if (tb.bad) { s_abort = 1; if (blockIdx.x == 0) record_error(&hdr->status, MOE_ERR_INVALID_ARG); }
+      s_units = tb.bad ? 0 : tb.U * (g.RTG * g.SG + g.RTD * g.SD);
+      build_order(ord, g, tb.bad ? 0 : tb.U);
+      mbar_arrive(&tab_full);
+    }
+    named_bar(2 + NGRP, EPI_WARP0 * 32);
+  }
   g.U = tb.U;
   g.nG = g.U * g.RTG * g.SG;
   g.nD = g.U * g.RTD * g.SD;
@@ -555,13 +621,6 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
   // next i from a shared counter when they start a unit, so a pipeline waiting for h does not hold up the rest;
   // each publishes the ids it took through its queue uq[j] to its MMA thread and epilogue group.
   const int my_units = nunits > (int)blockIdx.x ? (nunits - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-  if (threadIdx.x == 0) {  // does any of this CTA's units need the resident x parts?
-    int hg = 0;
-    for (int i = 0; i < my_units && !hg; ++i) hg = unit_of((int)blockIdx.x + i * (int)gridDim.x, g, ord).d == 0;
-    s_has_g = hg;
-  }
-  __syncthreads();
-  const bool has_g = s_has_g != 0;
 
   if (warp < 2 * NPIPE) {
     // ---------------- producers, two warps per pipeline j (lane 0 issues): warp j streams the weight tiles of
@@ -678,13 +737,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
     }
     __syncwarp();
   } else {
-    // ---------------- epilogue warps: first the resident x parts of the CTA's gate/up segment
-    if (has_g) {
-      split_x_res(a, g, (int)blockIdx.x % g.SG, warp - EPI_WARP0, xres, xres_sf, xfirst);
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> MMA (async proxy) reads
-      named_bar(1 + NGRP, 4 * NGRP * 32);
-      if (warp == EPI_WARP0 && lane == 0) mbar_arrive(&xres_full);
-    }
+    // ---------------- epilogue warps (the resident x parts are done)
     epilogue(a, g, tb, ord, tbase, acc_full, acc_empty, uq_full, uq, cnt, s_last, s_ok, s_unit, &s_abort);
   }
   tc_fence_before();
@@ -700,6 +753,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
       for (int q = 0; q < tb.U * 16; ++q) cnt[C_HREADY + q] = 0;
       for (int q = 0; q < tb.U * g.RTG; ++q) cnt[C_G + q] = 0;
       for (int q = 0; q < g.RTD; ++q) cnt[C_D + q] = 0;
+      cnt[C_ROUTE] = 0;
       __threadfence();
       cnt[C_DONE] = 0;
     }
@@ -715,7 +769,8 @@ size_t workspace_bytes(const moe_layer_t* L, int T_max, int k) {
 
 // The caller (ffn.cu) has checked pointers, T in [1, 8], k in [1, 8], the shape and the device.
 moe_status_t run(const moe_layer_t* L, const void* x, int T, const int32_t* idx, const float* w, int k, float* y,
-                 void* y_bf16, int accumulate, void* ws, size_t ws_bytes, void* stream) {
+                 void* y_bf16, int accumulate, void* ws, size_t ws_bytes, void* stream, const void* router_w,
+                 int32_t* idx_out, float* w_out) {
   if (L->fmt != MOE_FMT_MXFP4) return MOE_ERR_UNSUPPORTED_FORMAT;
   if (((uintptr_t)x & 1) || ((uintptr_t)y & 3)) return MOE_ERR_INVALID_ARG;
   // the workspace is laid out for the T_max it was sized for; recover it from the size (largest T_max that fits)
@@ -732,6 +787,11 @@ moe_status_t run(const moe_layer_t* L, const void* x, int T, const int32_t* idx,
   a.x = (const uint16_t*)x;
   a.idx = idx;
   a.w = w;
+  a.wr = (const uint16_t*)router_w;
+  a.idx_out = idx_out;
+  a.w_out = w_out;
+  if (router_w && (L->E > kRouteMaxE / 4 || k > L->E || ((uintptr_t)x & 15) || ((uintptr_t)router_w & 15)))
+    return router_w && L->E > kRouteMaxE / 4 ? MOE_ERR_SHAPE : MOE_ERR_INVALID_ARG;
   a.y = y;
   a.yb = (__nv_bfloat16*)y_bf16;
   a.accumulate = accumulate;
@@ -782,7 +842,8 @@ size_t tc_decode_workspace_bytes(const moe_layer_t* L, int T_max, int k) {
   return moe::dtc::workspace_bytes(L, T_max, k);
 }
 moe_status_t tc_decode(const moe_layer_t* L, const void* x, int T, const int32_t* idx, const float* w, int k, float* y,
-                       void* y_bf16, int accumulate, void* ws, size_t ws_bytes, void* stream) {
-  return moe::dtc::run(L, x, T, idx, w, k, y, y_bf16, accumulate, ws, ws_bytes, stream);
+                       void* y_bf16, int accumulate, void* ws, size_t ws_bytes, void* stream, const void* router_w,
+                       int32_t* idx_out, float* w_out) {
+  return moe::dtc::run(L, x, T, idx, w, k, y, y_bf16, accumulate, ws, ws_bytes, stream, router_w, idx_out, w_out);
 }
 }  // namespace moe_internal

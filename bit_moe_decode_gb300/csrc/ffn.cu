@@ -704,6 +704,28 @@ extern "C" moe_status_t moe_expert_ffn_decode(const moe_layer_t* L, const void* 
   return ffn_common("decode", L, x_bf16, 1, idx, w, k, y, y_bf16, accumulate, ws, ws_bytes, stream);
 }
 
+// Router and expert FFN in one launch (tensor-core layout, MXFP4): the decode kernel computes the router logits
+// across the grid first, every CTA selects the experts, CTA 0 writes idx / w, then the FFN proceeds as in
+// moe_expert_ffn_verify. The routing equals moe_route_topk's bit for bit (same arithmetic, route.cuh).
+extern "C" moe_status_t moe_route_expert_ffn(const moe_layer_t* L, const void* router_w_f16, const void* x_bf16, int32_t T,
+                                            int32_t k, int32_t* idx, float* w, float* y, void* y_bf16,
+                                            int32_t accumulate, void* ws, size_t ws_bytes, void* stream) {
+  if (moe_internal::fault("route_ffn")) return MOE_ERR_FAULT_INJECTED;
+  if (!L || !router_w_f16 || !x_bf16 || !idx || !w || !y || !ws) return MOE_ERR_INVALID_ARG;
+  if (L->layout != MOE_LAYOUT_TC || L->fmt != MOE_FMT_MXFP4) return MOE_ERR_UNSUPPORTED_FORMAT;
+  if (!L->gate_up || !L->down || ((uintptr_t)L->gate_up & 15) || ((uintptr_t)L->down & 15)) return MOE_ERR_INVALID_ARG;
+  if (((uintptr_t)x_bf16 & 15) || ((uintptr_t)router_w_f16 & 15) || ((uintptr_t)ws & 255) || ((uintptr_t)y & 3) ||
+      ((uintptr_t)idx & 3) || ((uintptr_t)w & 3))
+    return MOE_ERR_INVALID_ARG;
+  if (y_bf16 && ((uintptr_t)y_bf16 & 1)) return MOE_ERR_INVALID_ARG;
+  if (T < 1 || T > kMaxT || k < 1 || k > kMaxK || L->E < k || L->E > 256) return MOE_ERR_SHAPE;
+  if (!moe_internal::shape_ok(L->H, L->I)) return MOE_ERR_SHAPE;
+  moe_status_t st = moe_check_device();
+  if (st != MOE_OK) return st;
+  return moe_internal::tc_decode(L, x_bf16, T, nullptr, nullptr, k, y, y_bf16, accumulate, ws, ws_bytes, stream,
+                                 router_w_f16, idx, w);
+}
+
 extern "C" moe_status_t moe_expert_ffn_verify(const moe_layer_t* L, const void* x_bf16, int32_t T, const int32_t* idx,
                                               const float* w, int32_t k, float* y, void* y_bf16, int32_t accumulate,
                                               void* ws, size_t ws_bytes, void* stream) {

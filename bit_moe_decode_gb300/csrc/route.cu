@@ -2,7 +2,7 @@
 // router, top-6 of 256 routed experts) and hash routing ("quant surgery" (blog.meowhead.cn), section 4: the first
 // layers map a token id to fixed experts through a tid2eid table).
 //
-// Softmax mode: one thread-block cluster of 16 CTAs handles up to 8 tokens. Each of its 256 warps computes the
+// Softmax mode (arithmetic in route.cuh): one thread-block cluster of 16 CTAs handles up to 8 tokens. Each of its 256 warps computes the
 // logits of its experts (fp16 x bf16 products are exact in fp32; each lane sums its strided slice in order, then a
 // fixed butterfly reduces the lanes), keeps them in its CTA's shared memory, and CTA 0 gathers all logits through
 // distributed shared memory and selects the top k per token (one warp per token): k rounds of a warp arg-max with
@@ -12,6 +12,7 @@
 #include <cooperative_groups.h>
 
 #include "common.cuh"
+#include "route.cuh"
 #include "api_internal.h"
 
 namespace cg = cooperative_groups;
@@ -20,8 +21,6 @@ namespace moe {
 
 constexpr int kRouteCluster = 16;
 constexpr int kRouteWarps = 16;
-constexpr int kRouteTPC = 8;                // tokens per cluster
-constexpr int kRouteMaxE = 1024;
 constexpr int kRouteSlots = kRouteMaxE / (kRouteCluster * kRouteWarps);  // experts per warp (max 4)
 
 __global__ void __launch_bounds__(kRouteWarps * 32, 1)
@@ -51,101 +50,31 @@ route_kernel(const uint16_t* __restrict__ wr, const uint16_t* __restrict__ x, in
     const int e = gw + sl * kRouteCluster * kRouteWarps;
     if (e >= E) break;
     float acc[kRouteTPC];
+    route_row_logits<16>(wr + (size_t)e * H, H, nt, [&](int t) { return xs + (size_t)t * H; }, acc);
+    if (lane == 0)
 #pragma unroll
-    for (int t = 0; t < kRouteTPC; ++t) acc[t] = 0.f;
-    const uint16_t* row = wr + (size_t)e * H;
-    // the row's 16-byte pieces for this lane, fetched in batches of 8 so the loads are in flight together
-    for (int h0 = lane * 8; h0 < H; h0 += 256 * 8) {
-      uint4 wv[8];
-#pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        const int h = h0 + 256 * b;
-        wv[b] = h < H ? __ldg(reinterpret_cast<const uint4*>(row + h)) : make_uint4(0u, 0u, 0u, 0u);
-      }
-#pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        const int h = h0 + 256 * b;
-        if (h >= H) break;
-        const uint32_t ww[4] = {wv[b].x, wv[b].y, wv[b].z, wv[b].w};
-        float wf[8];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          wf[2 * j] = __half2float(__ushort_as_half((unsigned short)(ww[j] & 0xFFFFu)));
-          wf[2 * j + 1] = __half2float(__ushort_as_half((unsigned short)(ww[j] >> 16)));
-        }
-#pragma unroll
-        for (int t = 0; t < kRouteTPC; ++t) {
-          if (t < nt) {
-            const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)t * H + h);
-            const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              acc[t] = fmaf(wf[2 * j], __uint_as_float(xx[j] << 16), acc[t]);
-              acc[t] = fmaf(wf[2 * j + 1], __uint_as_float(xx[j] & 0xFFFF0000u), acc[t]);
-            }
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int t = 0; t < kRouteTPC; ++t) {
-      float v = acc[t];
-      v += __shfl_xor_sync(0xffffffffu, v, 16);
-      v += __shfl_xor_sync(0xffffffffu, v, 8);
-      v += __shfl_xor_sync(0xffffffffu, v, 4);
-      v += __shfl_xor_sync(0xffffffffu, v, 2);
-      v += __shfl_xor_sync(0xffffffffu, v, 1);
-      if (lane == 0) lg[sl * kRouteWarps + warp][t] = v;
-    }
+      for (int t = 0; t < kRouteTPC; ++t) lg[sl * kRouteWarps + warp][t] = acc[t];
   }
   cluster.sync();
 
   if (cr == 0 && warp < nt) {
     const int t = warp;
     // gather: expert e lives in CTA (e % 256) / 16, warp e % 16, slot e / 256
-    float v[kRouteMaxE / 32];
-#pragma unroll
-    for (int j = 0; j < kRouteMaxE / 32; ++j) {
-      const int e = lane + 32 * j;
-      v[j] = -__int_as_float(0x7f800000);
-      if (e < E) {
-        const int owner = (e % (kRouteCluster * kRouteWarps)) / kRouteWarps;
-        const int slot = (e / (kRouteCluster * kRouteWarps)) * kRouteWarps + e % kRouteWarps;
-        float* remote = cluster.map_shared_rank(&lg[0][0], owner);
-        v[j] = remote[slot * kRouteTPC + t];
-      }
-    }
-    float sel[8];
     int sid[8];
-    for (int r = 0; r < k; ++r) {
-      float best = -__int_as_float(0x7f800000);
-      int bi = 0x7fffffff;
-#pragma unroll
-      for (int j = 0; j < kRouteMaxE / 32; ++j) {
-        const int e = lane + 32 * j;
-        if (e < E && (v[j] > best || (v[j] == best && e < bi))) { best = v[j]; bi = e; }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ob = __shfl_xor_sync(0xffffffffu, best, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
-      }
-      sel[r] = best;
-      sid[r] = bi;
-      // remove the winner
-#pragma unroll
-      for (int j = 0; j < kRouteMaxE / 32; ++j)
-        if (lane + 32 * j == bi) v[j] = -__int_as_float(0x7f800000);
-    }
-    if (lane == 0) {
-      float den = 0.f;
-      for (int r = 0; r < k; ++r) den += expf(sel[r] - sel[0]);
+    float sw[8];
+    route_topk_warp<kRouteMaxE / 32>(
+        [&](int e) {
+          const int owner = (e % (kRouteCluster * kRouteWarps)) / kRouteWarps;
+          const int slot = (e / (kRouteCluster * kRouteWarps)) * kRouteWarps + e % kRouteWarps;
+          const float* remote = cluster.map_shared_rank(&lg[0][0], owner);
+          return remote[slot * kRouteTPC + t];
+        },
+        E, k, sid, sw);
+    if (lane == 0)
       for (int r = 0; r < k; ++r) {
         idx_out[(size_t)(t0 + t) * k + r] = sid[r];
-        w_out[(size_t)(t0 + t) * k + r] = expf(sel[r] - sel[0]) / den;
+        w_out[(size_t)(t0 + t) * k + r] = sw[r];
       }
-    }
   }
   cluster.sync();  // keep every CTA's logits alive until CTA 0 has read them
 }

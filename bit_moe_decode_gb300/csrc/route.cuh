@@ -1,0 +1,108 @@
+// route.cuh -- the router arithmetic shared by the standalone router (route.cu) and the decode kernel that routes
+// in its first phase (decode_tc.cu), so that both give the same bits ("Mixed-precision compression of
+// DeepSeek-V4-Flash" (lumirain.cn), "The recipe": F16 router, top-6 of 256 routed experts, softmax weights).
+//
+// Logit of expert e for token t: sum over h of W_r[e, h] * x[t, h] (fp16 x bf16 products are exact in fp32). Lane
+// l of a warp sums, in order, the 8-element pieces at h = 8 l + 256 i (i = 0, 1, ...) with fused multiply-adds;
+// then a fixed butterfly (xor 16, 8, 4, 2, 1) adds the lanes. Top-k: k rounds of a warp arg-max with ties to the
+// lower expert index; weights exp(l_r - l_0) / sum_j exp(l_j - l_0) in rank order.
+#pragma once
+#include <cstdint>
+#include <cuda_fp16.h>
+
+namespace moe {
+
+constexpr int kRouteTPC = 8;    // tokens per pass
+constexpr int kRouteMaxE = 1024;
+
+// Logits of one expert row for tokens 0 .. nt-1; xrow(t) points at token t's x (shared or global memory). BATCH
+// pieces per lane are loaded before they are used; it changes when the loads are issued, not the sums.
+template <int BATCH, typename XRow>
+__device__ __forceinline__ void route_row_logits(const uint16_t* __restrict__ row, int H, int nt, XRow xrow,
+                                                 float (&acc)[kRouteTPC]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int t = 0; t < kRouteTPC; ++t) acc[t] = 0.f;
+  // the row's 16-byte pieces for this lane, fetched in batches so the loads are in flight together
+  for (int h0 = lane * 8; h0 < H; h0 += 256 * BATCH) {
+    uint4 wv[BATCH];
+#pragma unroll
+    for (int b = 0; b < BATCH; ++b) {
+      const int h = h0 + 256 * b;
+      wv[b] = h < H ? __ldg(reinterpret_cast<const uint4*>(row + h)) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int b = 0; b < BATCH; ++b) {
+      const int h = h0 + 256 * b;
+      if (h >= H) break;
+      const uint32_t ww[4] = {wv[b].x, wv[b].y, wv[b].z, wv[b].w};
+      float wf[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        wf[2 * j] = __half2float(__ushort_as_half((unsigned short)(ww[j] & 0xFFFFu)));
+        wf[2 * j + 1] = __half2float(__ushort_as_half((unsigned short)(ww[j] >> 16)));
+      }
+#pragma unroll
+      for (int t = 0; t < kRouteTPC; ++t) {
+        if (t < nt) {
+          const uint4 xv = *reinterpret_cast<const uint4*>(xrow(t) + h);
+          const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            acc[t] = fmaf(wf[2 * j], __uint_as_float(xx[j] << 16), acc[t]);
+            acc[t] = fmaf(wf[2 * j + 1], __uint_as_float(xx[j] & 0xFFFF0000u), acc[t]);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < kRouteTPC; ++t) {
+    float v = acc[t];
+    v += __shfl_xor_sync(0xffffffffu, v, 16);
+    v += __shfl_xor_sync(0xffffffffu, v, 8);
+    v += __shfl_xor_sync(0xffffffffu, v, 4);
+    v += __shfl_xor_sync(0xffffffffu, v, 2);
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    acc[t] = v;
+  }
+}
+
+// Top-k of one token by the whole warp; logit(e) gives expert e's logit (e < E <= 32 * NE). Lane 0 gets the experts
+// in rank order in sid[] and their weights in sw[].
+template <int NE, typename Logit>
+__device__ __forceinline__ void route_topk_warp(Logit logit, int E, int k, int (&sid)[8], float (&sw)[8]) {
+  const int lane = threadIdx.x & 31;
+  float v[NE];
+#pragma unroll
+  for (int j = 0; j < NE; ++j) {
+    const int e = lane + 32 * j;
+    v[j] = e < E ? logit(e) : -__int_as_float(0x7f800000);
+  }
+  float sel[8];
+  for (int r = 0; r < k; ++r) {
+    float best = -__int_as_float(0x7f800000);
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < NE; ++j) {
+      const int e = lane + 32 * j;
+      if (e < E && (v[j] > best || (v[j] == best && e < bi))) { best = v[j]; bi = e; }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ob = __shfl_xor_sync(0xffffffffu, best, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
+    }
+    sel[r] = best;
+    sid[r] = bi;
+#pragma unroll
+    for (int j = 0; j < NE; ++j)  // remove the winner
+      if (lane + 32 * j == bi) v[j] = -__int_as_float(0x7f800000);
+  }
+  float den = 0.f;
+  for (int r = 0; r < k; ++r) den += expf(sel[r] - sel[0]);
+  for (int r = 0; r < k; ++r) sw[r] = expf(sel[r] - sel[0]) / den;
+}
+
+}  // namespace moe

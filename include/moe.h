@@ -164,6 +164,18 @@ moe_status_t moe_expert_ffn_verify(const moe_layer_t* layer, const void* x_bf16,
                                    const float* w, int32_t k, float* y, void* y_bf16, int32_t accumulate, void* ws,
                                    size_t ws_bytes, void* stream);
 
+/* Router and expert FFN of T tokens (1 <= T <= 8) in one launch, for a MOE_LAYOUT_TC MXFP4 layer with E <= 256
+ * ("Mixed-precision compression of DeepSeek-V4-Flash", "The recipe": F16 router, softmax top-6 of 256 routed
+ * experts; the fused always-on neighbours of the expert FFN). The kernel first computes the router logits across
+ * the whole grid (workspace scratch), every CTA then selects each token's top-k, and the FFN follows.
+ *   router_w_f16 [E, H] fp16 and x_bf16 [T, H] (both 16-byte aligned); idx [T, k] int32 and w [T, k] fp32 are
+ *   OUTPUTS, bit-identical to moe_route_topk's for the same router and x; y [T, H] (and y_bf16) are bit-identical
+ *   to moe_expert_ffn_verify's with that idx / w. Workspace as for moe_expert_ffn_verify.
+ *   Errors: MOE_ERR_UNSUPPORTED_FORMAT (other layout or format), MOE_ERR_SHAPE (T, k, E out of range). */
+moe_status_t moe_route_expert_ffn(const moe_layer_t* layer, const void* router_w_f16, const void* x_bf16, int32_t T,
+                                  int32_t k, int32_t* idx, float* w, float* y, void* y_bf16, int32_t accumulate,
+                                  void* ws, size_t ws_bytes, void* stream);
+
 /* Decode of one token exactly like moe_expert_ffn_decode, but without a workspace argument: its scratch is a
  * fixed array of 2,101,248 bytes inside the library (one per GPU that loads it, kept until the process exits).
  * The pages have no counterpart; it exists for callers that cannot allocate device memory (a plugin given only

@@ -9,8 +9,8 @@ import pytest
 import torch
 
 import oracle
-from moe_inputs import x_bf16_bits
-from tests._harness import Weights, make_layer, oracle_moe, tol_check
+from moe_inputs import router_f16_bits, x_bf16_bits
+from tests._harness import Weights, dev_bits, make_layer, oracle_moe, tol_check
 from tests.test_gpu_ffn import _decode, _routing, _verify
 
 pytestmark = pytest.mark.gpu
@@ -161,3 +161,55 @@ def test_tc_special_exponents(m):
                                    np.array([[1.0]], np.float32), x)
         tol_check(y, yr[0], ab[0], "expert %d" % e)
     assert np.all(np.isnan(y))
+
+
+# ---------------------------------------------------------------- router and FFN in one launch
+def _route_ffn(m, layer, ws, wr, x, k):
+    T, H = x.shape
+    idx = torch.full((T, k), -1, dtype=torch.int32, device=DEV)
+    w = torch.zeros((T, k), dtype=torch.float32, device=DEV)
+    y = torch.full((T, H), float("nan"), device=DEV)
+    m.moe_route_expert_ffn(layer, dev_bits(wr, DEV), dev_bits(x, DEV), T, k, idx, w, y, None, False, ws)
+    torch.cuda.synchronize()
+    assert m.moe_get_device_status(ws) == 0
+    return idx.cpu().numpy(), w.cpu().numpy(), y.cpu().numpy()
+
+
+def _route_sep(m, wr, x, k):
+    T, H = x.shape
+    idx = torch.full((T, k), -1, dtype=torch.int32, device=DEV)
+    w = torch.zeros((T, k), dtype=torch.float32, device=DEV)
+    m.moe_route_topk(dev_bits(wr, DEV), dev_bits(x, DEV), T, H, wr.shape[0], k, None, None, 0, idx, w)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), w.cpu().numpy()
+
+
+@pytest.mark.parametrize("T", [1, 3, 8])
+def test_tc_route_ffn_equals_route_then_verify_full_shape(m, big, T):
+    """the fused call routes exactly as moe_route_topk and computes exactly what verify computes with that routing"""
+    E, H, k, x, layer = (big[n] for n in ("E", "H", "k", "x", "layer"))
+    wr = router_f16_bits(1000, 0, E, H)  # the router the fixture's routing came from
+    ws = layer.workspace(8, k)
+    fi, fw, fy = _route_ffn(m, layer, ws, wr, x[:T], k)
+    si, sw = _route_sep(m, wr, x[:T], k)
+    assert np.array_equal(fi, si) and np.array_equal(fw.view(np.uint32), sw.view(np.uint32))
+    assert np.array_equal(fi, big["idx"][:T])
+    yv = _verify(m, layer, ws, x[:T], si, sw, k)
+    assert np.array_equal(fy.view(np.uint32), yv.view(np.uint32))
+
+
+def test_tc_route_ffn_small_layer(m, small):
+    W, layer = small
+    E, H, k, T = 8, 512, 2, 5
+    wr = router_f16_bits(7, 0, E, H)
+    x = x_bf16_bits(7, range(T), H)
+    ws = layer.workspace(8, k)
+    fi, fw, fy = _route_ffn(m, layer, ws, wr, x, k)
+    si, sw = _route_sep(m, wr, x, k)
+    assert np.array_equal(fi, si) and np.array_equal(fw.view(np.uint32), sw.view(np.uint32))
+    yr, ab = oracle_moe(MXFP4, W, si, sw, x)
+    for t in range(T):
+        tol_check(fy[t], yr[t], ab[t], "fused row %d" % t)
+    # repeated calls reuse the workspace (its router counter is reset by the last CTA)
+    fi2, fw2, fy2 = _route_ffn(m, layer, ws, wr, x, k)
+    assert np.array_equal(fy2.view(np.uint32), fy.view(np.uint32))
