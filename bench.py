@@ -37,6 +37,7 @@ def parse():
     p.add_argument("--tokens", type=int, default=NTOK)
     p.add_argument("--seed", type=int, default=1)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-verify", action="store_true", help="skip the verify-cost measurements")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--experts", type=int, default=E, help="expert slots of the layer (smaller only for profiling)")
     p.add_argument("--layout", default="auto", choices=["auto", "tc", "decode"],
@@ -303,6 +304,7 @@ def run_ours(args):
         e2e_ms = float(tt.item())
 
     prefill = bench_prefill(m, torch, args, dev, stream, layer_p, E) if do_prefill else None
+    verify = bench_verify(m, torch, args, dev, stream, layer, wr, x_host, E, per_expert) if (use_tc and not args.no_verify) else None
 
     out = None
     if rank == 0:
@@ -344,11 +346,72 @@ def run_ours(args):
                     "h2d_bytes_per_step": int(T * H * 2), "d2h_bytes_per_step": int(T * H * 4)},
             "clocks": clk,
             "prefill": prefill,
+            "verify": verify,
             "setup_s": round(setup_s, 1),
             "cuda_graph": use_graph,
         }
     if dist:
         dist.destroy_process_group()
+    return out
+
+
+def bench_verify(m, torch, args, dev, stream, layer, wr, x_host, E, per_expert):
+    """Verify cost (speculative verify of T = 1, 2, 4, 8 tokens in one sweep) on the same layer:
+    (i) shared routing: the T tokens all use the first token's experts, t(8) / t(1);
+    (ii) independent routing: t(T) / (t(1) * U_T / 6), U_T = union of the tokens' experts;
+    (iii) raw t(T) / t(1). Each t is the mean over 200 calls of a CUDA graph (the window of tokens advances)."""
+    n_calls = 200
+    xs = torch.from_numpy(x_host.view(np.int16)).to(dev)
+    nt = xs.shape[0]
+    ws = layer.workspace(8, K_TOP)
+    idx_all = torch.zeros((nt, K_TOP), dtype=torch.int32, device=dev)
+    w_all = torch.zeros((nt, K_TOP), dtype=torch.float32, device=dev)
+    m.moe_route_topk(wr, xs, nt, H, E, K_TOP, None, None, 0, idx_all, w_all, stream=stream)
+    stream.synchronize()
+    idx_np = idx_all.cpu().numpy()
+    out = {}
+    y = torch.zeros((8, H), dtype=torch.float32, device=dev)
+    for shared in (False, True):
+        res = {}
+        for T in (1, 2, 4, 8):
+            starts = [(i * T) % (nt - 8) for i in range(n_calls)]
+            if shared:   # every token of the window routed (and weighted) like the window's first token
+                sidx = torch.stack([idx_all[st].expand(T, -1) for st in starts]).contiguous()
+                sw = torch.stack([w_all[st].expand(T, -1) for st in starts]).contiguous()
+                args_of = [(xs[st:st + T], sidx[i], sw[i]) for i, st in enumerate(starts)]
+                u = float(np.mean([len(set(idx_np[st])) for st in starts]))
+            else:
+                args_of = [(xs[st:st + T], idx_all[st:st + T], w_all[st:st + T]) for st in starts]
+                u = float(np.mean([len(set(idx_np[st:st + T].ravel())) for st in starts]))
+
+            def launch():
+                for xa, ia, wa in args_of:
+                    m.moe_expert_ffn_verify(layer, xa, T, ia, wa, K_TOP, y, None, False, ws, stream=stream)
+            with torch.cuda.stream(stream):
+                launch()
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                launch()
+            with torch.cuda.stream(stream):
+                g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            with torch.cuda.stream(stream):
+                g.replay()
+                g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            res[T] = (e0.elapsed_time(e1) * 1e3 / (2 * n_calls), u)
+        t1, u1 = res[1]
+        key = "shared_routing" if shared else "independent_routing"
+        out[key] = {"us": {str(T): round(res[T][0], 3) for T in res},
+                    "union_experts": {str(T): round(res[T][1], 2) for T in res},
+                    "raw_ratio": {str(T): round(res[T][0] / t1, 3) for T in res},
+                    "per_union_byte_ratio": {str(T): round(res[T][0] / (t1 * res[T][1] / u1), 3) for T in res},
+                    "gbs": {str(T): round(res[T][1] * per_expert / (res[T][0] * 1e-6) / 1e9, 1) for T in res}}
+    if m.moe_get_device_status(ws, stream) != 0:
+        raise RuntimeError("device status after the verify measurements")
     return out
 
 

@@ -52,9 +52,10 @@ constexpr int HROWS = NB;                // B rows of each expert's h parts
 constexpr int EPI_WARP0 = 3 * NPIPE;     // warps: 2 NPIPE producers, NPIPE MMA issuers, then the epilogue groups
 // (each issuing thread has a warp of its own: issuing lanes that share a warp diverge and run one after another)
 constexpr int NGRP = NPIPE;              // epilogue groups of 4 warps; group j drains pipeline j
-constexpr int QN = 8;                    // unit-id queue entries per pipeline
+constexpr int QN = 16;                   // unit-id queue entries per pipeline
+constexpr int ABUF_MAX = 4;              // accumulators per pipeline
 constexpr int THREADS = (EPI_WARP0 + 4 * NGRP) * 32;
-constexpr uint32_t TMEM_COLS = 512;      // accumulators: pipeline j, buffer a at 128 j + 64 a; scales from 384
+constexpr uint32_t TMEM_COLS = 512;      // accumulators: pipeline j, buffer a at W (j ABUF + a); scales from 384
 constexpr uint32_t SF_COL0 = 384;
 static_assert(128 * NPIPE <= (int)SF_COL0 && SF_COL0 + 8 * NSLOT <= TMEM_COLS, "TMEM budget");
 // Every gate/up unit of CTA b covers the same K segment (b mod S_G: the grid is a multiple of S_G), so the CTA keeps
@@ -70,6 +71,8 @@ struct Geo {
   int RTG, KTG, KSG, SG;   // gate/up: row tiles, k-tiles, k-tiles per unit, segments
   int RTD, KTD, KSD, SD;   // down
   int nG, nD;              // units
+  int W, ABUF;             // accumulator width = MMA N (16 ceil(6 T / 16): a column per part and token, in 16s;
+                           // each column is computed on its own, whatever N is) and accumulators per pipeline
 };
 // k-tiles per unit: gate/up 8 (or 4, 2), down 4 (or 2) -- shorter down units shorten the tail after the last h
 __host__ __device__ inline int ks_for_g(int kt) { return kt % 8 == 0 ? 8 : (kt % 4 == 0 ? 4 : 2); }
@@ -429,8 +432,8 @@ __device__ void combine_rows(const Args& a, const Geo& g, const Tables& tb, int 
   }
 }
 
-__device__ void epilogue(const Args& a, const Geo& g, const Tables& tb, const Order& ord, uint32_t tbase, uint64_t (*acc_full)[2],
-                         uint64_t (*acc_empty)[2], uint64_t (*uq_full)[QN], volatile int (*uq)[QN], uint32_t* cnt,
+__device__ void epilogue(const Args& a, const Geo& g, const Tables& tb, const Order& ord, uint32_t tbase,
+                         uint64_t (*acc_full)[ABUF_MAX], uint64_t (*acc_empty)[ABUF_MAX], uint64_t (*uq_full)[QN], volatile int (*uq)[QN], uint32_t* cnt,
                          volatile int* s_last, volatile int* s_ok, volatile int* s_unit, volatile int* s_abort) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = warp & 3;
   const int grp = (warp - EPI_WARP0) / 4;
@@ -443,14 +446,14 @@ __device__ void epilogue(const Args& a, const Geo& g, const Tables& tb, const Or
   // the units pipeline j = grp took, in order (each accumulator's phases in order)
   const int j = grp;
   for (int c = 0;; ++c) {
-    const int ab = c & 1;
+    const int ab = c % g.ABUF;
     // one thread waits; the verdict is shared so that the group's four warps leave (or stay) together
     if (et == 0) {
       int st = 0;
       if (bwait(&uq_full[j][c % QN], (uint32_t)((c / QN) & 1), s_abort, lim)) {
         const int i = uq[j][c % QN];
         if (i < 0) st = 2;
-        else { s_unit[grp] = i; st = bwait(&acc_full[j][ab], (uint32_t)((c >> 1) & 1), s_abort, lim) ? 1 : 0; }
+        else { s_unit[grp] = i; st = bwait(&acc_full[j][ab], (uint32_t)((c / g.ABUF) & 1), s_abort, lim) ? 1 : 0; }
       }
       s_ok[grp] = st;
     }
@@ -459,13 +462,14 @@ __device__ void epilogue(const Args& a, const Geo& g, const Tables& tb, const Or
     tc_fence_after();
     const int i = s_unit[grp];
     const Unit un = unit_of((int)blockIdx.x + i * (int)gridDim.x, g, ord);
-    const uint32_t taddr = tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)(128 * j + 64 * ab);
+    const uint32_t taddr = tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)(g.W * (j * g.ABUF + ab));
     // column t * PARTS + p = part p of token (or slot) t; sum the parts of each column group in part order
     float acc[MAX_T];
 #pragma unroll
     for (int t = 0; t < MAX_T; ++t) acc[t] = 0.f;
 #pragma unroll
     for (int cb = 0; cb < NB / 16; ++cb) {
+      if (16 * cb >= g.W) break;
       uint32_t v[16];
       tc_ld16(taddr + 16 * cb, v);
       tc_wait_ld();
@@ -513,7 +517,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
                                                             const __grid_constant__ CUtensorMap tm_h, const Args a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  __shared__ __align__(8) uint64_t full[NSLOT], empty[NSLOT], acc_full[NPIPE][2], acc_empty[NPIPE][2], drain[NPIPE];
+  __shared__ __align__(8) uint64_t full[NSLOT], empty[NSLOT], acc_full[NPIPE][ABUF_MAX],
+      acc_empty[NPIPE][ABUF_MAX], drain[NPIPE];
   __shared__ __align__(8) uint64_t uq_full[NPIPE][QN], xres_full, tab_full;
   uint8_t* xres = smem + NSLOT * SLOT_BYTES;    // resident x parts of this CTA's gate/up K segment
   uint8_t* xres_sf = xres + 8 * XRES_TILE;
@@ -551,8 +556,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSLOT; ++s) { mbar_init(&full[s], 2); mbar_init(&empty[s], 1); }  // full: both producers arrive
     for (int j = 0; j < NPIPE; ++j) {
-      mbar_init(&acc_full[j][0], 1); mbar_init(&acc_full[j][1], 1);
-      mbar_init(&acc_empty[j][0], 4); mbar_init(&acc_empty[j][1], 4);  // the 4 warps of one epilogue group
+      for (int b = 0; b < ABUF_MAX; ++b) {
+        mbar_init(&acc_full[j][b], 1);
+        mbar_init(&acc_empty[j][b], 4);  // the 4 warps of one epilogue group
+      }
       mbar_init(&drain[j], 1);
       for (int e = 0; e < QN; ++e) mbar_init(&uq_full[j][e], 1);
     }
@@ -640,7 +647,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
           i = atomicAdd(&s_next, 1);
           // entry c % QN was last read for unit c - QN: the weight producer is at most RING stages ahead of the
           // MMA, so (units having at least 2 stages) the MMA has started unit c - 3 and the epilogue group has
-          // finished unit c - 5; the activation producer is ahead of the MMA
+          // finished unit c - 3 - ABUF >= c - 7 > c - QN; the activation producer is ahead of the MMA
           uq[j][c % QN] = i < my_units ? i : -1;
           mbar_arrive(&uq_full[j][c % QN]);
         } else {
@@ -703,10 +710,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
         const int i = uq[j][c % QN];
         if (i < 0) break;
         const Unit un = unit_of((int)blockIdx.x + i * (int)gridDim.x, g, ord);
-        const int ab = c & 1;
-        if (!bwait(&acc_empty[j][ab], ((c >> 1) & 1) ^ 1, &s_abort, lim)) { ok = false; break; }
+        const int ab = c % g.ABUF;
+        if (!bwait(&acc_empty[j][ab], ((c / g.ABUF) & 1) ^ 1, &s_abort, lim)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t d_tmem = tbase + (uint32_t)(128 * j + 64 * ab);
+        const uint32_t d_tmem = tbase + (uint32_t)(g.W * (j * g.ABUF + ab));
         const int ks = un.d ? g.KSD : g.KSG;
         if (!un.d && !xres_ok) {  // the resident x parts (built by the epilogue warps at start)
           if (!bwait(&xres_full, 0, &s_abort, lim)) { ok = false; break; }
@@ -726,7 +733,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
           const uint64_t ad = umma_desc_sw64(smem_u32(st)), bd = umma_desc_sw64(smem_u32(bsrc));
 #pragma unroll
           for (int kh = 0; kh < 2; ++kh)  // two K = 64 halves of the 128-column tile, scale bytes 2kh, 2kh + 1
-            tc_mma_mxf4(d_tmem, ad + 2 * kh, bd + 2 * kh, idesc_mxf4(128, NB, 2 * kh), sfa, sfbc, (kk | kh) != 0);
+            tc_mma_mxf4(d_tmem, ad + 2 * kh, bd + 2 * kh, idesc_mxf4(128, (uint32_t)g.W, 2 * kh), sfa, sfbc, (kk | kh) != 0);
           tc_commit(&empty[slot]);
         }
         if (ok) tc_commit(&acc_full[j][ab]);
@@ -806,6 +813,9 @@ moe_status_t run(const moe_layer_t* L, const void* x, int T, const int32_t* idx,
   g.RTG = 2 * L->I / 128; g.KTG = L->H / 128; g.KSG = ks_for_g(g.KTG); g.SG = g.KTG / g.KSG;
   g.RTD = L->H / 128;     g.KTD = L->I / 128; g.KSD = ks_for_d(g.KTD); g.SD = g.KTD / g.KSD;
   g.nG = g.nD = 0;
+  g.W = 16 * ((PARTS * T + 15) / 16);
+  g.ABUF = g.W <= 32 ? 4 : 2;
+  if (NPIPE * g.ABUF * g.W > (int)SF_COL0) return MOE_ERR_SHAPE;
   CUtensorMap mgu, mdn, mh;
   const uint64_t hd[2] = {(uint64_t)L->I / 2, (uint64_t)(umax * HROWS)}, hs[1] = {(uint64_t)L->I / 2};
   const uint32_t hbox[2] = {64, HROWS};
