@@ -409,22 +409,33 @@ __device__ void combine_rows(const Args& a, const Geo& g, const Tables& tb, int 
   const float* dp = reinterpret_cast<const float*>(a.ws + a.L.dpart);
   const int j = jt * 128 + et;
   for (int t = 0; t < g.T; ++t) {
-    float acc = 0.f;
-    for (int r = 0; r < g.k; ++r) {
-      const int u = tb.pu[t][r], s = tb.ps[t][r];
-      const float* p = dp + (((int64_t)u * g.RTD + jt) * g.SD * a.ts + s) * 128 + et;
-      float sum = 0.f;
-      for (int k0 = 0; k0 < g.SD; k0 += 4) {
-        float pl[4];
+    // the partials of every (rank, segment) of the token are loaded before the sums (segments in order per rank,
+    // then ranks in order), four segments at a time
+    float sum[MAX_K];
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (k0 + q < g.SD) pl[q] = __ldcg(p + (int64_t)(k0 + q) * a.ts * 128);
+    for (int r = 0; r < MAX_K; ++r) sum[r] = 0.f;
+    for (int k0 = 0; k0 < g.SD; k0 += 4) {
+      float pl[MAX_K][4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (k0 + q < g.SD) sum += pl[q];
+      for (int r = 0; r < MAX_K; ++r) {
+        if (r < g.k) {
+          const float* p = dp + (((int64_t)tb.pu[t][r] * g.RTD + jt) * g.SD * a.ts + tb.ps[t][r]) * 128 + et;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (k0 + q < g.SD) pl[r][q] = __ldcg(p + (int64_t)(k0 + q) * a.ts * 128);
+        }
       }
-      acc = fmaf(tb.w[t][r], sum, acc);
+#pragma unroll
+      for (int r = 0; r < MAX_K; ++r)
+        if (r < g.k)
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (k0 + q < g.SD) sum[r] += pl[r][q];
     }
+    float acc = 0.f;
+#pragma unroll
+    for (int r = 0; r < MAX_K; ++r)
+      if (r < g.k) acc = fmaf(tb.w[t][r], sum[r], acc);
     float* yp = a.y + (int64_t)t * g.H + j;
     const float out = a.accumulate ? *yp + acc : acc;
     *yp = out;
