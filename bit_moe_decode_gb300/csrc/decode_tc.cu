@@ -368,15 +368,16 @@ __device__ void split_x_res(const Args& a, const Geo& g, int ks0, int ew, uint8_
 
 // All G segments of (expert u, row tile rt) are in: g, u of the 64 intermediate indices rt*64 .. +63 (tile rows
 // 0..63 gate, 64..127 up), h = SiLU(g) * u, PARTS E2M1 parts per 32-block into the D operand rows PARTS * s + p.
-// Threads et < 64 (two whole warps, one 32-block each) do the work.
+// The group's 128 threads take the token slots two at a time.
 __device__ void finalize_h(const Args& a, const Geo& g, const Tables& tb, int u, int rt, int et) {
-  if (et >= 64) return;
+  // thread et: row et % 64 of the tile (a warp = one 32-block), token slots et / 64, et / 64 + 2, ...
+  const int row = et & 63, lane = threadIdx.x & 31;
   const float* gp = reinterpret_cast<const float*>(a.ws + a.L.gpart) + ((int64_t)u * g.RTG + rt) * g.SG * a.ts * 128;
-  const int i = rt * 64 + et, kt = i / 128, kb = (i % 128) / 32;
+  const int i = rt * 64 + row, kt = i / 128, kb = (i % 128) / 32;
   uint8_t* hb = a.ws + a.L.hb + (int64_t)u * HROWS * (g.I / 2);
   uint8_t* hsf = a.ws + a.L.hsf + ((int64_t)u * g.KTD + kt) * 512;
   const int nt = tb.ntok[u];
-  for (int s = 0; s < nt; ++s) {
+  for (int s = et >> 6; s < nt; s += 2) {
     const int t = tb.tok[u][s];
     float gv = 0.f, uv = 0.f;
     for (int k0 = 0; k0 < g.SG; k0 += 4) {  // segments in order, loads issued four at a time
@@ -384,8 +385,8 @@ __device__ void finalize_h(const Args& a, const Geo& g, const Tables& tb, int u,
 #pragma unroll
       for (int q = 0; q < 4; ++q)
         if (k0 + q < g.SG) {
-          gl[q] = __ldcg(gp + ((int64_t)(k0 + q) * a.ts + t) * 128 + et);
-          ul[q] = __ldcg(gp + ((int64_t)(k0 + q) * a.ts + t) * 128 + 64 + et);
+          gl[q] = __ldcg(gp + ((int64_t)(k0 + q) * a.ts + t) * 128 + row);
+          ul[q] = __ldcg(gp + ((int64_t)(k0 + q) * a.ts + t) * 128 + 64 + row);
         }
 #pragma unroll
       for (int q = 0; q < 4; ++q)
@@ -397,8 +398,8 @@ __device__ void finalize_h(const Args& a, const Geo& g, const Tables& tb, int u,
     split_parts(h, c, ex);
 #pragma unroll
     for (int p = 0; p < PARTS; ++p) {
-      if (!(et & 1)) hb[(int64_t)(PARTS * s + p) * (g.I / 2) + i / 2] = (uint8_t)c[p];
-      if ((et & 31) == 0) hsf[sfb(PARTS * s + p, kb)] = (uint8_t)ex[p];
+      if (!(lane & 1)) hb[(int64_t)(PARTS * s + p) * (g.I / 2) + i / 2] = (uint8_t)c[p];
+      if (lane == 0) hsf[sfb(PARTS * s + p, kb)] = (uint8_t)ex[p];
     }
   }
 }
