@@ -12,9 +12,10 @@
 //      epilogue forms h = SiLU(g) * u in fp32 and quantises it to MXFP8 (per 32 along I) for the next GEMM.
 //   4. gemm<DOWN>: per (tile, 128 hidden indices) unit, D = H_tile * Down^T over K = I, fp32 rows per pair.
 //   5. combine: y[t] = sum_r w[t, r] * D[pair (t, r)] in rank order, fp32 and/or bf16 (round to nearest even).
-// The GEMM kernel is persistent (one CTA per SM) and warp-specialised: warp 0 issues TMA tensor copies into a
-// 6-stage shared-memory ring from 3 lanes, warp 1 issues tcgen05.cp (scale factors) and tcgen05.mma into one of two TMEM
-// accumulators, warps 2..5 drain the other accumulator with tcgen05.ld. Every wait is bounded (timeout ->
+// The GEMM kernel is persistent (one CTA per SM) and warp-specialised: warps 0..2 issue TMA tensor copies into a
+// 6-stage shared-memory ring (one issuing thread per warp: issuing lanes of one warp serialise), warp 3 issues
+// tcgen05.cp (scale factors) and tcgen05.mma into one of two TMEM accumulators, warps 4..7 drain the other
+// accumulator with tcgen05.ld. Every wait is bounded (timeout ->
 // device status MOE_ERR_DEVICE_TIMEOUT, the CTA drains its own copies and frees TMEM).
 #include <mutex>
 
@@ -36,8 +37,11 @@ constexpr int B_TX = BN * BK / 2;         // bytes the TMA engine reads for them
 constexpr int SF_BYTES = 512;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES + 2 * SF_BYTES;  // 33 KB, a multiple of 1024
 constexpr uint32_t STAGE_TX = A_BYTES + B_TX + 2 * SF_BYTES;
-constexpr int THREADS = 192;
-constexpr int PRODUCERS = 3;             // TMA-issuing lanes of warp 0
+constexpr int PRODUCERS = 3;             // TMA-issuing warps (lane 0 of warps 0 .. PRODUCERS - 1)
+constexpr int W_MMA = PRODUCERS;         // the MMA-issuing warp
+constexpr int W_EPI = 4;                 // epilogue warps 4 .. 7 (TMEM lanes 32 (warp % 4) ..)
+constexpr int THREADS = (W_EPI + 4) * 32;
+static_assert(W_MMA < W_EPI, "warp roles");
 constexpr uint32_t TMEM_COLS = 512;       // accumulators at columns 0 and 128, scale columns from 256
 constexpr uint32_t SF_COL0 = 256;
 constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
@@ -284,7 +288,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
     *s_abort = 0;
     fence_mbar_init();
   }
-  if (warp == 1) tc_alloc(s_tmem, TMEM_COLS);
+  if (warp == W_MMA) tc_alloc(s_tmem, TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -293,15 +297,15 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
   const int64_t n_units = (int64_t)(*a.n_tiles) * a.NB;
   const long long lim = a.wait_ns;
 
-  if (warp == 0) {
-    // ---------------- TMA producer. One issuing thread completes about one wait-and-issue round per 330 ns on
-    // GB300 however many bytes it moves, so PRODUCERS lanes take turns: lane l issues all four copies of stages
-    // l, l + PRODUCERS, ... of this CTA's sequence of (unit, k-group) stages.
-    if (lane < PRODUCERS) {
+  if (warp < PRODUCERS) {
+    // ---------------- TMA producers. One issuing thread completes about one wait-and-issue round per 330 ns on
+    // GB300 however many bytes it moves, so PRODUCERS warps take turns: warp w issues all four copies of stages
+    // w, w + PRODUCERS, ... of this CTA's sequence of (unit, k-group) stages.
+    if (lane == 0) {
       int issued_slot = -1;
       uint32_t issued_ph = 0;
       bool ok = true;
-      for (int64_t g = lane;; g += PRODUCERS) {
+      for (int64_t g = warp;; g += PRODUCERS) {
         const int64_t u = blockIdx.x + (g / KG) * gridDim.x;
         if (u >= n_units) break;
         const int kg = (int)(g % KG), s = (int)(g % STAGES);
@@ -326,7 +330,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == W_MMA) {
     // ---------------- MMA issuer
     if (lane == 0) {
       int stage = 0;
@@ -362,7 +366,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
     }
     __syncwarp();
   } else {
-    // ---------------- epilogue: warps 2..5 own TMEM lanes 32*(warp % 4) .. +31
+    // ---------------- epilogue: warps 4..7 own TMEM lanes 32*(warp % 4) .. +31
     const int q = warp & 3;
     const int r = q * 32 + lane;  // tile row = token slot inside the tile
     int j = 0;
@@ -437,7 +441,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tc_dealloc(tbase, TMEM_COLS);
+  if (warp == W_MMA) tc_dealloc(tbase, TMEM_COLS);
 }
 
 // ------------------------------------------------------------------ 5. weighted combine in rank order
