@@ -88,9 +88,10 @@ __host__ __device__ inline int ks_for_d(int kt) { return kt % 4 == 0 ? 4 : 2; }
 constexpr int64_t kCnt = 256;
 constexpr int C_DONE = 1, C_HREADY = 2, C_G = C_HREADY + MAX_U * 16, C_D = C_G + MAX_U * 64;
 constexpr int C_ROUTE = C_D + 32;      // experts whose logits are in (routing inside the kernel)
-constexpr int C_END = C_ROUTE + 1;
+constexpr int C_XP = C_ROUTE + 1;        // 32-blocks of x split into the x-part image
+constexpr int C_END = C_XP + 1;
 struct Ws {
-  int64_t hb, hsf, gpart, dpart, lg, total;
+  int64_t hb, hsf, gpart, dpart, lg, xp, total;
 };
 inline int64_t al1k(int64_t v) { return (v + 1023) & ~(int64_t)1023; }
 inline Ws ws_layout(int64_t H, int64_t I, int64_t Umax, int64_t TS) {
@@ -103,6 +104,7 @@ inline Ws ws_layout(int64_t H, int64_t I, int64_t Umax, int64_t TS) {
   w.gpart = o; o = al1k(o + Umax * RTG * SG * TS * 128 * 4);
   w.dpart = o; o = al1k(o + Umax * RTD * SD * TS * 128 * 4);
   w.lg = o;    o = al1k(o + (int64_t)kRouteTPC * kRouteMaxE * 4);  // router logits [token][expert]
+  w.xp = o;    o = al1k(o + (H / 128) * (XRES_TILE + 512));      // x parts: [k-tile][48 rows][64 B], then exponents
   w.total = o;
   return w;
 }
@@ -310,59 +312,46 @@ __device__ void build_tables(Tables& tb, const int32_t (*idx)[MAX_K], const floa
     }
 }
 
-// x of every token over the K segment ks0 (KSG k-tiles), split into PARTS E2M1 parts, written into the resident B
-// operand: k-tile kk at xres + kk * XRES_TILE, row PARTS * t + p, 64 bytes per row, 16-byte chunks swizzled as the
-// 64-byte TMA swizzle does (chunk c of row r at chunk c ^ ((r >> 1) & 3)); exponents into the permuted blocks at
-// xsf + kk * 512. Run by the 12 epilogue warps; warp ew takes the (token, 32-block) pairs ew, ew + 12, ...
-// The x values of the warp's first four pairs, loaded at kernel entry (before the weight stream saturates DRAM and
-// stretches load latency to microseconds).
-__device__ __forceinline__ void load_x4(const Args& a, const Geo& g, int ks0, int ew, int p0, float (&xs)[4]) {
+// The x parts, split once per call: 32-block j = (token t, k-tile kt, block kb) of x goes to warp j of the grid's
+// epilogue warps (warp ew of CTA b is number 12 b + ew), which splits it into PARTS E2M1 parts (split_parts_n) and
+// writes them into the x-part image in the workspace: k-tile kt at xp + kt * XRES_TILE, row PARTS * t + p, 64 bytes
+// a row, 16-byte chunks in the 64-byte TMA swizzle (chunk c of row r at chunk c ^ ((r >> 1) & 3)) -- the resident
+// B operand as it sits in shared memory -- and the exponents into the permuted blocks at xp + KTG XRES_TILE + 512 kt.
+// Each CTA then copies its K segment's tiles in with two bulk copies.
+__device__ __forceinline__ float load_x_block(const Args& a, const Geo& g, int j) {
   const int lane = threadIdx.x & 31;
-  const int nblk = 4 * g.KSG, npairs = nblk * g.T, step = 4 * NGRP;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int pr = p0 + q * step;
-    xs[q] = 0.f;
-    if (pr < npairs) {
-      const int t = pr / nblk, b = pr % nblk;
-      xs[q] = __uint_as_float((uint32_t)a.x[(int64_t)t * g.H + (ks0 * g.KSG + b / 4) * 128 + (b % 4) * 32 + lane] << 16);
-    }
-  }
+  if (j >= g.T * g.KTG * 4) return 0.f;
+  const int t = j / (g.KTG * 4), rem = j % (g.KTG * 4);
+  return __uint_as_float((uint32_t)a.x[(int64_t)t * g.H + rem * 32 + lane] << 16);
 }
-
-__device__ void split_x_res(const Args& a, const Geo& g, int ks0, int ew, uint8_t* xres, uint8_t* xsf,
-                            const float (&xfirst)[4]) {
+__device__ void split_x_global(const Args& a, const Geo& g, int gw, int nwarps, float xfirst) {
   const int lane = threadIdx.x & 31;
-  const int nblk = 4 * g.KSG, npairs = nblk * g.T, step = 4 * NGRP;
-  for (int p0 = ew; p0 < npairs; p0 += 4 * step) {
-    float xs[4];
-    if (p0 == ew) {
+  const int nblk = g.T * g.KTG * 4;
+  uint8_t* xp = a.ws + a.L.xp;
+  uint8_t* xpsf = xp + (int64_t)g.KTG * XRES_TILE;
+  for (int j = gw; j < nblk; j += nwarps) {
+    float r = j == gw ? xfirst : load_x_block(a, g, j);
+    const int t = j / (g.KTG * 4), rem = j % (g.KTG * 4), kt = rem / 4, kb = rem % 4;
+    const float am = warp_amax(r);
+    const bool nonfinite = !(am <= 3.4028235e38f);
+    const int e0 = mx4_exp(am);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) xs[q] = xfirst[q];
-    } else {
-      load_x4(a, g, ks0, ew, p0, xs);
-    }
-#pragma unroll 1
-    for (int q = 0; q < 4; ++q) {
-      const int pr = p0 + q * step;
-      if (pr >= npairs) break;
-      const int t = pr / nblk, b = pr % nblk, kk = b / 4, kb = b % 4;
-      // parts as in split_parts_n, stored as they are produced
-      float r = xs[q];
-      const float am = warp_amax(r);
-      const bool nonfinite = !(am <= 3.4028235e38f);
-      const int e0 = mx4_exp(am);
+    for (int p = 0; p < PARTS; ++p) {
+      const int e = nonfinite ? 255 : (e0 - 2 * p > 1 ? e0 - 2 * p : 1);
+      const uint32_t c = nonfinite ? 0u : e2m1_code(r * pow2_127m(e));
+      const uint32_t byte = c | (__shfl_down_sync(0xFFFFFFFFu, c, 1) << 4);  // elements (l, l + 1), even l
+      if (!nonfinite) r = r - e2m1_value(c) * pow2_m127(e);
+      // the 16 bytes of the part gathered into four words: word w from the even lanes 8 w .. 8 w + 6
+      uint32_t word = 0;
 #pragma unroll
-      for (int p = 0; p < PARTS; ++p) {
-        const int e = nonfinite ? 255 : (e0 - 2 * p > 1 ? e0 - 2 * p : 1);
-        const uint32_t c = nonfinite ? 0u : e2m1_code(r * pow2_127m(e));
-        const uint32_t hi = __shfl_down_sync(0xFFFFFFFFu, c, 1);
-        if (!nonfinite) r = r - e2m1_value(c) * pow2_m127(e);
-        const int n = PARTS * t + p;
-        if (!(lane & 1)) xres[kk * XRES_TILE + n * 64 + ((kb ^ ((n >> 1) & 3)) << 4) + (lane >> 1)] = (uint8_t)(c | (hi << 4));
-        if (lane == 0) xsf[kk * 512 + sfb(n, kb)] = (uint8_t)e;
-      }
+      for (int i = 0; i < 4; ++i) word |= (__shfl_sync(0xFFFFFFFFu, byte, (lane & ~7) + 2 * i) & 0xFFu) << (8 * i);
+      const int n = PARTS * t + p;
+      if ((lane & 7) == 0)
+        *reinterpret_cast<uint32_t*>(xp + (int64_t)kt * XRES_TILE + n * 64 + ((kb ^ ((n >> 1) & 3)) << 4) + (lane >> 1)) = word;
+      if (lane == 0) xpsf[kt * 512 + sfb(n, kb)] = (uint8_t)e;
     }
+    __syncwarp();
+    if (lane == 0) red_release_add(reinterpret_cast<uint32_t*>(a.ws + kCnt) + C_XP, 1u);
   }
 }
 
@@ -547,8 +536,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
   uint32_t* cnt = reinterpret_cast<uint32_t*>(a.ws + kCnt);
   Geo g = a.g;
   const long long lim = a.wait_ns;
-  float xfirst[4] = {0.f, 0.f, 0.f, 0.f};
-  if (warp >= EPI_WARP0) load_x4(a, g, (int)blockIdx.x % g.SG, warp - EPI_WARP0, warp - EPI_WARP0, xfirst);
+  const int xwarp = (int)blockIdx.x * (4 * NGRP) + (warp - EPI_WARP0), nxwarps = (int)gridDim.x * (4 * NGRP);
+  const float xfirst = warp >= EPI_WARP0 ? load_x_block(a, g, xwarp) : 0.f;  // before the weight stream starts
 
   float* lgw = reinterpret_cast<float*>(a.ws + a.L.lg);  // router logits [token][expert]
   if (a.wr && warp >= 2 && warp < 2 + 2 * NPIPE) {
@@ -587,12 +576,22 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
   tc_fence_after();
   const uint32_t tbase = s_tmem;
   if (warp >= EPI_WARP0) {
-    // the resident x parts of the CTA's gate/up segment (needed by its gate/up units; independent of the routing),
-    // while the other warps route and build the tables; then wait for the tables
-    split_x_res(a, g, (int)blockIdx.x % g.SG, warp - EPI_WARP0, xres, xres_sf, xfirst);
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> MMA (async proxy) reads
-    named_bar(1 + NGRP, 4 * NGRP * 32);
-    if (warp == EPI_WARP0 && lane == 0) mbar_arrive(&xres_full);
+    // this CTA's share of the x parts (independent of the routing), while the other warps route and build the
+    // tables; once every share is in, one thread copies the CTA's K segment of the image into the resident
+    // operand; then wait for the tables
+    split_x_global(a, g, xwarp, nxwarps, xfirst);
+    if (warp == EPI_WARP0 && lane == 0) {
+      if (wait_ge(cnt + C_XP, (uint32_t)(g.T * g.KTG * 4), &s_abort, lim)) {
+        asm volatile("fence.proxy.async.global;" ::: "memory");  // generic-proxy writes -> bulk-copy reads
+        const int ks0 = (int)blockIdx.x % g.SG;
+        const uint8_t* xp = a.ws + a.L.xp;
+        mbar_arrive_expect_tx(&xres_full, (uint32_t)(g.KSG * (XRES_TILE + 512)));
+        bulk_g2s_plain(xres, xp + (int64_t)ks0 * g.KSG * XRES_TILE, (uint32_t)(g.KSG * XRES_TILE), &xres_full);
+        bulk_g2s_plain(xres_sf, xp + (int64_t)g.KTG * XRES_TILE + ks0 * g.KSG * 512, (uint32_t)(g.KSG * 512), &xres_full);
+      } else {
+        record_error(&hdr->status, MOE_ERR_DEVICE_TIMEOUT);
+      }
+    }
     if (!bwait(&tab_full, 0, &s_abort, lim) && threadIdx.x == EPI_WARP0 * 32) record_error(&hdr->status, MOE_ERR_DEVICE_TIMEOUT);
   } else {
     if (a.wr) {
@@ -624,7 +623,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
     named_bar(2 + NGRP, EPI_WARP0 * 32);
     if (threadIdx.x == 0) {
       build_tables(tb, s_idx, s_wt, g.T, g.k, a.E);
-      if (tb.bad) { s_abort = 1; if (blockIdx.x == 0) record_error(&hdr->status, MOE_ERR_INVALID_ARG); }
+      // an expert id out of range: no units (every role finds an empty queue), status MOE_ERR_INVALID_ARG
+      if (tb.bad && blockIdx.x == 0) record_error(&hdr->status, MOE_ERR_INVALID_ARG);
       s_units = tb.bad ? 0 : tb.U * (g.RTG * g.SG + g.RTD * g.SD);
       build_order(ord, g, tb.bad ? 0 : tb.U);
       mbar_arrive(&tab_full);
@@ -773,6 +773,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
       for (int q = 0; q < tb.U * g.RTG; ++q) cnt[C_G + q] = 0;
       for (int q = 0; q < g.RTD; ++q) cnt[C_D + q] = 0;
       cnt[C_ROUTE] = 0;
+      cnt[C_XP] = 0;
       __threadfence();
       cnt[C_DONE] = 0;
     }
