@@ -175,7 +175,8 @@ __device__ __forceinline__ void split_parts_n(const float (&v)[NV], const bool (
 #pragma unroll
   for (int q = 0; q < NV; ++q) {
     r[q] = v[q];
-    am[q] = live[q] ? warp_amax(v[q]) : 0.f;
+    const float m = warp_amax(live[q] ? v[q] : 0.f);  // every lane takes part in the reduction
+    am[q] = live[q] ? m : 0.f;
   }
 #pragma unroll
   for (int q = 0; q < NV; ++q) {
@@ -252,17 +253,22 @@ struct Order {
   int start[2 * MAX_U + 1];    // first unit of each block; start[n] = total units
   int8_t d[2 * MAX_U], u[2 * MAX_U];
 };
-__device__ void build_order(Order& o, const Geo& g, int U) {
+// Blocks of the global unit order: G(0) .. G(U-1) then D(0) .. D(U-1) (every gate/up unit first: a down block
+// placed earlier waits for h of its expert while holding a pipeline). Built by one warp, a block per lane.
+static_assert(LAG == MAX_U, "the unit order puts every gate/up block first");
+__device__ void build_order_warp(Order& o, const Geo& g, int U) {
+  const int lane = threadIdx.x & 31;
   const int nGu = g.RTG * g.SG, nDu = g.RTD * g.SD;
-  int nb = 0, pos = 0;
-  auto add = [&](int d, int u) { o.start[nb] = pos; o.d[nb] = (int8_t)d; o.u[nb] = (int8_t)u; pos += d ? nDu : nGu; ++nb; };
-  for (int b = 0; b < U; ++b) {
-    add(0, b);
-    if (b >= LAG) add(1, b - LAG);
+  for (int b = lane; b < 2 * U; b += 32) {
+    const bool d = b >= U;
+    o.start[b] = d ? U * nGu + (b - U) * nDu : b * nGu;
+    o.d[b] = (int8_t)d;
+    o.u[b] = (int8_t)(d ? b - U : b);
   }
-  for (int b = U > LAG ? U - LAG : 0; b < U; ++b) add(1, b);
-  o.start[nb] = pos;
-  o.n = nb;
+  if (lane == 0) {
+    o.start[2 * U] = U * (nGu + nDu);
+    o.n = 2 * U;
+  }
 }
 __device__ __forceinline__ Unit unit_of(int v, const Geo& g, const Order& o) {
   int lo = 0, hi = o.n - 1;  // last block with start <= v
@@ -292,18 +298,42 @@ struct Tables {
   int bad;
 };
 
-__device__ void build_tables(Tables& tb, const int32_t (*idx)[MAX_K], const float (*w)[MAX_K], int T, int k, int E) {
-  tb.U = 0;
-  tb.bad = 0;
-  for (int t = 0; t < T; ++t)
-    for (int r = 0; r < k; ++r) tb.w[t][r] = w[t][r];
+// Built in two steps so that the weight stream starts as early as possible.
+// (1) build_union_warp, one warp: the union of the experts in first-appearance order over (t, r) and whether any id
+//     is out of range (match_any / ballot over the T k <= 64 entries, two per lane; no dependent memory chains).
+__device__ void build_union_warp(Tables& tb, const int32_t (*idx)[MAX_K], int T, int k, int E) {
+  const int lane = threadIdx.x & 31;
+  const int n = T * k;
+  const bool v0 = lane < n, v1 = lane + 32 < n;
+  const int e0 = v0 ? idx[lane / k][lane % k] : 0, e1 = v1 ? idx[(lane + 32) / k][(lane + 32) % k] : 0;
+  const bool bad = __any_sync(0xFFFFFFFFu, (v0 && (e0 < 0 || e0 >= E)) || (v1 && (e1 < 0 || e1 >= E)));
+  const int key0 = v0 ? e0 : -1 - lane, key1 = v1 ? e1 : -33 - lane;  // absent entries never match
+  const uint32_t lt = (1u << lane) - 1u;
+  // every lane takes part in each warp-wide operation (none sits inside a short-circuit or a branch)
+  const uint32_t m0 = __match_any_sync(0xFFFFFFFFu, key0), m1 = __match_any_sync(0xFFFFFFFFu, key1);
+  bool in0 = false;  // entry lane + 32 already appeared among entries 0 .. 31
+  for (int q = 0; q < 32; ++q) in0 |= __shfl_sync(0xFFFFFFFFu, key0, q) == key1;
+  const bool first0 = v0 && (m0 & lt) == 0;
+  const bool first1 = v1 && !in0 && (m1 & lt) == 0;
+  const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, first0), b1 = __ballot_sync(0xFFFFFFFFu, first1);
+  if (first0) tb.ue[__popc(b0 & lt)] = e0;
+  if (first1) tb.ue[__popc(b0) + __popc(b1 & lt)] = e1;
+  if (lane == 0) {
+    tb.U = __popc(b0) + __popc(b1);
+    tb.bad = bad ? 1 : 0;
+  }
+}
+// (2) build_slots, one thread, while the first weight tiles are in flight: the routing weights, each union expert's
+//     tokens (slot order = token order) and, per (t, r), the union index and the token's slot in that expert.
+__device__ void build_slots(Tables& tb, const int32_t (*idx)[MAX_K], const float (*w)[MAX_K], int T, int k) {
+  for (int u = 0; u < tb.U; ++u) tb.ntok[u] = 0;
   for (int t = 0; t < T; ++t)
     for (int r = 0; r < k; ++r) {
+      tb.w[t][r] = w[t][r];
       const int e = idx[t][r];
-      if (e < 0 || e >= E) { tb.bad = 1; tb.pu[t][r] = 0; tb.ps[t][r] = 0; continue; }
       int u = 0;
       while (u < tb.U && tb.ue[u] != e) ++u;
-      if (u == tb.U) { tb.ue[u] = e; tb.ntok[u] = 0; tb.U = u + 1; }
+      if (u == tb.U) { tb.pu[t][r] = 0; tb.ps[t][r] = 0; continue; }  // an invalid id (no units run)
       int s = 0;
       while (s < tb.ntok[u] && tb.tok[u][s] != t) ++s;
       if (s == tb.ntok[u]) { tb.tok[u][s] = (int8_t)t; tb.ntok[u] = (int8_t)(s + 1); }
@@ -520,7 +550,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ __align__(8) uint64_t full[NSLOT], empty[NSLOT], acc_full[NPIPE][ABUF_MAX],
       acc_empty[NPIPE][ABUF_MAX], drain[NPIPE];
-  __shared__ __align__(8) uint64_t uq_full[NPIPE][QN], xres_full, tab_full;
+  __shared__ __align__(8) uint64_t uq_full[NPIPE][QN], xres_full, tab_full, tab2_full;
   uint8_t* xres = smem + NSLOT * SLOT_BYTES;    // resident x parts of this CTA's gate/up K segment
   uint8_t* xres_sf = xres + 8 * XRES_TILE;
   __shared__ volatile int uq[NPIPE][QN];
@@ -566,6 +596,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
     }
     mbar_init(&xres_full, 1);
     mbar_init(&tab_full, 1);
+    mbar_init(&tab2_full, 1);
     s_abort = 0;
     s_next = 0;
     fence_mbar_init();
@@ -580,19 +611,31 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
     // tables; once every share is in, one thread copies the CTA's K segment of the image into the resident
     // operand; then wait for the tables
     split_x_global(a, g, xwarp, nxwarps, xfirst);
-    if (warp == EPI_WARP0 && lane == 0) {
-      if (wait_ge(cnt + C_XP, (uint32_t)(g.T * g.KTG * 4), &s_abort, lim)) {
-        asm volatile("fence.proxy.async.global;" ::: "memory");  // generic-proxy writes -> bulk-copy reads
-        const int ks0 = (int)blockIdx.x % g.SG;
-        const uint8_t* xp = a.ws + a.L.xp;
-        mbar_arrive_expect_tx(&xres_full, (uint32_t)(g.KSG * (XRES_TILE + 512)));
-        bulk_g2s_plain(xres, xp + (int64_t)ks0 * g.KSG * XRES_TILE, (uint32_t)(g.KSG * XRES_TILE), &xres_full);
-        bulk_g2s_plain(xres_sf, xp + (int64_t)g.KTG * XRES_TILE + ks0 * g.KSG * 512, (uint32_t)(g.KSG * 512), &xres_full);
-      } else {
-        record_error(&hdr->status, MOE_ERR_DEVICE_TIMEOUT);
+    if (warp == EPI_WARP0) {  // (the other lanes wait at the warp barrier, not spinning beside lane 0)
+      if (lane == 0) {
+        if (wait_ge(cnt + C_XP, (uint32_t)(g.T * g.KTG * 4), &s_abort, lim)) {
+          asm volatile("fence.proxy.async.global;" ::: "memory");  // generic-proxy writes -> bulk-copy reads
+          const int ks0 = (int)blockIdx.x % g.SG;
+          const uint8_t* xp = a.ws + a.L.xp;
+          mbar_arrive_expect_tx(&xres_full, (uint32_t)(g.KSG * (XRES_TILE + 512)));
+          bulk_g2s_plain(xres, xp + (int64_t)ks0 * g.KSG * XRES_TILE, (uint32_t)(g.KSG * XRES_TILE), &xres_full);
+          bulk_g2s_plain(xres_sf, xp + (int64_t)g.KTG * XRES_TILE + ks0 * g.KSG * 512, (uint32_t)(g.KSG * 512),
+                         &xres_full);
+        } else {
+          record_error(&hdr->status, MOE_ERR_DEVICE_TIMEOUT);
+        }
       }
+      __syncwarp();
     }
     if (!bwait(&tab_full, 0, &s_abort, lim) && threadIdx.x == EPI_WARP0 * 32) record_error(&hdr->status, MOE_ERR_DEVICE_TIMEOUT);
+    if (warp == EPI_WARP0) {  // the token tables the epilogues need, while the first tiles stream in
+      if (lane == 0) {
+        build_slots(tb, s_idx, s_wt, g.T, g.k);
+        mbar_arrive(&tab2_full);
+      }
+      __syncwarp();
+    }
+    if (!bwait(&tab2_full, 0, &s_abort, lim) && threadIdx.x == EPI_WARP0 * 32) record_error(&hdr->status, MOE_ERR_DEVICE_TIMEOUT);
   } else {
     if (a.wr) {
       // routing, phase 2: every CTA selects each token's experts from all the logits (one warp per token)
@@ -621,13 +664,18 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
       s_wt[threadIdx.x / g.k][threadIdx.x % g.k] = a.w[threadIdx.x];
     }
     named_bar(2 + NGRP, EPI_WARP0 * 32);
-    if (threadIdx.x == 0) {
-      build_tables(tb, s_idx, s_wt, g.T, g.k, a.E);
-      // an expert id out of range: no units (every role finds an empty queue), status MOE_ERR_INVALID_ARG
-      if (tb.bad && blockIdx.x == 0) record_error(&hdr->status, MOE_ERR_INVALID_ARG);
-      s_units = tb.bad ? 0 : tb.U * (g.RTG * g.SG + g.RTD * g.SD);
-      build_order(ord, g, tb.bad ? 0 : tb.U);
-      mbar_arrive(&tab_full);
+    if (warp == 0) {
+      build_union_warp(tb, s_idx, g.T, g.k, a.E);
+      __syncwarp();
+      const int U = tb.bad ? 0 : tb.U;
+      build_order_warp(ord, g, U);
+      __syncwarp();
+      if (lane == 0) {
+        // an expert id out of range: no units (every role finds an empty queue), status MOE_ERR_INVALID_ARG
+        if (tb.bad && blockIdx.x == 0) record_error(&hdr->status, MOE_ERR_INVALID_ARG);
+        s_units = U * (g.RTG * g.SG + g.RTD * g.SD);
+        mbar_arrive(&tab_full);
+      }
     }
     named_bar(2 + NGRP, EPI_WARP0 * 32);
   }
