@@ -103,7 +103,7 @@ inline Ws ws_layout(int64_t H, int64_t I, int64_t Umax, int64_t TS) {
   w.hsf = o;   o = al1k(o + Umax * KTD * 512);
   w.gpart = o; o = al1k(o + Umax * RTG * SG * TS * 128 * 4);
   w.dpart = o; o = al1k(o + Umax * RTD * SD * TS * 128 * 4);
-  w.lg = o;    o = al1k(o + (int64_t)kRouteTPC * kRouteMaxE * 4);  // router logits [token][expert]
+  w.lg = o;    o = al1k(o + (int64_t)kRouteTPC * 2 * kRouteMaxE * 4);  // router logit halves [token][half][expert]
   w.xp = o;    o = al1k(o + (H / 128) * (XRES_TILE + 512));      // x parts: [k-tile][48 rows][64 B], then exponents
   w.total = o;
   return w;
@@ -569,15 +569,16 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
   const int xwarp = (int)blockIdx.x * (4 * NGRP) + (warp - EPI_WARP0), nxwarps = (int)gridDim.x * (4 * NGRP);
   const float xfirst = warp >= EPI_WARP0 ? load_x_block(a, g, xwarp) : 0.f;  // before the weight stream starts
 
-  float* lgw = reinterpret_cast<float*>(a.ws + a.L.lg);  // router logits [token][expert]
+  float* lgw = reinterpret_cast<float*>(a.ws + a.L.lg);  // router logit halves [token][half][expert]
   if (a.wr && warp >= 2 && warp < 2 + 2 * NPIPE) {
-    // routing, phase 1 (at entry, while thread 0 and warp 1 set the CTA up): the logits of experts
-    // blockIdx.x + gridDim.x * (w + 2 NPIPE i), w = warp - 2, spread over the grid
-    for (int e = (int)blockIdx.x + (int)gridDim.x * (warp - 2); e < a.E; e += (int)gridDim.x * 2 * NPIPE) {
+    // routing, phase 1 (at entry, while thread 0 and warp 1 set the CTA up): the logit halves (expert e, half c),
+    // task q = blockIdx.x + gridDim.x * (w + 2 NPIPE i), e = q / 2, c = q % 2, w = warp - 2, spread over the grid
+    for (int q = (int)blockIdx.x + (int)gridDim.x * (warp - 2); q < 2 * a.E; q += (int)gridDim.x * 2 * NPIPE) {
+      const int e = q >> 1, c = q & 1;
       float acc[kRouteTPC];
-      route_row_logits<8>(a.wr + (size_t)e * g.H, g.H, g.T, [&](int t) { return a.x + (size_t)t * g.H; }, acc);
+      route_half_logits<8>(a.wr + (size_t)e * g.H, g.H, g.T, [&](int t) { return a.x + (size_t)t * g.H; }, c, acc);
       if (lane == 0)
-        for (int t = 0; t < g.T; ++t) __stcg(lgw + t * a.E + e, acc[t]);
+        for (int t = 0; t < g.T; ++t) __stcg(lgw + (t * 2 + c) * a.E + e, acc[t]);
       __syncwarp();
       if (lane == 0) red_release_add(cnt + C_ROUTE, 1u);
     }
@@ -641,13 +642,14 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
       // routing, phase 2: every CTA selects each token's experts from all the logits (one warp per token)
       if (warp < g.T) {
         bool ok = true;
-        if (lane == 0) ok = wait_ge(cnt + C_ROUTE, (uint32_t)a.E, &s_abort, lim);
+        if (lane == 0) ok = wait_ge(cnt + C_ROUTE, (uint32_t)(2 * a.E), &s_abort, lim);
         ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
         int sid[8];
         float sw[8];
         if (ok) {
-          const float* row = lgw + warp * a.E;
-          route_topk_warp<kRouteMaxE / 32 / 4>([&](int e) { return __ldcg(row + e); }, a.E, g.k, sid, sw);
+          const float* row = lgw + warp * 2 * a.E;  // half 0, then half 1, of every expert's logit
+          route_topk_warp<kRouteMaxE / 32 / 4>([&](int e) { return __ldcg(row + e) + __ldcg(row + a.E + e); }, a.E, g.k,
+                                               sid, sw);
         }
         if (lane == 0)
           for (int r = 0; r < g.k; ++r) {

@@ -2,9 +2,8 @@
 // in its first phase (decode_tc.cu), so that both give the same bits ("Mixed-precision compression of
 // DeepSeek-V4-Flash" (lumirain.cn), "The recipe": F16 router, top-6 of 256 routed experts, softmax weights).
 //
-// Logit of expert e for token t: sum over h of W_r[e, h] * x[t, h] (fp16 x bf16 products are exact in fp32). Lane
-// l of a warp sums, in order, the 8-element pieces at h = 8 l + 256 i (i = 0, 1, ...) with fused multiply-adds;
-// then a fixed butterfly (xor 16, 8, 4, 2, 1) adds the lanes. Top-k: k rounds of a warp arg-max with ties to the
+// Logit of expert e for token t: sum over h of W_r[e, h] * x[t, h] (fp16 x bf16 products are exact in fp32), as two
+// halves over h, each a lane-strided ordered sum and a fixed butterfly (route_half_logits), added. Top-k: k rounds of a warp arg-max with ties to the
 // lower expert index; weights exp(l_r - l_0) / sum_j exp(l_j - l_0) in rank order.
 #pragma once
 #include <cstdint>
@@ -15,26 +14,29 @@ namespace moe {
 constexpr int kRouteTPC = 8;    // tokens per pass
 constexpr int kRouteMaxE = 1024;
 
-// Logits of one expert row for tokens 0 .. nt-1; xrow(t) points at token t's x (shared or global memory). BATCH
-// pieces per lane are loaded before they are used; it changes when the loads are issued, not the sums.
+// Half c (0 or 1) of the logits of one expert row for tokens 0 .. nt-1: lane l sums, in order, the 8-element
+// pieces at h = 8 l + 256 i for i in [c P2, min(P, (c + 1) P2)), P = H / 256, P2 = ceil(P / 2), with fused
+// multiply-adds; then a fixed butterfly (xor 16, 8, 4, 2, 1) adds the lanes. The logit is half 0 + half 1, so the
+// two halves can be computed by different warps. xrow(t) points at token t's x (shared or global memory); BATCH
+// pieces per lane are loaded before they are used (it changes when the loads are issued, not the sums).
 template <int BATCH, typename XRow>
-__device__ __forceinline__ void route_row_logits(const uint16_t* __restrict__ row, int H, int nt, XRow xrow,
-                                                 float (&acc)[kRouteTPC]) {
+__device__ __forceinline__ void route_half_logits(const uint16_t* __restrict__ row, int H, int nt, XRow xrow, int c,
+                                                  float (&acc)[kRouteTPC]) {
   const int lane = threadIdx.x & 31;
+  const int P = H / 256, P2 = (P + 1) / 2, i_beg = c * P2, i_end = min(P, (c + 1) * P2);
 #pragma unroll
   for (int t = 0; t < kRouteTPC; ++t) acc[t] = 0.f;
-  // the row's 16-byte pieces for this lane, fetched in batches so the loads are in flight together
-  for (int h0 = lane * 8; h0 < H; h0 += 256 * BATCH) {
+  for (int i0 = i_beg; i0 < i_end; i0 += BATCH) {
     uint4 wv[BATCH];
 #pragma unroll
     for (int b = 0; b < BATCH; ++b) {
-      const int h = h0 + 256 * b;
-      wv[b] = h < H ? __ldg(reinterpret_cast<const uint4*>(row + h)) : make_uint4(0u, 0u, 0u, 0u);
+      const int h = lane * 8 + 256 * (i0 + b);
+      wv[b] = i0 + b < i_end ? __ldg(reinterpret_cast<const uint4*>(row + h)) : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
     for (int b = 0; b < BATCH; ++b) {
-      const int h = h0 + 256 * b;
-      if (h >= H) break;
+      if (i0 + b >= i_end) break;
+      const int h = lane * 8 + 256 * (i0 + b);
       const uint32_t ww[4] = {wv[b].x, wv[b].y, wv[b].z, wv[b].w};
       float wf[8];
 #pragma unroll
@@ -66,6 +68,16 @@ __device__ __forceinline__ void route_row_logits(const uint16_t* __restrict__ ro
     v += __shfl_xor_sync(0xffffffffu, v, 1);
     acc[t] = v;
   }
+}
+// The whole logit: half 0 + half 1.
+template <int BATCH, typename XRow>
+__device__ __forceinline__ void route_row_logits(const uint16_t* __restrict__ row, int H, int nt, XRow xrow,
+                                                 float (&acc)[kRouteTPC]) {
+  float h1[kRouteTPC];
+  route_half_logits<BATCH>(row, H, nt, xrow, 0, acc);
+  route_half_logits<BATCH>(row, H, nt, xrow, 1, h1);
+#pragma unroll
+  for (int t = 0; t < kRouteTPC; ++t) acc[t] = acc[t] + h1[t];
 }
 
 // Top-k of one token by the whole warp; logit(e) gives expert e's logit (e < E <= 32 * NE). Lane 0 gets the experts
