@@ -20,8 +20,8 @@
 // then D units; the grid is a multiple of the number of gate/up segments, so all G units of a CTA share one K
 // segment and the CTA keeps that segment's x parts resident in shared memory (computed at kernel start).
 // Inside a CTA, three independent pipelines take the CTA's units as they free up. A pipeline is a weight-issuing
-// warp, an activation-issuing warp (h parts of D units, after their h is final), an MMA-issuing warp, a five-slot
-// shared-memory ring, two TMEM accumulators and a group of four epilogue warps. One issuing thread sustains only
+// warp, an activation-issuing warp (h parts of D units, after their h is final), an MMA-issuing warp, a three-slot
+// shared-memory ring, two to four TMEM accumulators and a group of four epilogue warps. One issuing thread sustains only
 // about one wait-and-issue round per 330 ns (TMA) or one stage of MMAs plus commit per ~600 cycles (tcgen05),
 // while one SM must consume an 8.5 KB weight tile every ~180 ns to keep pace with HBM. Cross-CTA dependencies
 // (partials complete, h of an expert's K segment final) are global counters with bounded waits; the last CTA to
@@ -40,7 +40,8 @@ namespace moe {
 namespace dtc {
 
 constexpr int NPIPE = 3;                 // pipelines per CTA
-constexpr int RING = 5;                  // stage slots per pipeline
+constexpr int RING = 3;                  // stage slots per pipeline (more bytes in flight only lengthen the queues:
+                                         // every dependent L2 round trip of the call then takes longer)
 constexpr int NSLOT = NPIPE * RING;
 constexpr int PARTS = 6;                 // E2M1 parts per activation value
 constexpr int NB = 48;                   // B rows (MMA N): PARTS x 8 tokens
