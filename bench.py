@@ -110,7 +110,7 @@ class ClockSampler:
 # ------------------------------------------------------------------------------------------------ GPU arm
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the tensor-core decode kernel as it stands, from the
 # ncu capture summarised in profiles/decode_kernel_mxfp4_ds4_t1.md (routing given, small expert pool, same 6-expert bytes)
-TC_TRAFFIC = 83406336
+TC_TRAFFIC = 82944512
 
 
 def run_ours(args):
