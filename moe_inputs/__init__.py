@@ -96,3 +96,22 @@ def zipf_routing(seed: int, T: int, E: int, k: int, s: float = 1.1):
     u = rng.uniform(0.5, 1.5, size=(T, k))
     w = (u / u.sum(axis=1, keepdims=True)).astype(np.float32)
     return idx, w
+
+
+def spec_inputs(seed: int, K: int, V: int, spread: float = 2.0, noise: float = 0.5):
+    """Synthetic speculative-decoding inputs: target distributions p [K+1, V] and draft distributions q [K, V]
+    (fp32, each row the fp32 rounding of a float64 softmax of N(0, spread) logits; a draft row's logits are the
+    target row's plus N(0, noise)), K drafted tokens drawn from the q rows, and K + 1 uniforms u in [0, 1) with
+    24 random bits each."""
+    rng = _rng(seed, 8181, K, V)
+    lp = rng.normal(0.0, spread, size=(K + 1, V))
+    lq = lp[:K] + rng.normal(0.0, noise, size=(K, V))
+
+    def softmax(l):
+        e = np.exp(l - l.max(axis=1, keepdims=True))
+        return e / e.sum(axis=1, keepdims=True)
+
+    p64, q64 = softmax(lp), softmax(lq) if K else np.zeros((0, V))
+    draft = np.array([rng.choice(V, p=q64[k]) for k in range(K)], dtype=np.int32)
+    u = (rng.integers(0, 1 << 24, size=K + 1) * 2.0 ** -24).astype(np.float32)
+    return p64.astype(np.float32), q64.astype(np.float32), draft, u

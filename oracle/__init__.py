@@ -76,6 +76,7 @@ def lib():
                 "orc_moe_batch": (None, [i32, i32, i32, i32, i32, P, P, P, i32, P, P, P, P, P, i32]),
                 "orc_prefill_token": (None, [i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P, P]),
                 "orc_max_threads": (i32, []),
+                "orc_spec_accept": (None, [P, P, i32, i32, P, P, P]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -279,3 +280,23 @@ def prefill_token(H: int, I: int, gate_of, up_of, down_of, idx_t, w_t, x_t_bf16)
                             _p(hc), _p(hs), _p(h))
     return dict(y=y, absterm=ab, xq_codes=xc, xq_scales=xs, hq_codes=hc.reshape(k, I),
                 hq_scales=hs.reshape(k, I // 32), h=h.reshape(k, I))
+
+
+# ---------------------------------------------------------------- speculative acceptance
+def spec_accept(p: np.ndarray, q: np.ndarray, draft, u) -> tuple[int, int]:
+    """The chain of K drafted tokens under the acceptance rule of [P2] "What compression does not solve"
+    (accept draft k with probability min(1, p_k(d)/q_k(d)); at the first rejection draw from max(p_k - q_k, 0)
+    normalised; after K acceptances draw from p_K). p [K+1, V] fp32, q [K, V] fp32, draft [K] int32,
+    u [K+1] fp32 (u[K] drives the draw). -> (accepted drafts n, drawn token); (-1, -1) for a draft id outside
+    [0, V). The arithmetic of the decision and of the draw is fixed in oracle.c (fp32 quotient, exact integer
+    inverse CDF)."""
+    pp = _c(p, np.float32)
+    K1, V = pp.shape
+    K = K1 - 1
+    qq = _c(q, np.float32).reshape(K, V) if K > 0 else np.zeros((1, V), np.float32)
+    d = _c(np.asarray(draft, dtype=np.int32).reshape(-1), np.int32) if K > 0 else np.zeros(1, np.int32)
+    uu = _c(np.asarray(u, dtype=np.float32).reshape(-1), np.float32)
+    assert uu.size == K + 1 and (K == 0 or d.size == K)
+    out = np.empty(2, dtype=np.int32)
+    lib().orc_spec_accept(_p(pp), _p(qq), K, V, _p(d), _p(uu), _p(out))
+    return int(out[0]), int(out[1])

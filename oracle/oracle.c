@@ -674,3 +674,64 @@ int orc_max_threads(void) {
   return 1;
 #endif
 }
+
+/* ---------------------------------------------------------------- speculative acceptance
+ * [P2] "What compression does not solve": a drafted token x is accepted with probability min(1, p(x) / q(x));
+ * on a rejection the token is drawn from max(p - q, 0), normalised; this keeps the target's distribution exact.
+ * The chain of K drafts is the usual reading: drafts are tested in order, the first rejection ends the chain
+ * and is replaced by a draw from that position's residual; if all K are accepted, one more token is drawn
+ * from the target's distribution after the last draft.
+ *
+ * Readings (the pages give the rule, not its arithmetic):
+ *   - p, q, u are fp32; draft k is accepted when u[k] < p_k(d) / q_k(d), the quotient one fp32 division
+ *     (q = 0 < p accepts; p = q = 0 rejects);
+ *   - a draw from weights r(v) (r = p - q or p, clamped to [0, 1], NaN as 0) with the uniform u_s: the
+ *     smallest v whose running sum exceeds u_s times the total, in exact integers: R(v) = floor(r(v) 2^40),
+ *     U = floor(u_s 2^32) (u_s clamped to [0, 1)), threshold floor(U * sum R / 2^32); V <= 2^22 keeps the
+ *     sums inside 64 bits;
+ *   - a residual with no mass falls back to p of that position; a row with no mass gives token -1;
+ *   - a draft id outside [0, V) gives n = -1 and token -1.
+ * p [K+1][V], q [K][V], draft [K], u [K+1] (u[K] is the draw's uniform); out[0] = accepted drafts n,
+ * out[1] = the token drawn after them. */
+static uint64_t spec_weight(const float* p, const float* q, int v) {
+  float r = q ? p[v] - q[v] : p[v];
+  if (!(r > 0.0f)) r = 0.0f;  /* negative or NaN: no mass */
+  if (r > 1.0f) r = 1.0f;     /* a probability is at most 1 */
+  return (uint64_t)ldexp((double)r, 40);
+}
+static int64_t spec_draw(const float* p, const float* q, int V, float us) {
+  uint64_t total = 0;
+  for (int v = 0; v < V; ++v) total += spec_weight(p, q, v);
+  if (total == 0) return -1;
+  double uc = us < 0.0f ? 0.0 : (double)us;
+  uint64_t U = uc >= 1.0 ? 0xFFFFFFFFull : (uint64_t)ldexp(uc, 32);
+  const uint64_t thr = (uint64_t)(((unsigned __int128)U * total) >> 32);
+  uint64_t run = 0;
+  for (int v = 0; v < V; ++v) {
+    run += spec_weight(p, q, v);
+    if (run > thr) return v;
+  }
+  return -1;
+}
+
+void orc_spec_accept(const float* p, const float* q, int K, int V, const int32_t* draft, const float* u,
+                     int32_t* out) {
+  for (int k = 0; k < K; ++k)
+    if (draft[k] < 0 || draft[k] >= V) { out[0] = -1; out[1] = -1; return; }
+  int n = 0;
+  while (n < K) {
+    const int d = draft[n];
+    const float ratio = p[(int64_t)n * V + d] / q[(int64_t)n * V + d];
+    if (!(u[n] < ratio)) break;
+    ++n;
+  }
+  int64_t tok;
+  if (n < K) {
+    tok = spec_draw(p + (int64_t)n * V, q + (int64_t)n * V, V, u[K]);
+    if (tok < 0) tok = spec_draw(p + (int64_t)n * V, NULL, V, u[K]);
+  } else {
+    tok = spec_draw(p + (int64_t)K * V, NULL, V, u[K]);
+  }
+  out[0] = n;
+  out[1] = (int32_t)tok;
+}
