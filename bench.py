@@ -305,6 +305,7 @@ def run_ours(args):
 
     prefill = bench_prefill(m, torch, args, dev, stream, layer_p, E) if do_prefill else None
     verify = bench_verify(m, torch, args, dev, stream, layer, wr, x_host, E, per_expert) if (use_tc and not args.no_verify) else None
+    spec = bench_spec(m, torch, dev, stream) if not args.no_verify else None
 
     out = None
     if rank == 0:
@@ -347,6 +348,7 @@ def run_ours(args):
             "clocks": clk,
             "prefill": prefill,
             "verify": verify,
+            "spec_accept": spec,
             "setup_s": round(setup_s, 1),
             "cuda_graph": use_graph,
         }
@@ -413,6 +415,43 @@ def bench_verify(m, torch, args, dev, stream, layer, wr, x_host, E, per_expert):
     if m.moe_get_device_status(ws, stream) != 0:
         raise RuntimeError("device status after the verify measurements")
     return out
+
+
+def bench_spec(m, torch, dev, stream, K=7, V=32768, n_sets=32, reps=8):
+    """Acceptance of K = 7 drafts (a verify batch of 8 tokens) over a V = 32768 vocabulary (the hash-routed layers'
+    vocabulary): n_sets seeded (p, q, drafts, u) sets, one call each, replayed reps times as a CUDA graph.
+    The kernel reads one or two rows of V floats per call; its time is latency (one CTA, two block scans)."""
+    from moe_inputs import spec_inputs
+    sets = [spec_inputs(500 + i, K, V) for i in range(n_sets)]
+    P = torch.from_numpy(np.stack([s[0] for s in sets])).to(dev)
+    Q = torch.from_numpy(np.stack([s[1] for s in sets])).to(dev)
+    D = torch.from_numpy(np.stack([s[2] for s in sets])).to(dev)
+    U = torch.from_numpy(np.stack([s[3] for s in sets])).to(dev)
+    R = torch.zeros((n_sets, 2), dtype=torch.int32, device=dev)
+
+    def launch():
+        for i in range(n_sets):
+            m.moe_spec_accept(P[i], Q[i], K, V, D[i], U[i], R[i], stream=stream)
+    with torch.cuda.stream(stream):
+        launch()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        launch()
+    with torch.cuda.stream(stream):
+        g.replay()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            g.replay()
+    e1.record(stream)
+    e1.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (reps * n_sets)
+    kept = R[:, 0].float().mean().item()
+    return {"workload": "acceptance of %d drafts, vocabulary %d, %d seeded sets" % (K, V, n_sets),
+            "us_per_call": round(us, 3), "calls": reps * n_sets, "mean_kept": round(kept, 2),
+            "gpu_launches_per_call": 1}
 
 
 def bench_prefill(m, torch, args, dev, stream, layer_p, E):

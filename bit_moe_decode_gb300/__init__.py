@@ -31,7 +31,7 @@ EXPORTS = ["moe_status_string", "moe_version", "moe_check_device", "moe_canonica
            "moe_encode_blocks", "moe_pack_weights", "moe_route_topk", "moe_workspace_bytes", "moe_workspace_init",
            "moe_get_device_status", "moe_expert_ffn_decode", "moe_expert_ffn_verify", "moe_route_expert_ffn",
            "moe_debug_unpack", "moe_debug_timeout_probe", "moe_expert_ffn_decode_static", "moe_prefill_workspace_bytes",
-           "moe_expert_grouped_gemm_prefill", "moe_debug_prefill"]
+           "moe_expert_grouped_gemm_prefill", "moe_debug_prefill", "moe_spec_accept"]
 
 
 class MoeError(RuntimeError):
@@ -66,6 +66,7 @@ def lib() -> C.CDLL:
             "moe_encode_blocks": (C.c_int, [C.c_int, P, i64, i64, P, P]),
             "moe_pack_weights": (C.c_int, [C.c_int, C.c_int, C.c_int, C.c_int, i64, i64, i64, P, P, P, sz, P]),
             "moe_route_topk": (C.c_int, [P, P, i32, i32, i32, i32, P, P, i32, P, P, P]),
+            "moe_spec_accept": (C.c_int, [P, P, i32, i32, P, P, P, P]),
             "moe_workspace_bytes": (sz, [LP, i32, i32]),
             "moe_workspace_init": (C.c_int, [P, sz, P]),
             "moe_get_device_status": (C.c_int, [P, P]),
@@ -141,6 +142,12 @@ def moe_route_topk(router_w_f16, x_bf16, T: int, H: int, E: int, k: int, token_i
                    idx: torch.Tensor, weights: torch.Tensor, stream=None):
     _check(lib().moe_route_topk(_ptr(router_w_f16), _ptr(x_bf16), T, H, E, k, _ptr(token_ids), _ptr(tid2eid), V,
                                 _ptr(idx), _ptr(weights), _stream(stream)), "moe_route_topk")
+
+
+def moe_spec_accept(p, q, K: int, V: int, draft, u, result, stream=None):
+    """Acceptance of K drafted tokens (see include/moe.h): result[0] = drafts kept, result[1] = the drawn token."""
+    _check(lib().moe_spec_accept(_ptr(p), _ptr(q), K, V, _ptr(draft), _ptr(u), _ptr(result), _stream(stream)),
+           "moe_spec_accept")
 
 
 def moe_workspace_bytes(layer: "Layer", T_max: int, k: int) -> int:

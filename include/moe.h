@@ -25,7 +25,7 @@
  *     workspace; read it with moe_get_device_status(). After such an error call moe_workspace_init() again.
  *   - The library keeps no mutable global state except a per-process cache of device properties.
  *   - Host-side fault injection for tests: if the environment variable MOE_FAULT names a call
- *     ("pack", "route", "decode", "verify", "prefill", "encode"), that call returns MOE_ERR_FAULT_INJECTED
+ *     ("pack", "route", "decode", "verify", "prefill", "encode", "spec"), that call returns MOE_ERR_FAULT_INJECTED
  *     without launching anything.
  */
 #ifndef BIT_MOE_DECODE_GB300_MOE_H
@@ -189,6 +189,30 @@ moe_status_t moe_route_expert_ffn(const moe_layer_t* layer, const void* router_w
 moe_status_t moe_expert_ffn_decode_static(const moe_layer_t* layer, const void* x_bf16, const int32_t* idx,
                                           const float* w, int32_t k, float* y, void* y_bf16, int32_t accumulate,
                                           void* stream);
+
+/* ---------------------------------------------------------------- speculative acceptance ------------------------ */
+
+/* Acceptance of K drafted tokens after the verify sweep that scored them ("Mixed-precision compression of
+ * DeepSeek-V4-Flash" (lumirain.cn), "What compression does not solve": a draft x is kept with probability
+ * min(1, p(x) / q(x)); on a rejection the token is drawn from max(p - q, 0), normalised, which keeps the target's
+ * distribution exactly).
+ *   p [K+1, V] fp32: the target's distribution at each drafted position and after the last draft;
+ *   q [K, V] fp32: the drafter's distribution at each drafted position;
+ *   draft [K] int32: the drafted tokens; u [K+1] fp32 uniforms in [0, 1): u[k] decides draft k, u[K] drives the
+ *   one draw. All are device pointers; the caller owns them.
+ *   result [2] int32 (device): result[0] = n, the drafts kept (the first n, in order); result[1] = the token
+ *   drawn after them: from the normalised max(p_n - q_n, 0) if draft n was rejected (from p_n if that residual
+ *   has no mass), from p_K if all K were kept; -1 if the row has no mass.
+ *   Arithmetic: draft k is kept when u[k] < p_k(d) / q_k(d) (one fp32 division: q = 0 < p keeps, p = q = 0
+ *   rejects); the draw is an exact integer inverse CDF: weights clamped to [0, 1] (NaN as 0) scaled to
+ *   floor(r 2^40), threshold floor(floor(u 2^32) * total / 2^32), the smallest v whose running sum exceeds it.
+ *   The same inputs always give the same tokens.
+ *   Limits: 0 <= K <= 8, 1 <= V <= 2^22; 4-byte aligned pointers; q and draft may be NULL when K = 0.
+ *   A draft id outside [0, V) is device data: the call then writes n = -1 and token -1.
+ *   Errors: MOE_ERR_INVALID_ARG (null or misaligned pointer), MOE_ERR_SHAPE (K or V out of range), both before
+ *   any launch. One CTA; runs on `stream`. */
+moe_status_t moe_spec_accept(const float* p, const float* q, int32_t K, int32_t V, const int32_t* draft,
+                             const float* u, int32_t* result, void* stream);
 
 /* ---------------------------------------------------------------- prefill --------------------------------------- */
 

@@ -687,7 +687,7 @@ int orc_max_threads(void) {
  *     (q = 0 < p accepts; p = q = 0 rejects);
  *   - a draw from weights r(v) (r = p - q or p, clamped to [0, 1], NaN as 0) with the uniform u_s: the
  *     smallest v whose running sum exceeds u_s times the total, in exact integers: R(v) = floor(r(v) 2^40),
- *     U = floor(u_s 2^32) (u_s clamped to [0, 1)), threshold floor(U * sum R / 2^32); V <= 2^22 keeps the
+ *     U = floor(u_s 2^32) (u_s clamped to [0, 1), NaN as 0), threshold floor(U * sum R / 2^32); V <= 2^22 keeps the
  *     sums inside 64 bits;
  *   - a residual with no mass falls back to p of that position; a row with no mass gives token -1;
  *   - a draft id outside [0, V) gives n = -1 and token -1.
@@ -703,8 +703,8 @@ static int64_t spec_draw(const float* p, const float* q, int V, float us) {
   uint64_t total = 0;
   for (int v = 0; v < V; ++v) total += spec_weight(p, q, v);
   if (total == 0) return -1;
-  double uc = us < 0.0f ? 0.0 : (double)us;
-  uint64_t U = uc >= 1.0 ? 0xFFFFFFFFull : (uint64_t)ldexp(uc, 32);
+  const double uc = us > 0.0f ? (double)us : 0.0;  /* negative or NaN: 0 */
+  const uint64_t U = uc >= 1.0 ? 0xFFFFFFFFull : (uint64_t)ldexp(uc, 32);
   const uint64_t thr = (uint64_t)(((unsigned __int128)U * total) >> 32);
   uint64_t run = 0;
   for (int v = 0; v < V; ++v) {

@@ -82,3 +82,13 @@ def test_fault_injection_and_argument_checks(m, monkeypatch):
     assert L.moe_pack_weights(1, 0, 0, 0, 1, 512, 256, None, None, None, 0, None) == 1
     assert L.moe_pack_weights(9, 0, 0, 0, 1, 512, 256, None, None, None, 0, None) == 3
     assert L.moe_route_topk(None, None, 1, 4096, 256, 6, None, None, 0, None, None, None) == 1
+    # speculative acceptance: pointers, then K and V, are checked on the host before any launch
+    buf = (C.c_float * 16)()
+    ib = (C.c_int32 * 16)()
+    assert L.moe_spec_accept(None, buf, 1, 4, ib, buf, ib, None) == 1
+    assert L.moe_spec_accept(buf, None, 1, 4, ib, buf, ib, None) == 1       # q is needed when K > 0
+    assert L.moe_spec_accept(buf, buf, 9, 4, ib, buf, ib, None) == 2
+    assert L.moe_spec_accept(buf, buf, 1, 0, ib, buf, ib, None) == 2
+    assert L.moe_spec_accept(buf, buf, 1, (1 << 22) + 1, ib, buf, ib, None) == 2
+    monkeypatch.setenv("MOE_FAULT", "spec")
+    assert L.moe_spec_accept(buf, buf, 1, 4, ib, buf, ib, None) == 8
