@@ -27,6 +27,22 @@ H, I, E, K_TOP, NTOK = 4096, 2048, 256, 6, 1000
 FMT_IDS = {"mxfp4": 1, "int4g32": 2, "q2k": 3}
 
 
+def max_over_ranks(value: float, dist, device) -> float:
+    """The largest of the ranks' values (a timed region lasts as long as its slowest replica); `value` itself
+    with one process (dist None)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_token_seed(seed: int, rank: int) -> int:
+    """Seed of the tokens a replica decodes: every rank decodes tokens of its own."""
+    return seed + rank * 7919
+
+
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -160,7 +176,7 @@ def run_ours(args):
     setup_s = time.time() - t0
 
     wr = torch.from_numpy(router_f16_bits(args.seed, 0, E, H).view(np.int16)).to(dev)
-    x_host = x_bf16_bits(args.seed + rank * 7919, range(T), H)   # each rank decodes its own tokens
+    x_host = x_bf16_bits(rank_token_seed(args.seed, rank), range(T), H)   # each rank decodes its own tokens
     x = torch.from_numpy(x_host.view(np.int16)).to(dev)
     idx = torch.zeros((T, K_TOP), dtype=torch.int32, device=dev)
     w = torch.zeros((T, K_TOP), dtype=torch.float32, device=dev)
@@ -244,9 +260,7 @@ def run_ours(args):
     ms = ev0.elapsed_time(ev1)
     clk = clocks.stop()
     if dist:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+        ms = max_over_ranks(ms, dist, dev)
         dist.barrier()
     status = m.moe_get_device_status(ws, stream)
     if status != 0:
@@ -298,10 +312,7 @@ def run_ours(args):
     s1.record(stream)
     s1.synchronize()
     e2e_ms = s0.elapsed_time(s1) / e2e_steps
-    if dist:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
 
     prefill = bench_prefill(m, torch, args, dev, stream, layer_p, E) if do_prefill else None
     verify = bench_verify(m, torch, args, dev, stream, layer, wr, x_host, E, per_expert) if (use_tc and not args.no_verify) else None
