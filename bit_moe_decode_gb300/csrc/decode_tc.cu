@@ -5,9 +5,9 @@
 // tensor-core tile layout (8 KB per 128 x 128 tile in shared memory, no unpacking), and a few activation columns as
 // operand B: x (gate/up) and h (down) are each split into PARTS = 6 E2M1 parts per 32-block (split_parts_n: part p
 // has exponent e0 - 2p and quantises what the earlier parts left; error below 1/3072 of the block's largest value).
-// Column t * PARTS + p holds part p of token t; N = 48 for every call. A token's result is the sum of its part
-// columns in part order; the MMA computes every column independently, so a token's numbers do not depend on which
-// other tokens share the sweep (verify row t == decode of token t).
+// Column t * PARTS + p holds part p of token t; N = W = 16 ceil(6 T / 16) columns. A token's result is the sum of
+// its part columns in part order; the MMA computes every column on its own (whatever N is), so a token's numbers
+// do not depend on which other tokens share the sweep (verify row t == decode of token t).
 //
 // Work units (fixed for every T, so the arithmetic of a token never changes):
 //   G unit (expert u, 128-row tile rt of [Gate;Up], K segment ks): fp32 partial g/u of the tile's 64 gate and 64
@@ -18,14 +18,17 @@
 //     combines y[t] = sum_r w[t, r] * d_r in rank order.
 // Units are dealt round-robin to persistent CTAs (one per SM, cooperative launch), G units first (expert-major),
 // then D units; the grid is a multiple of the number of gate/up segments, so all G units of a CTA share one K
-// segment and the CTA keeps that segment's x parts resident in shared memory (computed at kernel start).
+// segment. x is split into its parts once per call by the epilogue warps of the whole grid (an operand image in
+// the workspace); each CTA then bulk-copies its segment's part tiles into shared memory and keeps them resident.
+// With a router (moe_route_expert_ffn), warps 2..7 of every CTA first compute halves of the router logits, and
+// every CTA then selects each token's experts itself (route.cuh, the same arithmetic as the standalone router).
 // Inside a CTA, three independent pipelines take the CTA's units as they free up. A pipeline is a weight-issuing
 // warp, an activation-issuing warp (h parts of D units, after their h is final), an MMA-issuing warp, a three-slot
-// shared-memory ring, two to four TMEM accumulators and a group of four epilogue warps. One issuing thread sustains only
-// about one wait-and-issue round per 330 ns (TMA) or one stage of MMAs plus commit per ~600 cycles (tcgen05),
-// while one SM must consume an 8.5 KB weight tile every ~180 ns to keep pace with HBM. Cross-CTA dependencies
-// (partials complete, h of an expert's K segment final) are global counters with bounded waits; the last CTA to
-// finish resets them.
+// shared-memory ring, two to four TMEM accumulators and a group of four epilogue warps. One issuing thread
+// sustains only about one wait-and-issue round per 330 ns (TMA) or one stage of MMAs plus commit per ~600 cycles
+// (tcgen05), while one SM must consume an 8.5 KB weight tile every ~180 ns to keep pace with HBM. Cross-CTA
+// dependencies (partials complete, h of an expert's K segment final) are global counters with bounded waits; the
+// last CTA to finish resets them.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <mutex>
