@@ -171,6 +171,7 @@ __device__ __forceinline__ float warp_amax(float v) {
 // 1/3072 of the block's largest magnitude. Only e0 needs a warp reduction. Even lanes get the packed byte of
 // elements (l, l + 1) of each part in bytes[p] (element l in the low nibble). A block holding NaN or infinity has
 // no E2M1 encoding: every part gets the E8M0 NaN exponent (255), which the block-scaled MMA turns into NaN.
+// live[q] must be the same for every lane of the warp (the parts of a dead block are skipped by all lanes).
 template <int NV>
 __device__ __forceinline__ void split_parts_n(const float (&v)[NV], const bool (&live)[NV], uint32_t (&bytes)[NV][PARTS],
                                               int (&exps)[NV][PARTS]) {
