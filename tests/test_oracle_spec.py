@@ -41,31 +41,31 @@ def _first_true(pred) -> float:
     return 1.0 if hi == ONE_BITS else _f32(hi)
 
 
-def _accept_prob(p, q, d):
+def _accept_prob(p, q, d, accept=oracle.spec_accept):
     """Measure of the acceptance uniforms (u in [0, 1)) that accept draft d (K = 1)."""
-    return _first_true(lambda ua: oracle.spec_accept(p, q, [d], [ua, 0.5])[0] == 0)
+    return _first_true(lambda ua: accept(p, q, [d], [ua, 0.5])[0] == 0)
 
 
-def _draw_law(p, q, draft, ua):
+def _draw_law(p, q, draft, ua, accept=oracle.spec_accept):
     """Law of the drawn token over its uniform: the draw is monotone in it, so each token's share is the
     distance between the uniforms where the token first reaches v and v + 1."""
     V = p.shape[1]
-    starts = [0.0] + [_first_true(lambda us: oracle.spec_accept(p, q, draft, list(ua) + [us])[1] >= v)
+    starts = [0.0] + [_first_true(lambda us: accept(p, q, draft, list(ua) + [us])[1] >= v)
                       for v in range(1, V)] + [1.0]
     return np.diff(np.array(starts))
 
 
-def _first_token_law(p, q):
+def _first_token_law(p, q, accept=oracle.spec_accept):
     """Law of the first committed token with K = 1 over the draft d ~ q and both uniforms."""
     V = p.shape[1]
     law = np.zeros(V)
     for d in range(V):
         if q[0, d] == 0:
             continue
-        pa = _accept_prob(p, q, d)
+        pa = _accept_prob(p, q, d, accept)
         law[d] += q[0, d] * pa
         if pa < 1.0:
-            law += q[0, d] * (1.0 - pa) * _draw_law(p, q, [d], [0.9999999])
+            law += q[0, d] * (1.0 - pa) * _draw_law(p, q, [d], [0.9999999], accept)
     return law
 
 
