@@ -40,49 +40,54 @@ def build(force: bool = False) -> str:
     return _LIB
 
 
+def bind(path: str) -> C.CDLL:
+    """Load a build of oracle.c and set the argument and result types of its functions."""
+    L = C.CDLL(path)
+    P = C.c_void_p
+    i64, i32, dbl = C.c_int64, C.c_int, C.c_double
+    sig = {
+        "orc_f16_to_f64": (dbl, [C.c_uint16]),
+        "orc_bf16_to_f64": (dbl, [C.c_uint16]),
+        "orc_round_f32": (dbl, [dbl]),
+        "orc_round_f16": (dbl, [dbl]),
+        "orc_round_bf16": (dbl, [dbl]),
+        "orc_f32_to_f16_rne": (C.c_uint16, [C.c_float]),
+        "orc_e2m1_value": (dbl, [i32]),
+        "orc_e8m0_scale": (dbl, [i32]),
+        "orc_e4m3_value": (dbl, [i32]),
+        "orc_decode_mxfp4": (None, [P, i64, P]),
+        "orc_decode_int4": (None, [P, i64, P]),
+        "orc_decode_q2k": (None, [P, i64, P]),
+        "orc_encode_mxfp4": (None, [P, i64, P]),
+        "orc_encode_int4": (None, [P, i64, P]),
+        "orc_encode_q2k": (None, [P, i64, P]),
+        "orc_quant_mxfp8": (None, [P, i64, P, P]),
+        "orc_mxfp4_half_lut": (None, [P]),
+        "orc_router_logits": (None, [P, P, i32, i32, i32, P, P]),
+        "orc_topk_from_logits": (None, [P, i32, i32, i32, P, P]),
+        "orc_route_topk": (None, [P, P, i32, i32, i32, i32, P, P, P, P]),
+        "orc_route_hash": (None, [P, P, i32, i32, P, P]),
+        "orc_weight_at": (dbl, [i32, P, i32, i64, i32]),
+        "orc_expert_ffn": (None, [i32, i32, i32, P, P, P, P, P, P, P, P, P]),
+        "orc_moe_token": (None, [i32, i32, i32, i32, P, P, P, P, P, P, P]),
+        "orc_moe_batch": (None, [i32, i32, i32, i32, i32, P, P, P, i32, P, P, P, P, P, i32]),
+        "orc_prefill_token": (None, [i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P, P]),
+        "orc_max_threads": (i32, []),
+        "orc_spec_accept": (None, [P, P, i32, i32, P, P, P]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    return L
+
+
 def lib():
     global _lib
     with _lock:
         if _lib is None:
             build()
-            L = C.CDLL(_LIB)
-            P = C.c_void_p
-            i64, i32, dbl = C.c_int64, C.c_int, C.c_double
-            sig = {
-                "orc_f16_to_f64": (dbl, [C.c_uint16]),
-                "orc_bf16_to_f64": (dbl, [C.c_uint16]),
-                "orc_round_f32": (dbl, [dbl]),
-                "orc_round_f16": (dbl, [dbl]),
-                "orc_round_bf16": (dbl, [dbl]),
-                "orc_f32_to_f16_rne": (C.c_uint16, [C.c_float]),
-                "orc_e2m1_value": (dbl, [i32]),
-                "orc_e8m0_scale": (dbl, [i32]),
-                "orc_e4m3_value": (dbl, [i32]),
-                "orc_decode_mxfp4": (None, [P, i64, P]),
-                "orc_decode_int4": (None, [P, i64, P]),
-                "orc_decode_q2k": (None, [P, i64, P]),
-                "orc_encode_mxfp4": (None, [P, i64, P]),
-                "orc_encode_int4": (None, [P, i64, P]),
-                "orc_encode_q2k": (None, [P, i64, P]),
-                "orc_quant_mxfp8": (None, [P, i64, P, P]),
-                "orc_mxfp4_half_lut": (None, [P]),
-                "orc_router_logits": (None, [P, P, i32, i32, i32, P, P]),
-                "orc_topk_from_logits": (None, [P, i32, i32, i32, P, P]),
-                "orc_route_topk": (None, [P, P, i32, i32, i32, i32, P, P, P, P]),
-                "orc_route_hash": (None, [P, P, i32, i32, P, P]),
-                "orc_weight_at": (dbl, [i32, P, i32, i64, i32]),
-                "orc_expert_ffn": (None, [i32, i32, i32, P, P, P, P, P, P, P, P, P]),
-                "orc_moe_token": (None, [i32, i32, i32, i32, P, P, P, P, P, P, P]),
-                "orc_moe_batch": (None, [i32, i32, i32, i32, i32, P, P, P, i32, P, P, P, P, P, i32]),
-                "orc_prefill_token": (None, [i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P, P]),
-                "orc_max_threads": (i32, []),
-                "orc_spec_accept": (None, [P, P, i32, i32, P, P, P]),
-            }
-            for name, (res, args) in sig.items():
-                f = getattr(L, name)
-                f.restype = res
-                f.argtypes = args
-            _lib = L
+            _lib = bind(_LIB)
     return _lib
 
 

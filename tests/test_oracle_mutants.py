@@ -1,0 +1,63 @@
+"""The oracle's pins catch plausible mistakes: each test plants one mistake in a copy of oracle.c (on the CPU, in a
+temporary directory), binds the copy in place of the oracle and checks that at least one of the named pins of
+tests/test_oracle_formats.py and tests/test_oracle_router_ffn.py fails on it. The unmodified oracle passes them all
+(those files' own runs)."""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import tests.test_oracle_formats as tf
+import tests.test_oracle_router_ffn as tr
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+# name: (text in oracle.c, the planted mistake, pins of which at least one must fail)
+MUTANTS = {
+    "mxfp4_nibble_order": ("return (j % 2 == 0) ? (b >> 4) : (b & 15);",
+                           "return (j % 2 == 0) ? (b & 15) : (b >> 4);",
+                           [tf.test_mxfp4_element_order_follows_printed_unpack, tf.test_mxfp4_handbuilt_blocks]),
+    "e8m0_bias": ("return ldexp(1.0, e - 127);", "return ldexp(1.0, e - 126);",
+                  [tf.test_e8m0_rule, tf.test_mxfp4_handbuilt_blocks]),
+    "int4_sign": ("return n >= 8 ? n - 16 : n;   /* two's complement */", "return n;",
+                  [tf.test_int4_layout_and_decode_closed_form]),
+    "q2k_min_sign": ("  return bq - c;\n}", "  return bq + c;\n}",
+                     [tf.test_q2k_handbuilt_block, tf.test_q2k_decode_matches_closed_form_random_blocks]),
+    "router_ties_to_upper": ("if (best < 0 || l[e] > l[best]) best = e;", "if (best < 0 || l[e] >= l[best]) best = e;",
+                             [tr.test_router_ties_go_to_lower_index]),
+    "router_weights_unnormalised": ("for (int r = 0; r < k; ++r) den += exp(sel[r] - mx);",
+                                    "for (int r = 0; r < k; ++r) den = 1.0;",
+                                    [tr.test_router_matches_sort_and_scipy_softmax]),
+    "silu_as_sigmoid": ("static double silu(double g) { return g / (1.0 + exp(-g)); }",
+                        "static double silu(double g) { return 1.0 / (1.0 + exp(-g)); }",
+                        [tr.test_ffn_integer_case_is_exact, lambda: tr.test_ffn_random_matches_numpy_path(oracle.MXFP4)]),
+    "combine_weight_dropped": ("      y[j] += (double)w[r] * d[j];\n      if (absterm) absterm[j] += fabs((double)w[r]) * da[j];",
+                               "      y[j] += d[j];\n      if (absterm) absterm[j] += fabs((double)w[r]) * da[j];",
+                               [lambda: tr.test_moe_combine_batch_and_token_agree_with_numpy(oracle.MXFP4)]),
+}
+
+
+def _bind_mutant(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) >= 1, name  # every occurrence gets the mistake (the combine appears in two functions)
+    path = tmp_path / (name + ".c")
+    path.write_text(src.replace(old, new))
+    so = tmp_path / ("lib" + name + ".so")
+    subprocess.run(["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+                    str(path), "-o", str(so), "-lm"], check=True)
+    return oracle.bind(str(so))
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_fails_a_pin(tmp_path, monkeypatch, name):
+    old, new, pins = MUTANTS[name]
+    oracle.lib()  # the real oracle is built and bound first; the mutant replaces it for this test only
+    monkeypatch.setattr(oracle, "_lib", _bind_mutant(tmp_path, name, old, new))
+    failed = 0
+    for pin in pins:
+        try:
+            pin()
+        except AssertionError:
+            failed += 1
+    assert failed > 0, "no pin caught the planted mistake %s" % name
