@@ -330,6 +330,25 @@ def test_e4m3_values_and_quantiser_vs_torch():
         assert np.array_equal(codes[b], ref), b
 
 
+def test_mxfp8_quantiser_ties_go_to_even_codes_vs_torch():
+    # values exactly halfway between neighbouring E4M3 values (normal and subnormal), in blocks whose largest
+    # value is 448 so that the scale is 2^0 and the quantiser sees them unscaled; torch's float8_e4m3fn
+    # conversion rounds them to the even code
+    pos = torch.arange(0, 127, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()   # 0 .. 448
+    mids = (pos[:-1] + pos[1:]) / 2.0
+    vals = np.concatenate([mids, -mids])
+    nb = (len(vals) + 30) // 31
+    blocks = np.zeros((nb, 32))
+    blocks[:, 0] = 448.0
+    flat = np.zeros(nb * 31)
+    flat[:len(vals)] = vals
+    blocks[:, 1:] = flat.reshape(nb, 31)
+    codes, scales = oracle.quant_mxfp8(blocks)
+    assert np.all(scales[:, 0] == 127)
+    ref = torch.from_numpy(blocks).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(codes, ref)
+
+
 # ---------------------------------------------------------------- the half LUT of the Metal section
 def test_mxfp4_half_lut_properties():
     lut = oracle.mxfp4_half_lut()

@@ -35,6 +35,14 @@ MUTANTS = {
     "combine_weight_dropped": ("      y[j] += (double)w[r] * d[j];\n      if (absterm) absterm[j] += fabs((double)w[r]) * da[j];",
                                "      y[j] += d[j];\n      if (absterm) absterm[j] += fabs((double)w[r]) * da[j];",
                                [lambda: tr.test_moe_combine_batch_and_token_agree_with_numpy(oracle.MXFP4)]),
+    "e2m1_ties_to_odd": ("if (d < bestd || (d == bestd && (c % 2) == 0)) { bestd = d; best = c; }\n  }\n  if (a > 6.0) best = 7;",
+                         "if (d < bestd || (d == bestd && (c % 2) == 1)) { bestd = d; best = c; }\n  }\n  if (a > 6.0) best = 7;",
+                         [tf.test_mxfp4_encoder_ties_and_roundtrip, tf.test_mxfp4_encoder_brute_force_small]),
+    "mx_scale_one_too_small": ("  int e = k + 127;\n", "  int e = k + 126;\n",
+                               [tf.test_mxfp4_encoder_brute_force_small, tf.test_mxfp4_encoder_ties_and_roundtrip]),
+    "e4m3_ties_to_odd": ("    double d = fabs(a - orc_e4m3_value(c));\n    if (d < bestd || (d == bestd && (c % 2) == 0))",
+                         "    double d = fabs(a - orc_e4m3_value(c));\n    if (d < bestd || (d == bestd && (c % 2) == 1))",
+                         [tf.test_e4m3_values_and_quantiser_vs_torch, tf.test_mxfp8_quantiser_ties_go_to_even_codes_vs_torch]),
 }
 
 
