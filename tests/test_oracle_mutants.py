@@ -43,6 +43,20 @@ MUTANTS = {
     "e4m3_ties_to_odd": ("    double d = fabs(a - orc_e4m3_value(c));\n    if (d < bestd || (d == bestd && (c % 2) == 0))",
                          "    double d = fabs(a - orc_e4m3_value(c));\n    if (d < bestd || (d == bestd && (c % 2) == 1))",
                          [tf.test_e4m3_values_and_quantiser_vs_torch, tf.test_mxfp8_quantiser_ties_go_to_even_codes_vs_torch]),
+    "int4_grid_without_1": ("const float grid[6] = {6.0f / 7.0f, 0.9f, 0.95f, 1.0f, 1.05f, 1.1f};",
+                            "const float grid[6] = {6.0f / 7.0f, 0.9f, 0.95f, 1.05f, 1.05f, 1.1f};",
+                            [tf.test_int4_encoder_is_grid_argmin]),
+    "int4_clamp_at_minus_7": ("if (qq < -8.0f) qq = -8.0f;", "if (qq < -7.0f) qq = -7.0f;",
+                              [tf.test_int4_encoder_is_grid_argmin]),
+    "router_drops_last_term": ("      for (int h = 0; h < H; ++h) {\n        double p = orc_f16_to_f64(wr",
+                               "      for (int h = 0; h < H - 1; ++h) {\n        double p = orc_f16_to_f64(wr",
+                               [tr.test_router_matches_sort_and_scipy_softmax]),
+    "hash_weight": ("w[(int64_t)t * k + r] = (float)(1.0 / k);", "w[(int64_t)t * k + r] = (float)(1.0 / (k + 1));",
+                    [tr.test_hash_routing_gathers_table_with_equal_weights]),
+    "gate_up_swapped": ("    h[i] = silu(gv[i]) * s;", "    h[i] = silu(s) * gv[i];",
+                        [tr.test_ffn_integer_case_is_exact, lambda: tr.test_ffn_random_matches_numpy_path(oracle.MXFP4)]),
+    "down_transposed": ("      double p = D[(int64_t)j * I + i] * h[i];", "      double p = D[(int64_t)i * H + j % H] * h[i];",
+                        [lambda: tr.test_ffn_random_matches_numpy_path(oracle.MXFP4)]),
 }
 
 
