@@ -57,6 +57,12 @@ MUTANTS = {
                         [tr.test_ffn_integer_case_is_exact, lambda: tr.test_ffn_random_matches_numpy_path(oracle.MXFP4)]),
     "down_transposed": ("      double p = D[(int64_t)j * I + i] * h[i];", "      double p = D[(int64_t)i * H + j % H] * h[i];",
                         [lambda: tr.test_ffn_random_matches_numpy_path(oracle.MXFP4)]),
+    "prefill_h_unquantised": ("        double p = weight_at(1, down[r], I, j, i) * hq[i];",
+                              "        double p = weight_at(1, down[r], I, j, i) * h[i];",
+                              [tr.test_prefill_token_matches_torch_float8_path]),
+    "prefill_x_unquantised": ("    orc_expert_ffn(1, H, I, gate[r], up[r], down[r], xq, NULL, NULL, h, NULL, NULL);",
+                              "    orc_expert_ffn(1, H, I, gate[r], up[r], down[r], x, NULL, NULL, h, NULL, NULL);",
+                              [tr.test_prefill_token_matches_torch_float8_path]),
 }
 
 
