@@ -12,6 +12,8 @@
  *   - Verify of width 1+K: "Mixed-precision compression...", "What compression does not solve" and "Width drift":
  *     several tokens share one sweep of the expert weights, and row t of a wide verify must equal the width-1
  *     decode of token t bit for bit ("Why this is not a host-side patch").
+ *   - Speculative acceptance of drafted tokens: "Mixed-precision compression...", "What compression does not
+ *     solve" (keep a draft with probability min(1, p/q); on a rejection draw from the normalised max(p - q, 0)).
  *   - Weight formats: "quantization" glossary, sections "MXFP4" (17-byte blocks: one E8M0 exponent, 32 E2M1
  *     codes; e = 0 is zero) and "core principle" (Q2_K, 84 bytes per 256 weights); INT4 group 32 with a BF16
  *     scale: "DeepSeek-V4-Flash-0731-W4A16" model card (alphaneural.io), quantisation scheme.
@@ -23,7 +25,10 @@
  *     nothing is launched then. MOE_ERR_CUDA reports a failed launch (cudaGetLastError).
  *   - Device-side errors (a bounded wait that ran out) are written to a status word inside the caller's
  *     workspace; read it with moe_get_device_status(). After such an error call moe_workspace_init() again.
- *   - The library keeps no mutable global state except a per-process cache of device properties.
+ *   - The library keeps no mutable global state except a per-process cache of device properties, the one-time
+ *     kernel attribute settings (shared-memory sizes: once per process for the decode and prefill kernels, once
+ *     per device for the others; one process drives one GPU) and the static scratch of
+ *     moe_expert_ffn_decode_static.
  *   - Host-side fault injection for tests: if the environment variable MOE_FAULT names a call
  *     ("pack", "route", "decode", "verify", "prefill", "encode", "spec"), that call returns MOE_ERR_FAULT_INJECTED
  *     without launching anything.
