@@ -53,7 +53,7 @@ def parse():
     p.add_argument("--tokens", type=int, default=NTOK)
     p.add_argument("--seed", type=int, default=1)
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--no-verify", action="store_true", help="skip the verify-cost measurements")
+    p.add_argument("--no-verify", action="store_true", help="skip the verify-cost and speculative-acceptance measurements")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--experts", type=int, default=E, help="expert slots of the layer (smaller only for profiling)")
     p.add_argument("--layout", default="auto", choices=["auto", "tc", "decode"],
