@@ -30,7 +30,8 @@
  *     per device for the others; one process drives one GPU) and the static scratch of
  *     moe_expert_ffn_decode_static.
  *   - Host-side fault injection for tests: if the environment variable MOE_FAULT names a call
- *     ("pack", "route", "decode", "verify", "prefill", "encode", "spec"), that call returns MOE_ERR_FAULT_INJECTED
+ *     ("pack", "route", "decode", "verify", "route_ffn", "prefill", "encode", "spec"), that call returns
+ *     MOE_ERR_FAULT_INJECTED
  *     without launching anything.
  */
 #ifndef BIT_MOE_DECODE_GB300_MOE_H

@@ -92,3 +92,44 @@ def test_fault_injection_and_argument_checks(m, monkeypatch):
     assert L.moe_spec_accept(buf, buf, 1, (1 << 22) + 1, ib, buf, ib, None) == 2
     monkeypatch.setenv("MOE_FAULT", "spec")
     assert L.moe_spec_accept(buf, buf, 1, 4, ib, buf, ib, None) == 8
+
+
+def _aligned(nbytes: int, align: int):
+    """A host buffer and an address inside it aligned to `align` (only for checks that precede any launch)."""
+    buf = (C.c_uint8 * (nbytes + align))()
+    addr = C.addressof(buf)
+    return buf, addr + (-addr) % align
+
+
+def test_ffn_and_fused_call_argument_checks(m):
+    """Every argument error of the decode / verify / fused calls is found on the host, before the device check, so
+    these run without a GPU."""
+    L = m.lib()
+    keep = []
+    def ptr(n=1 << 12, align=256):
+        b, a = _aligned(n, align)
+        keep.append(b)
+        return C.c_void_p(a)
+    gu, dn, x, ws, y, idx, w, wr = (ptr() for _ in range(8))
+    def layer(fmt=1, layout=1, H=4096, I=2048, E=256, g=gu, d=dn):
+        return m.moe_layer_t(fmt, layout, H, I, E, g, d)
+    lay = layer()
+    ver = L.moe_expert_ffn_verify
+    # verify: null pointers, bad format / layout, sizes
+    assert ver(C.byref(lay), None, 1, idx, w, 6, y, None, 0, ws, 1 << 20, None) == 1
+    assert ver(C.byref(layer(fmt=4)), x, 1, idx, w, 6, y, None, 0, ws, 1 << 20, None) == 3
+    assert ver(C.byref(layer(layout=5)), x, 1, idx, w, 6, y, None, 0, ws, 1 << 20, None) == 3
+    assert ver(C.byref(lay), x, 9, idx, w, 6, y, None, 0, ws, 1 << 20, None) == 2
+    assert ver(C.byref(lay), x, 0, idx, w, 6, y, None, 0, ws, 1 << 20, None) == 2
+    assert ver(C.byref(lay), x, 1, idx, w, 9, y, None, 0, ws, 1 << 20, None) == 2
+    assert ver(C.byref(layer(H=4096 + 64)), x, 1, idx, w, 6, y, None, 0, ws, 1 << 20, None) == 2
+    assert ver(C.byref(layer(fmt=2)), x, 1, idx, w, 6, y, None, 0, ws, 1 << 20, None) == 3   # INT4 has no TC layout
+    assert ver(C.byref(lay), x, 1, idx, w, 6, y, None, 0, C.c_void_p(ws.value + 8), 1 << 20, None) == 1  # ws alignment
+    # fused router + FFN: MXFP4 in the tensor-core layout, E <= 256, 16-byte aligned router and x
+    fused = L.moe_route_expert_ffn
+    assert fused(C.byref(lay), None, x, 1, 6, idx, w, y, None, 0, ws, 1 << 20, None) == 1
+    assert fused(C.byref(layer(layout=0)), wr, x, 1, 6, idx, w, y, None, 0, ws, 1 << 20, None) == 3
+    assert fused(C.byref(layer(E=300)), wr, x, 1, 6, idx, w, y, None, 0, ws, 1 << 20, None) == 2
+    assert fused(C.byref(layer(E=4)), wr, x, 1, 6, idx, w, y, None, 0, ws, 1 << 20, None) == 2          # E < k
+    assert fused(C.byref(lay), wr, C.c_void_p(x.value + 4), 1, 6, idx, w, y, None, 0, ws, 1 << 20, None) == 1
+    assert fused(C.byref(lay), wr, x, 9, 6, idx, w, y, None, 0, ws, 1 << 20, None) == 2
