@@ -133,3 +133,28 @@ def test_ffn_and_fused_call_argument_checks(m):
     assert fused(C.byref(layer(E=4)), wr, x, 1, 6, idx, w, y, None, 0, ws, 1 << 20, None) == 2          # E < k
     assert fused(C.byref(lay), wr, C.c_void_p(x.value + 4), 1, 6, idx, w, y, None, 0, ws, 1 << 20, None) == 1
     assert fused(C.byref(lay), wr, x, 9, 6, idx, w, y, None, 0, ws, 1 << 20, None) == 2
+
+
+def test_prefill_argument_checks(m):
+    """The prefill call's argument and size errors, found on the host before the device check."""
+    L = m.lib()
+    keep = []
+    def ptr(n=1 << 12, align=256):
+        b, a = _aligned(n, align)
+        keep.append(b)
+        return C.c_void_p(a)
+    gu, dn, x, ws, y, idx, w = (ptr() for _ in range(7))
+    def layer(fmt=1, layout=1, H=4096, I=2048, E=256):
+        return m.moe_layer_t(fmt, layout, H, I, E, gu, dn)
+    pre = L.moe_expert_grouped_gemm_prefill
+    lay = layer()
+    assert pre(C.byref(lay), None, 16, idx, w, 6, y, None, ws, 1 << 20, None) == 1
+    assert pre(C.byref(lay), x, 16, idx, w, 6, None, None, ws, 1 << 20, None) == 1      # neither y nor y_bf16
+    assert pre(C.byref(layer(fmt=3)), x, 16, idx, w, 6, y, None, ws, 1 << 20, None) == 3
+    assert pre(C.byref(layer(layout=0)), x, 16, idx, w, 6, y, None, ws, 1 << 20, None) == 3
+    assert pre(C.byref(layer(H=4096 + 64)), x, 16, idx, w, 6, y, None, ws, 1 << 20, None) == 2
+    assert pre(C.byref(lay), x, 0, idx, w, 6, y, None, ws, 1 << 20, None) == 2
+    assert pre(C.byref(lay), x, 16, idx, w, 9, y, None, ws, 1 << 20, None) == 2
+    assert pre(C.byref(layer(E=4)), x, 16, idx, w, 6, y, None, ws, 1 << 20, None) == 2     # k > E
+    assert pre(C.byref(lay), C.c_void_p(x.value + 4), 16, idx, w, 6, y, None, ws, 1 << 20, None) == 1
+    assert pre(C.byref(lay), x, 16, idx, w, 6, y, None, ws, 16, None) == 5                # workspace too small
