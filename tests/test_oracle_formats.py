@@ -350,6 +350,15 @@ def test_mxfp8_quantiser_ties_go_to_even_codes_vs_torch():
 
 
 # ---------------------------------------------------------------- the half LUT of the Metal section
+def test_mxfp4_half_lut_hash_has_not_drifted():
+    # the generated 4096-entry table is pinned by its SHA-256, written by tests/golden/make_lut_hash.py from the
+    # oracle when the table was checked entry by entry (test_mxfp4_half_lut_properties)
+    import hashlib
+    lut = oracle.mxfp4_half_lut()
+    want = open(os.path.join(GOLD, "mxfp4_half_lut.sha256")).read().split()[0]
+    assert hashlib.sha256(lut.astype("<u2").tobytes()).hexdigest() == want
+
+
 def test_mxfp4_half_lut_properties():
     lut = oracle.mxfp4_half_lut()
     assert lut.shape == (256, 16) and lut.size == 4096
