@@ -63,6 +63,11 @@ MUTANTS = {
     "prefill_x_unquantised": ("    orc_expert_ffn(1, H, I, gate[r], up[r], down[r], xq, NULL, NULL, h, NULL, NULL);",
                               "    orc_expert_ffn(1, H, I, gate[r], up[r], down[r], x, NULL, NULL, h, NULL, NULL);",
                               [tr.test_prefill_token_matches_torch_float8_path]),
+    "q2k_codes_floored": ("        float qq = rne_int(t / step);\n        if (qq < 0.0f) qq = 0.0f;\n        if (qq > 3.0f) qq = 3.0f;",
+                          "        float qq = floorf(t / step);\n        if (qq < 0.0f) qq = 0.0f;\n        if (qq > 3.0f) qq = 3.0f;",
+                          [tf.test_q2k_size_and_encoder_bounds]),
+    "q2k_offset_dropped": ("        float t = x[i] + off;", "        float t = x[i];",
+                           [tf.test_q2k_size_and_encoder_bounds]),
 }
 
 
