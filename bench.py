@@ -71,6 +71,21 @@ def measured_peaks():
         return None
 
 
+def peak_of(peaks, key: str):
+    """One measured peak from MEASURED_PEAKS.json: a positive number stored under `key` directly or as
+    {"value": number}; None when the file, the key or a usable number is missing (the caller then falls back)."""
+    if not isinstance(peaks, dict):
+        return None
+    v = peaks.get(key)
+    if isinstance(v, dict):
+        v = v.get("value")
+    try:
+        v = float(v)
+    except (TypeError, ValueError):
+        return None
+    return v if v > 0 else None
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms while the timed region runs."""
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
@@ -320,8 +335,8 @@ def run_ours(args):
 
     out = None
     if rank == 0:
-        peaks = measured_peaks()
-        peak = float(peaks["hbm_gbs"]) if peaks else 6800.0
+        hbm_measured = peak_of(measured_peaks(), "hbm_gbs")
+        peak = hbm_measured or 6800.0
         achieved = alg_bytes / (ffn_us * 1e-6) / 1e9
         ms_step = ms / args.steps
         value = world * T / (ms_step * 1e-3)
@@ -353,7 +368,7 @@ def run_ours(args):
                          "traffic": TC_TRAFFIC if use_tc else None,
                          "kernel": "decode_kernel (tcgen05)" if use_tc else "ffn_kernel<%s>" % args.fmt,
                          "bytes_per_launch": alg_bytes,
-                         "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if peaks else "fallback"},
+                         "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if hbm_measured else "fallback"},
             "e2e": {"value": round(world * T / (e2e_ms * 1e-3), 1), "unit": "tok/s",
                     "h2d_bytes_per_step": int(T * H * 2), "d2h_bytes_per_step": int(T * H * 4)},
             "clocks": clk,
@@ -502,9 +517,9 @@ def bench_prefill(m, torch, args, dev, stream, layer_p, E):
     flops = pairs * 3 * 2.0 * H * I
     wbytes = int(np.count_nonzero(counts)) * (m.moe_packed_bytes(1, 1, 0, 1, H, I) + m.moe_packed_bytes(1, 1, 1, 1, H, I))
     peaks = measured_peaks()
-    bf16 = float(peaks["bf16_tflops"]) if peaks and "bf16_tflops" in peaks else None
+    bf16 = peak_of(peaks, "bf16_tflops")
     peak = 2.0 * bf16 if bf16 else 3800.0
-    hbm = float(peaks["hbm_gbs"]) if peaks else 6800.0
+    hbm = peak_of(peaks, "hbm_gbs") or 6800.0
     tflops = flops / (ms * 1e-3) / 1e12
     return {"workload": "prefill of %d tokens, top-6, Zipf(1.1) expert popularity over %d experts (%d pairs, "
                         "%d tiles of 128)" % (Tp, E, pairs, int(np.sum((counts + 127) // 128))),
