@@ -16,7 +16,7 @@
  *        E2M1 table, E8M0 = 2^(e-127) with e=0 as zero, Q2_K super-block (84 bytes: scales[16], qs[64],
  *        fp16 d, fp16 dmin), the "Metal MXFP4 -> half LUT" section (4096 exact products rounded once).
  *
- * Readings where the pages are silent or garbled (also listed in the design doc):
+ * Readings where the pages are silent or garbled:
  *   - MXFP4 nibble order: element 2j is the HIGH nibble of code byte j, element 2j+1 the LOW nibble
  *     (the only printed unpack, P4 step 1 "dequant_fp4", takes byte>>4 first).
  *   - E8M0: e=0 -> 0 (P5 comment "e=0 treated as zero"), e=255 -> NaN (P5 LUT section: the 0xff row
