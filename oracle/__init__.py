@@ -289,7 +289,8 @@ def prefill_token(H: int, I: int, gate_of, up_of, down_of, idx_t, w_t, x_t_bf16)
 
 # ---------------------------------------------------------------- speculative acceptance
 def spec_accept(p: np.ndarray, q: np.ndarray, draft, u) -> tuple[int, int]:
-    """The chain of K drafted tokens under the acceptance rule of [P2] "What compression does not solve"
+    """The chain of K drafted tokens under the acceptance rule of "Mixed-precision compression of DeepSeek-V4-Flash"
+    (lumirain.cn), "What compression does not solve"
     (accept draft k with probability min(1, p_k(d)/q_k(d)); at the first rejection draw from max(p_k - q_k, 0)
     normalised; after K acceptances draw from p_K). p [K+1, V] fp32, q [K, V] fp32, draft [K] int32,
     u [K+1] fp32 (u[K] drives the draw). -> (accepted drafts n, drawn token); (-1, -1) for a draft id outside
