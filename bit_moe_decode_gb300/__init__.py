@@ -30,7 +30,8 @@ BLOCK = {MOE_FMT_MXFP4: (32, 17), MOE_FMT_INT4G32: (32, 18), MOE_FMT_Q2K: (256, 
 EXPORTS = ["moe_status_string", "moe_version", "moe_check_device", "moe_canonical_bytes", "moe_packed_bytes",
            "moe_encode_blocks", "moe_pack_weights", "moe_route_topk", "moe_workspace_bytes", "moe_workspace_init",
            "moe_get_device_status", "moe_expert_ffn_decode", "moe_expert_ffn_verify", "moe_route_expert_ffn",
-           "moe_debug_unpack", "moe_debug_timeout_probe", "moe_expert_ffn_decode_static", "moe_prefill_workspace_bytes",
+           "moe_debug_unpack", "moe_debug_timeout_probe", "moe_expert_ffn_decode_static", "moe_static_device_status",
+           "moe_prefill_workspace_bytes",
            "moe_expert_grouped_gemm_prefill", "moe_debug_prefill", "moe_spec_accept"]
 
 
@@ -76,6 +77,7 @@ def lib() -> C.CDLL:
             "moe_debug_unpack": (C.c_int, [C.c_int, C.c_int, C.c_int, P, i64, i64, i64, P, P]),
             "moe_debug_timeout_probe": (C.c_int, [P, sz, i32, P]),
             "moe_expert_ffn_decode_static": (C.c_int, [LP, P, P, P, i32, P, P, i32, P]),
+            "moe_static_device_status": (C.c_int, [P]),
             "moe_prefill_workspace_bytes": (sz, [LP, i32, i32]),
             "moe_expert_grouped_gemm_prefill": (C.c_int, [LP, P, i32, P, P, i32, P, P, P, sz, P]),
             "moe_debug_prefill": (C.c_int, [LP, P, i32, P, P, i32, P, P, P, sz, P, P, P]),
@@ -192,6 +194,11 @@ def moe_expert_ffn_decode_static(layer: "Layer", x_bf16, idx, w, k: int, y, y_bf
     _check(lib().moe_expert_ffn_decode_static(C.byref(layer.c), _ptr(x_bf16), _ptr(idx), _ptr(w), k, _ptr(y),
                                               _ptr(y_bf16), int(accumulate), _stream(stream)),
            "moe_expert_ffn_decode_static")
+
+
+def moe_static_device_status(stream=None) -> int:
+    """Device status word of the last moe_expert_ffn_decode_static call on the current device (syncs `stream`)."""
+    return lib().moe_static_device_status(_stream(stream))
 
 
 def moe_prefill_workspace_bytes(layer: "Layer", T_max: int, k: int) -> int:

@@ -655,7 +655,7 @@ static moe_status_t launch_ffn(const FfnArgs& a, cudaStream_t s) {
 static moe_status_t ffn_common(const char* site, const moe_layer_t* L, const void* x, int32_t T, const int32_t* idx,
                                const float* w, int32_t k, float* y, void* y_bf16, int32_t accumulate, void* ws,
                                size_t ws_bytes, void* stream) {
-  if (moe_internal::fault(site)) return MOE_ERR_FAULT_INJECTED;
+  if (site && moe_internal::fault(site)) return MOE_ERR_FAULT_INJECTED;
   if (!L || !x || !idx || !w || !y || !ws) return MOE_ERR_INVALID_ARG;
   if (L->fmt < MOE_FMT_MXFP4 || L->fmt > MOE_FMT_Q2K) return MOE_ERR_UNSUPPORTED_FORMAT;
   if (L->layout != MOE_LAYOUT_DECODE && L->layout != MOE_LAYOUT_TC) return MOE_ERR_UNSUPPORTED_FORMAT;
@@ -746,7 +746,24 @@ namespace {
 constexpr size_t kStaticScratchBytes = kWsCounters + (size_t)kMaxK * kMaxT * 4096 * 4 + (size_t)kMaxK * 4096 * kMaxT * 4;
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 std::mutex g_static_mu;
-void* g_static_ptr[64];  // device address of g_static_scratch, per device, looked up once
+// Device address of g_static_scratch, per device ordinal, looked up by the first call on that device (with the
+// device current). cudaDeviceReset() unloads the module, so the cached address is stale after it: a process that
+// resets a device must not call moe_expert_ffn_decode_static() on that device again.
+void* g_static_ptr[64];
+
+moe_status_t static_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    // host code only sees a stand-in for the symbol; the kernel needs its device address
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+    g_static_ptr[dev] = p;
+  }
+  *out = g_static_ptr[dev];
+  return MOE_OK;
+}
 }  // namespace
 
 extern "C" moe_status_t moe_expert_ffn_decode_static(const moe_layer_t* L, const void* x_bf16, const int32_t* idx,
@@ -759,20 +776,23 @@ extern "C" moe_status_t moe_expert_ffn_decode_static(const moe_layer_t* L, const
   if (ws_needed(L, 1, k) > kStaticScratchBytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
   moe_status_t st = moe_check_device();
   if (st != MOE_OK) return st;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
   void* scratch = nullptr;
-  {
-    std::lock_guard<std::mutex> lk(g_static_mu);
-    if (!g_static_ptr[dev]) {
-      // host code only sees a stand-in for the symbol; the kernel needs its device address
-      void* p = nullptr;
-      if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
-      g_static_ptr[dev] = p;
-    }
-    scratch = g_static_ptr[dev];
-  }
+  st = static_scratch(&scratch);
+  if (st != MOE_OK) return st;
   // every call shares the array: clear the counters and status word the kernel expects to start at zero
   if (cudaMemsetAsync(scratch, 0, kWsCounters, (cudaStream_t)stream) != cudaSuccess) return MOE_ERR_CUDA;
-  return ffn_common("decode", L, x_bf16, 1, idx, w, k, y, y_bf16, accumulate, scratch, kStaticScratchBytes, stream);
+  return ffn_common(nullptr, L, x_bf16, 1, idx, w, k, y, y_bf16, accumulate, scratch, kStaticScratchBytes, stream);
+}
+
+// Device status word of the most recent moe_expert_ffn_decode_static() call on the current device (the first word of
+// the static scratch): synchronises `stream`, then copies it out. The next static call clears it.
+extern "C" moe_status_t moe_static_device_status(void* stream) {
+  moe_status_t st = moe_check_device();
+  if (st != MOE_OK) return st;
+  int32_t v = 0;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemcpyFromSymbolAsync(&v, g_static_scratch, sizeof(v), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  return (moe_status_t)v;
 }

@@ -186,15 +186,20 @@ moe_status_t moe_route_expert_ffn(const moe_layer_t* layer, const void* router_w
  * fixed array of 2,101,248 bytes inside the library (one per GPU that loads it, kept until the process exits).
  * The pages have no counterpart; it exists for callers that cannot allocate device memory (a plugin given only
  * its input and output buffers, code under a memory budget owned by another allocator).
- *   Limits: k <= 8 and H, I <= 4096 (MOE_ERR_WORKSPACE_TOO_SMALL / MOE_ERR_SHAPE otherwise). It calls no
- *   allocation routine. The first call on a device looks up the array's device address (cudaGetSymbolAddress)
- *   with that device current; make that first call before any stream capture.
+ *   Layout MOE_LAYOUT_DECODE, any format. Limits: k <= 8 and H, I <= 4096 (MOE_ERR_WORKSPACE_TOO_SMALL /
+ *   MOE_ERR_SHAPE otherwise). It calls no allocation routine. The first call on a device looks up the array's
+ *   device address (cudaGetSymbolAddress) with that device current and keeps it for the life of the process; make
+ *   that first call before any stream capture, and do not call it again on a device after cudaDeviceReset().
  *   Every call shares the array and clears its counters and status word first (an asynchronous memset on
- *   `stream`), so device-side errors of a call are not kept for later inspection. Calls that overlap on the GPU
- *   (other streams, other threads) race on the array and must be serialised by the caller. */
+ *   `stream`). Calls that overlap on the GPU (other streams, other threads) race on the array and must be
+ *   serialised by the caller. Its results are bit-identical to moe_expert_ffn_decode's with a workspace. */
 moe_status_t moe_expert_ffn_decode_static(const moe_layer_t* layer, const void* x_bf16, const int32_t* idx,
                                           const float* w, int32_t k, float* y, void* y_bf16, int32_t accumulate,
                                           void* stream);
+/* Device status word (MOE_OK, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_INVALID_ARG for an expert id >= E) left by the most
+ * recent moe_expert_ffn_decode_static() on the current device: synchronises `stream`, then reads it. The next
+ * static call clears it. No counterpart on the pages. */
+moe_status_t moe_static_device_status(void* stream);
 
 /* ---------------------------------------------------------------- speculative acceptance ------------------------ */
 
