@@ -53,6 +53,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* b, uint32_t byte
 __device__ __forceinline__ void mbar_arrive(uint64_t* b) {
   asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(b)) : "memory");
 }
+// `n` arrivals at once
+__device__ __forceinline__ void mbar_arrive_n(uint64_t* b, uint32_t n) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(b)), "r"(n)
+               : "memory");
+}
 // Arrive without release semantics: for a consumer handing back a buffer it only read through TMEM or that only
 // the async proxy touched. A default (release) arrive would first wait until every global store the thread has in
 // flight is performed, which under a saturated memory system costs about a microsecond.

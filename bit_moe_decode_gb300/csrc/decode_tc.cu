@@ -1,34 +1,44 @@
 // decode_tc.cu -- decode and verify (1..8 tokens) of MXFP4 experts in the tensor-core layout on tcgen05.
 //
-// The work is a mat-vec per expert, so the block-scaled MMA (kind::mxf4: E2M1 x E2M1, one UE8M0 exponent per 32,
-// K = 64 per instruction) runs with the weights as the 128-row operand A, read as PACKED codes straight from the
-// tensor-core tile layout (8 KB per 128 x 128 tile in shared memory, no unpacking), and a few activation columns as
-// operand B: x (gate/up) and h (down) are each split into PARTS = 6 E2M1 parts per 32-block (split_parts_n: part p
-// has exponent e0 - 2p and quantises what the earlier parts left; error below 1/3072 of the block's largest value).
-// Column t * PARTS + p holds part p of token t; N = W = 16 ceil(6 T / 16) columns. A token's result is the sum of
-// its part columns in part order; the MMA computes every column on its own (whatever N is), so a token's numbers
-// do not depend on which other tokens share the sweep (verify row t == decode of token t).
+// What it computes: y_t = sum_r w[t,r] * Down_e( SiLU(Gate_e x_t) * (Up_e x_t) ), e = idx[t,r] ("quantization"
+// glossary, "Q4_K routed experts": gate and up fused in one pass, the down projection accumulated into the output;
+// "Mixed-precision compression of DeepSeek-V4-Flash", "What compression does not solve": one decode step reads every
+// active expert weight once, so the step is bound by HBM bandwidth).
 //
-// Work units (fixed for every T, so the arithmetic of a token never changes):
-//   G unit (expert u, 128-row tile rt of [Gate;Up], K segment ks): fp32 partial g/u of the tile's 64 gate and 64
-//     up rows over KS_G k-tiles, written to the workspace. The unit that completes the last segment of (u, rt)
-//     sums the segments in order, forms h = SiLU(g) * u and writes the E2M1 parts of h for the D units.
-//   D unit (expert u, 128-row tile jt of Down, segment ks): fp32 partial of Down * h. The unit that completes the
-//     last D unit of row tile jt (over all experts and segments) sums each (expert, token) in segment order and
-//     combines y[t] = sum_r w[t, r] * d_r in rank order.
-// Units are dealt round-robin to persistent CTAs (one per SM, cooperative launch), G units first (expert-major),
-// then D units; the grid is a multiple of the number of gate/up segments, so all G units of a CTA share one K
-// segment. x is split into its parts once per call by the epilogue warps of the whole grid (an operand image in
-// the workspace); each CTA then bulk-copies its segment's part tiles into shared memory and keeps them resident.
-// With a router (moe_route_expert_ffn), warps 2..7 of every CTA first compute halves of the router logits, and
-// every CTA then selects each token's experts itself (route.cuh, the same arithmetic as the standalone router).
-// Inside a CTA, three independent pipelines take the CTA's units as they free up. A pipeline is a weight-issuing
-// warp, an activation-issuing warp (h parts of D units, after their h is final), an MMA-issuing warp, a three-slot
-// shared-memory ring, two to four TMEM accumulators and a group of four epilogue warps. One issuing thread
-// sustains only about one wait-and-issue round per 330 ns (TMA) or one stage of MMAs plus commit per ~600 cycles
-// (tcgen05), while one SM must consume an 8.5 KB weight tile every ~180 ns to keep pace with HBM. Cross-CTA
-// dependencies (partials complete, h of an expert's K segment final) are global counters with bounded waits; the
-// last CTA to finish resets them.
+// Arithmetic. The block-scaled MMA (kind::mxf4: E2M1 x E2M1, one UE8M0 exponent per 32, K = 64 per instruction) has
+// the weights as the 128-row operand A, read as PACKED codes straight from the layout, and a few activation columns
+// as operand B: x (gate/up) and h (down) are each split into PARTS = 6 E2M1 parts per 32-block (part p has exponent
+// e0 - 2p and quantises what the earlier parts left; the error is below 1/3072 of the block's largest value).
+// Column 6 t + p holds part p of token t; N = W = 16 ceil(6 T / 16). A token's value is the sum of its part
+// columns in part order, and every column is computed on its own, so a token's numbers do not depend on which
+// other tokens share the sweep (verify row t == decode of token t, "Width drift").
+//
+// Decomposition. A SLICE is 64 intermediate indices of one expert: one 128-row gate/up tile row (64 gate + 64 up
+// rows) over all of H, and the 64 matching columns of Down (the DOWN layout stores them as chunks of 256 rows x 64
+// columns). The arithmetic of a slice never changes:
+//   g, u of the slice = sum over SG segments (KSG k-tiles each, accumulated in TMEM) in segment order;
+//   h = SiLU(g) * u in fp32, split into E2M1 parts;
+//   one MMA (K = 64) per 128 rows of Down gives the slice's partial of those rows of the expert output;
+//   y[t] = sum_r w[t, r] * (sum over the expert's slices, in slice order, of the partials), ranks in order.
+// Only WHICH CTA does which slice depends on the call. Every CTA owns nw = floor(slices / CTAs) WHOLE slices: it
+// runs all their segments, forms h in its own shared memory and runs their down chunks, with no global hand-off.
+// The remaining R < CTAs slices are SPLIT: their segments (exports) are spread over the CTAs and run first; their
+// partials go to global memory and are counted. Their down chunks (imports) are dealt in contiguous runs, so a CTA
+// imports from one or two split slices, forms each one's h itself from the counted partials, and runs the chunks
+// last; the runs are sized so that every CTA streams the same number of weight bytes to within one tile. Each
+// CTA's order: the first whole slice's segments, the exports (they stream while that slice's h is formed), the
+// other whole slices (W1 D0 W2 D1 ... so that forming h of a slice overlaps the next slice's stream), imports. A grid barrier then lets every CTA sum the down partials of its share of the outputs (one warp
+// per (token, 32 rows, rank): a lane per row, the slices in order).
+//
+// Inside a CTA, three independent pipelines take the CTA's units as they free up: a copy-issuing warp, an
+// MMA-issuing warp, a three-slot shared-memory ring, TMEM accumulators and a group of
+// four epilogue warps. A helper warp does the work that waits on global memory (storing and counting export
+// partials, forming the h of imported slices) so that no epilogue group stalls on it. One issuing thread sustains only about one wait-and-issue round per 330 ns (TMA) or one
+// stage of MMAs plus commit per ~600 cycles (tcgen05), while one SM must consume an 8.5 KB weight tile every
+// ~180 ns to keep pace with HBM. Every wait is bounded; on a timeout the kernel records MOE_ERR_DEVICE_TIMEOUT, lets
+// its own copies land, frees TMEM and returns. With a router (moe_route_expert_ffn), warps 2..7 of every CTA first
+// compute halves of the router logits, and every CTA then selects each token's experts itself (route.cuh, the same
+// arithmetic as the standalone router).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <mutex>
@@ -43,72 +53,165 @@ namespace moe {
 namespace dtc {
 
 constexpr int NPIPE = 3;                 // pipelines per CTA
-constexpr int RING = 3;                  // stage slots per pipeline (more bytes in flight only lengthen the queues:
-                                         // every dependent L2 round trip of the call then takes longer)
-constexpr int NSLOT = NPIPE * RING;
+constexpr int RING_MAX = 4;              // stage slots per pipeline: 4 when shared memory allows (T <= 4), else 3
+constexpr int NSLOT = NPIPE * RING_MAX;
+constexpr int NC_MAX = 2;                // down chunks per local down unit at most
 constexpr int PARTS = 6;                 // E2M1 parts per activation value
-constexpr int NB = 48;                   // B rows (MMA N): PARTS x 8 tokens
-constexpr int A_BYTES = 8192;            // 128 rows x 64 B of packed E2M1 weight codes
-constexpr int B_BYTES = NB * 64;         // 48 rows x 64 B of packed E2M1 activation parts
-constexpr int SLOT_BYTES = A_BYTES + B_BYTES + 1024;  // + two 512-byte exponent blocks; 12 KB
 constexpr int MAX_T = 8, MAX_K = 8, MAX_U = MAX_T * MAX_K;
-constexpr int HROWS = NB;                // B rows of each expert's h parts
-constexpr int EPI_WARP0 = 3 * NPIPE;     // warps: 2 NPIPE producers, NPIPE MMA issuers, then the epilogue groups
-// (each issuing thread has a warp of its own: issuing lanes that share a warp diverge and run one after another)
-constexpr int NGRP = NPIPE;              // epilogue groups of 4 warps; group j drains pipeline j
-constexpr int QN = 16;                   // unit-id queue entries per pipeline
-constexpr int ABUF_MAX = 4;              // accumulators per pipeline
-constexpr int THREADS = (EPI_WARP0 + 4 * NGRP) * 32;
-constexpr uint32_t TMEM_COLS = 512;      // accumulators: pipeline j, buffer a at W (j ABUF + a); scales from 384
-constexpr uint32_t SF_COL0 = 384;
-static_assert(128 * NPIPE <= (int)SF_COL0 && SF_COL0 + 8 * NSLOT <= TMEM_COLS, "TMEM budget");
-// Every gate/up unit of CTA b covers the same K segment (b mod S_G: the grid is a multiple of S_G), so the CTA keeps
-// that segment's x parts resident: 8 k-tiles x 48 rows x 64 B in the 64-byte-swizzled MMA layout, and their
-// exponent blocks.
-constexpr int XRES_TILE = NB * 64;       // 3 KB per k-tile
-constexpr int XRES_BYTES = 8 * XRES_TILE + 8 * 512;
-constexpr int SMEM = NSLOT * SLOT_BYTES + XRES_BYTES + 1024;
+constexpr int WMAX = 48;                 // B rows (MMA N) at most: PARTS x 8 tokens
+// a stage slot: [0, 8192) weight codes (gate/up tile 128 rows x 64 B, 64-byte swizzle; down chunk 256 rows x 32 B,
+// 32-byte swizzle), [8192, 8704) weight exponents (a down chunk is one 8704-byte copy); [8704, 9216) activation
+// exponents, [9216, 12288) activation codes (x parts W x 64 B, swizzled like the weights)
+constexpr int SL_SFA = 8192, SL_SFB = 8704, SLOT_BYTES = 12288;  // activation codes at SL_SFB + 512
+// activation images: [512 B exponent block][W rows of codes, pre-arranged in the MMA's swizzle], so one bulk copy
+// (x, from global memory) or none (h, formed in shared memory) gives a stage its whole activation operand
+constexpr int XIMG = 512 + WMAX * 64;    // per gate/up k-tile (x parts), in the workspace
+constexpr int HIMG = 2048;               // per slice (h parts: 512 + WMAX * 32), in shared memory
+constexpr int NHB = 2;                   // h buffers of whole slices in flight per CTA
+constexpr int NIB = 4;                   // h buffers of imported slices
+constexpr int NXB = 4;                   // staging buffers of export partials
+constexpr int MAX_SG = 8;                // segments per slice at most
+constexpr int RMAX = 256;                // split slices at most (fewer than the CTAs)
+constexpr int EPI_WARP0 = 2 * NPIPE;     // warps: NPIPE producers, NPIPE MMA issuers (each issuing thread has a warp
+constexpr int NGRP = NPIPE;              // of its own: issuing lanes of one warp run one after another), then the epilogue
+constexpr int QN = 32;                   // groups of 4 warps (group j drains pipeline j), then the helper warp;
+constexpr int HELPER = EPI_WARP0 + 4 * NGRP;  // unit-queue entries per pipeline
+constexpr int THREADS = (HELPER + 1) * 32;
+constexpr uint32_t TMEM_COLS = 512;      // accumulators below SF_COL0, 8 scale columns per slot from there
+constexpr uint32_t SF_COL0 = TMEM_COLS - 8 * NSLOT;
+static_assert(SF_COL0 + 8 * NSLOT <= TMEM_COLS, "TMEM budget");
 
-// ------------------------------------------------------------------ geometry of one call
+// unit types
+enum { U_EXPORT = 0, U_LOCAL = 1, U_DLOCAL = 2, U_DIMPORT = 3 };
+
+// ------------------------------------------------------------------ geometry and schedule of one call
 struct Geo {
-  int H, I, T, k, U;
-  int RTG, KTG, KSG, SG;   // gate/up: row tiles, k-tiles, k-tiles per unit, segments
-  int RTD, KTD, KSD, SD;   // down
-  int nG, nD;              // units
-  int W, ABUF;             // accumulator width = MMA N (16 ceil(6 T / 16): a column per part and token, in 16s;
-                           // each column is computed on its own, whatever N is) and accumulators per pipeline
+  int H, I, T, k, E, W, RING;
+  int RC, UREG;                 // TMEM columns of one unit's accumulator region, regions per pipeline
+  int NC, NDL;                  // down chunks per local down unit, local down units per slice
+  int NS, NQ, KTG, KSG, SG;     // slices per expert, row pairs of Down, k-tiles of gate/up, k-tiles per segment, segments
+  int G;                        // CTAs
+  // schedule (depends on U, set on the device once the routing is known)
+  int U, Z, nw, Zw, R, ne_lo, X, A, A1;
+  int F1, Rm1, F2, Rm2;         // import counts: CTA c gets F + (1 if its index < Rm) of each dealing round
 };
-// k-tiles per unit: gate/up 8 (or 4, 2), down 4 (or 2) -- shorter down units shorten the tail after the last h
-__host__ __device__ inline int ks_for_g(int kt) { return kt % 8 == 0 ? 8 : (kt % 4 == 0 ? 4 : 2); }
-__host__ __device__ inline int ks_for_d(int kt) { return kt % 4 == 0 ? 4 : 2; }
+// Segments of a gate/up slice: the largest divisor SG of the k-tile count with SG <= MAX_SG and at least two k-tiles
+// per segment (one k-tile when there are only two); a function of H alone, so every call sums the same segments.
+__host__ __device__ inline int sg_for(int ktg) {
+  for (int sg = MAX_SG; sg > 1; --sg)
+    if (ktg % sg == 0 && ktg / sg >= 2) return sg;
+  return 1;
+}
+
+__host__ __device__ inline void make_schedule(Geo& g, int U) {
+  g.U = U;
+  g.Z = U * g.NS;
+  g.nw = g.Z / g.G;
+  g.Zw = g.nw * g.G;
+  g.R = g.Z - g.Zw;
+  const int ne = g.R * g.SG;                     // export segments
+  g.ne_lo = ne / g.G;
+  g.X = ne % g.G;                                // CTAs with one export segment more
+  g.A = g.R * g.NQ;                              // import chunks
+  // the CTAs without the extra segment first get up to KSG chunks each (a segment is KSG tiles), then the rest goes
+  // round-robin over all CTAs: every CTA streams the same number of tiles to within one
+  const int a1 = (g.G - g.X) * g.KSG;
+  g.A1 = g.A < a1 ? g.A : a1;
+  g.F1 = g.A1 / (g.G - g.X);
+  g.Rm1 = g.A1 % (g.G - g.X);
+  g.F2 = (g.A - g.A1) / g.G;
+  g.Rm2 = (g.A - g.A1) % g.G;
+}
+
+struct Unit {
+  int type, u, s, x, li, ib;  // x: segment (gate/up) or first row pair q (down); li: local slice ordinal or split
+};                            // index; ib: ordinal of the import slice in this CTA
+// packed form of a unit for the table in shared memory
+__device__ __forceinline__ uint64_t pack_unit(const Unit& r) {
+  return (uint64_t)(r.type & 255) | ((uint64_t)(r.x & 255) << 8) | ((uint64_t)(r.u & 255) << 16) |
+         ((uint64_t)(r.s & 255) << 24) | ((uint64_t)(r.li & 0xFFFF) << 32) | ((uint64_t)(r.ib & 255) << 48);
+}
+__device__ __forceinline__ Unit unpack_unit(uint64_t v) {
+  Unit r;
+  r.type = (int)(v & 255); r.x = (int)((v >> 8) & 255); r.u = (int)((v >> 16) & 255); r.s = (int)((v >> 24) & 255);
+  r.li = (int)((v >> 32) & 0xFFFF); r.ib = (int)((v >> 48) & 255);
+  return r;
+}
+struct Mine {                 // this CTA's share: export segments, whole-slice units, imports (a contiguous run of
+  int ne, nloc, nimp, n;      // the import chunks, numbered split slice * NQ + row pair, from a0)
+  int a0, nis;                // first import chunk, import slices
+};
+__host__ __device__ inline int mn(int a, int b) { return a < b ? a : b; }
+__host__ __device__ inline Mine my_share(const Geo& g, int c) {
+  Mine m;
+  m.ne = g.ne_lo + (c < g.X ? 1 : 0);
+  m.nloc = g.nw * (g.SG + g.NDL);
+  const int n1 = c < g.X ? 0 : g.F1 + (c - g.X < g.Rm1 ? 1 : 0);
+  const int n2 = g.F2 + (c < g.Rm2 ? 1 : 0);
+  const int p1 = c <= g.X ? 0 : g.F1 * (c - g.X) + mn(c - g.X, g.Rm1);
+  const int p2 = g.F2 * c + mn(c, g.Rm2);
+  m.nimp = n1 + n2;
+  m.a0 = p1 + p2;
+  m.nis = m.nimp > 0 ? (m.a0 + m.nimp - 1) / g.NQ - m.a0 / g.NQ + 1 : 0;
+  m.n = m.ne + m.nloc + m.nimp;
+  return m;
+}
+// Position of export segment xo (0 .. ne - 1) in the CTA's order: after the first whole slice's segments, so that
+// they stream while that slice's h is formed (first of all when the CTA has no whole slice); their importers run
+// their chunks last.
+__host__ __device__ inline int export_pos(const Geo& g, int xo) { return g.nw > 0 ? g.SG + xo : xo; }
+__device__ inline Unit unit_at(const Geo& g, const Mine& mi, int c, int i) {
+  Unit r;
+  r.ib = 0;
+  const int e0 = export_pos(g, 0);
+  if (i >= e0 && i < e0 + mi.ne) {                  // export segment
+    const int j = c + g.G * (i - e0);
+    const int z = g.Zw + j / g.SG;
+    r.type = U_EXPORT; r.u = z / g.NS; r.s = z % g.NS; r.x = j % g.SG; r.li = z - g.Zw;
+    return r;
+  }
+  if (i >= e0) i -= mi.ne;
+  if (i < mi.nloc) {                                // whole slices: W0 W1 D0 W2 D1 ... W(nw-1) D(nw-2) D(nw-1)
+    int m, isd, x;
+    if (i < g.SG) { m = 0; isd = 0; x = i; }
+    else {
+      const int ip = i - g.SG, blk = g.SG + g.NDL;
+      const int b = ip / blk + 1, rr = ip % blk;
+      if (b < g.nw && rr < g.SG) { m = b; isd = 0; x = rr; }
+      else if (b < g.nw) { m = b - 1; isd = 1; x = rr - g.SG; }
+      else { m = g.nw - 1; isd = 1; x = rr; }
+    }
+    const int z = c * g.nw + m;
+    r.type = isd ? U_DLOCAL : U_LOCAL; r.u = z / g.NS; r.s = z % g.NS; r.x = isd ? x * g.NC : x; r.li = m;
+    return r;
+  }
+  i -= mi.nloc;                                     // import chunk
+  const int a = mi.a0 + i;
+  const int z = g.Zw + a / g.NQ;
+  r.type = U_DIMPORT; r.u = z / g.NS; r.s = z % g.NS; r.x = a % g.NQ; r.li = z - g.Zw;
+  r.ib = a / g.NQ - mi.a0 / g.NQ;
+  return r;
+}
 
 // ------------------------------------------------------------------ workspace (byte offsets from the base)
-// [0, 256)       WsHeader (status word)
-// [256, ...)     counters (uint32): (unused), done, h_ready[64][16] (per expert and down K segment),
-//                g_cnt[64 * 64] (per expert and gate/up row tile), d_cnt[32] (per down row tile)
-// then hb [Umax * 48][I/2] packed E2M1 h parts, hsf [Umax][I/128][512] their exponents,
-//      gpart [Umax][2I/128][S_G][TS][128] fp32, dpart [Umax][H/128][S_D][TS][128] fp32
-// with Umax = T_max * k union experts and TS = T_max token columns of the partial buffers.
+// [0, 256)   WsHeader (status word, done, grid barrier)
+// [256, ..)  counters (uint32): x parts done, router logits done, then per split slice: its segments stored
+// then gpart [RMAX * MAX_SG][TS][128] fp32 (split slices' segment partials, by token), ximg [KTG][XIMG] (x parts),
+//      dpart [cols][H / 32][NS][32] fp32 (down partials: a column per (expert, token) pair of the call),
+//      lg [tokens][2][E] router logit halves.
 constexpr int64_t kCnt = 256;
-constexpr int C_DONE = 1, C_HREADY = 2, C_G = C_HREADY + MAX_U * 16, C_D = C_G + MAX_U * 64;
-constexpr int C_ROUTE = C_D + 32;      // experts whose logits are in (routing inside the kernel)
-constexpr int C_XP = C_ROUTE + 1;        // 32-blocks of x split into the x-part image
-constexpr int C_END = C_XP + 1;
+constexpr int C_XP = 0, C_ROUTE = 1, C_SPLIT = 2, C_END = C_SPLIT + RMAX;
 struct Ws {
-  int64_t hb, hsf, gpart, dpart, lg, xp, total;
+  int64_t gpart, ximg, dpart, lg, total;
 };
 inline int64_t al1k(int64_t v) { return (v + 1023) & ~(int64_t)1023; }
-inline Ws ws_layout(int64_t H, int64_t I, int64_t Umax, int64_t TS) {
+inline Ws ws_layout(int64_t H, int64_t I, int64_t cols, int64_t TS) {
   Ws w;
   int64_t o = al1k(kCnt + (int64_t)C_END * 4);
-  const int64_t RTG = 2 * I / 128, KTG = H / 128, RTD = H / 128, KTD = I / 128;
-  const int64_t SG = KTG / ks_for_g((int)KTG), SD = KTD / ks_for_d((int)KTD);
-  w.hb = o;    o = al1k(o + Umax * HROWS * I / 2);
-  w.hsf = o;   o = al1k(o + Umax * KTD * 512);
-  w.gpart = o; o = al1k(o + Umax * RTG * SG * TS * 128 * 4);
-  w.dpart = o; o = al1k(o + Umax * RTD * SD * TS * 128 * 4);
-  w.lg = o;    o = al1k(o + (int64_t)kRouteTPC * 2 * kRouteMaxE * 4);  // router logit halves [token][half][expert]
-  w.xp = o;    o = al1k(o + (H / 128) * (XRES_TILE + 512));      // x parts: [k-tile][48 rows][64 B], then exponents
+  w.gpart = o; o = al1k(o + (int64_t)RMAX * MAX_SG * TS * 128 * 4);
+  w.ximg = o;  o = al1k(o + (H / 128) * XIMG);
+  w.dpart = o; o = al1k(o + cols * H * (I / 64) * 4);
+  w.lg = o;    o = al1k(o + (int64_t)kRouteTPC * 2 * kRouteMaxE * 4);
   w.total = o;
   return w;
 }
@@ -126,15 +229,14 @@ struct Args {
   float* y;                   // [T][H]
   __nv_bfloat16* yb;          // [T][H] or NULL
   int accumulate;
-  int E;
   uint8_t* ws;
   Ws L;
-  int ts;                     // token stride of the partial buffers
+  int ts;                     // token stride of the segment partials
   Geo g;
   long long wait_ns;
 };
 
-// ------------------------------------------------------------------ small helpers
+// ------------------------------------------------------------------ E2M1 parts
 // Exponent of an E2M1 block: e = clamp(k + 127, 1, 254), k the smallest integer with amax <= 6 * 2^k.
 __device__ __forceinline__ int mx4_exp(float amax) {
   const uint32_t ab = __float_as_uint(amax) & 0x7FFFFFFFu;
@@ -155,10 +257,12 @@ __device__ __forceinline__ uint32_t e2m1_code(float v) {
   asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}" : "=h"(d) : "f"(0.0f), "f"(v));
   return d & 15u;
 }
+// value of E2M1 code c, built from its bits: exponent field f = (c >> 1) & 3 and mantissa bit m = c & 1 give
+// 2^(f - 1) (1 + m / 2) for f > 0 and m / 2 for f = 0; bit 3 is the sign
 __device__ __forceinline__ float e2m1_value(uint32_t c) {
-  const float mag = (c & 4) ? ((c & 2) ? ((c & 1) ? 6.f : 4.f) : ((c & 1) ? 3.f : 2.f))
-                            : (float)(c & 3) * 0.5f;
-  return (c & 8) ? -mag : mag;
+  const uint32_t f = (c >> 1) & 3u, m = c & 1u;
+  const uint32_t mag = f ? ((126u + f) << 23) | (m << 22) : (m ? 0x3F000000u : 0u);
+  return __uint_as_float(mag | ((c & 8u) << 28));
 }
 __device__ __forceinline__ float warp_amax(float v) {
   const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(v)));
@@ -168,48 +272,32 @@ __device__ __forceinline__ float warp_amax(float v) {
 // magnitude <= 6 * 2^(e0 - 127)); part p uses e0 - 2p (clamped at 1) and quantises what parts 0 .. p-1 left. After
 // a part the remainder is at most half an E2M1 step, <= 1 unit of its scale = 4 units of the next part's, so no
 // part saturates and each adds at least 2 bits: the final error is below 2^-10 of part 0's scale, i.e. below
-// 1/3072 of the block's largest magnitude. Only e0 needs a warp reduction. Even lanes get the packed byte of
-// elements (l, l + 1) of each part in bytes[p] (element l in the low nibble). A block holding NaN or infinity has
-// no E2M1 encoding: every part gets the E8M0 NaN exponent (255), which the block-scaled MMA turns into NaN.
-// live[q] must be the same for every lane of the warp (the parts of a dead block are skipped by all lanes).
-template <int NV>
-__device__ __forceinline__ void split_parts_n(const float (&v)[NV], const bool (&live)[NV], uint32_t (&bytes)[NV][PARTS],
-                                              int (&exps)[NV][PARTS]) {
-  const int lane = threadIdx.x & 31;
-  float r[NV], am[NV];
-#pragma unroll
-  for (int q = 0; q < NV; ++q) {
-    r[q] = v[q];
-    const float m = warp_amax(live[q] ? v[q] : 0.f);  // every lane takes part in the reduction
-    am[q] = live[q] ? m : 0.f;
-  }
-#pragma unroll
-  for (int q = 0; q < NV; ++q) {
-    if (!live[q]) continue;
-    const bool nonfinite = !(am[q] <= 3.4028235e38f);
-    const int e0 = mx4_exp(am[q]);
-#pragma unroll
-    for (int p = 0; p < PARTS; ++p) {
-      const int e = nonfinite ? 255 : (e0 - 2 * p > 1 ? e0 - 2 * p : 1);
-      const uint32_t c = nonfinite ? 0u : e2m1_code(r[q] * pow2_127m(e));
-      const uint32_t hi = __shfl_down_sync(0xFFFFFFFFu, c, 1);
-      bytes[q][p] = (lane & 1) ? 0u : (c | (hi << 4));
-      exps[q][p] = e;
-      if (!nonfinite) r[q] = r[q] - e2m1_value(c) * pow2_m127(e);
-    }
-  }
-}
+// 1/3072 of the block's largest magnitude. A block holding NaN or infinity has no E2M1 encoding: every part gets
+// the E8M0 NaN exponent (255), which the block-scaled MMA turns into NaN. Even lanes get the packed byte of elements
+// (l, l + 1) of part p in bytes[p] (element l in the low nibble), every lane the exponents. Every lane of the warp
+// must call it.
 __device__ __forceinline__ void split_parts(float v, uint32_t (&bytes)[PARTS], int (&exps)[PARTS]) {
-  const float vv[1] = {v};
-  const bool live[1] = {true};
-  uint32_t b[1][PARTS];
-  int e[1][PARTS];
-  split_parts_n<1>(vv, live, b, e);
+  const float am = warp_amax(v);
+  const bool nonfinite = !(am <= 3.4028235e38f);
+  const int e0 = mx4_exp(am);
+  float r = nonfinite ? 0.f : v;
+  uint32_t cs[PARTS];
 #pragma unroll
-  for (int p = 0; p < PARTS; ++p) { bytes[p] = b[0][p]; exps[p] = e[0][p]; }
+  for (int p = 0; p < PARTS; ++p) {  // the remainder chain first (the value times a power of two is exact)
+    const int e = e0 - 2 * p > 1 ? e0 - 2 * p : 1;
+    cs[p] = e2m1_code(r * pow2_127m(e));
+    r = fmaf(-e2m1_value(cs[p]), pow2_m127(e), r);
+  }
+#pragma unroll
+  for (int p = 0; p < PARTS; ++p) {
+    bytes[p] = cs[p] | (__shfl_down_sync(0xFFFFFFFFu, cs[p], 1) << 4);
+    exps[p] = nonfinite ? 255 : (e0 - 2 * p > 1 ? e0 - 2 * p : 1);
+  }
 }
-__device__ __forceinline__ int sfb(int row, int kb) { return (row & 31) * 16 + (row >> 5) * 4 + kb; }
+// byte of the permuted 512-byte exponent block that holds (operand row n, 32-block b)
+__device__ __forceinline__ int sfb(int n, int b) { return (n & 31) * 16 + (n >> 5) * 4 + b; }
 
+// ------------------------------------------------------------------ waits and counters
 // Bounded wait on a global counter (acquire); gives up when `abort_flag` is set elsewhere or after lim ns.
 __device__ __forceinline__ bool wait_ge(const uint32_t* p, uint32_t target, volatile int* abort_flag, long long lim) {
   if (ld_acquire_u32(p) >= target) return true;
@@ -233,79 +321,37 @@ __device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, volatile i
     if (globaltimer_ns() - t0 > lim) { *abort_flag = 1; return false; }
   }
 }
-
-// Publish: every store this thread has performed -- and, through the preceding CTA barrier, the stores of the
-// threads it synchronised with -- becomes visible before the increment (release at GPU scope).
 __device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-// Count-and-check: release our stores, acquire the stores of every earlier incrementer.
 __device__ __forceinline__ uint32_t atom_acq_rel_add(uint32_t* p, uint32_t v) {
   uint32_t old;
   asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
   return old;
 }
-
-struct Unit {
-  int d, u, rt, ks;
-};
-// Global order of the work: blocks of units G(u) (all row tiles and segments of expert u's gate/up) and D(u); D(u)
-// is placed after G(u + LAG). With LAG = MAX_U every G block comes first (G0 .. G(U-1) D0 .. D(U-1)), which measured
-// best: a D block placed earlier waits for h of its expert while holding a pipeline.
-constexpr int LAG = MAX_U;
-struct Order {
-  int n;                       // blocks
-  int start[2 * MAX_U + 1];    // first unit of each block; start[n] = total units
-  int8_t d[2 * MAX_U], u[2 * MAX_U];
-};
-// Blocks of the global unit order: G(0) .. G(U-1) then D(0) .. D(U-1) (every gate/up unit first: a down block
-// placed earlier waits for h of its expert while holding a pipeline). Built by one warp, a block per lane.
-static_assert(LAG == MAX_U, "the unit order puts every gate/up block first");
-__device__ void build_order_warp(Order& o, const Geo& g, int U) {
-  const int lane = threadIdx.x & 31;
-  const int nGu = g.RTG * g.SG, nDu = g.RTD * g.SD;
-  for (int b = lane; b < 2 * U; b += 32) {
-    const bool d = b >= U;
-    o.start[b] = d ? U * nGu + (b - U) * nDu : b * nGu;
-    o.d[b] = (int8_t)d;
-    o.u[b] = (int8_t)(d ? b - U : b);
-  }
-  if (lane == 0) {
-    o.start[2 * U] = U * (nGu + nDu);
-    o.n = 2 * U;
-  }
-}
-__device__ __forceinline__ Unit unit_of(int v, const Geo& g, const Order& o) {
-  int lo = 0, hi = o.n - 1;  // last block with start <= v
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (o.start[mid] <= v) lo = mid; else hi = mid - 1;
-  }
-  Unit r;
-  r.d = o.d[lo];
-  r.u = o.u[lo];
-  const int rr = v - o.start[lo], S = r.d ? g.SD : g.SG;
-  r.rt = rr / S;
-  r.ks = rr % S;
-  return r;
+// K-major operand with 32-byte rows and the 32-byte swizzle (8-row atoms of 256 bytes)
+__device__ __forceinline__ uint64_t umma_desc_sw32(uint32_t saddr) { return umma_desc(saddr, 16, 256, 6); }
+// kind::mxf4 instruction descriptor with separate scale-byte selectors for A and B (0 or 2)
+__device__ __forceinline__ uint32_t idesc_mxf4_ab(uint32_t N, uint32_t a_sf, uint32_t b_sf) {
+  return (b_sf << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | (1u << 23) | ((128u >> 4) << 24) | (a_sf << 29);
 }
 
+// ------------------------------------------------------------------ routing tables
 // Tables every CTA builds from idx: the union of experts (first-appearance order over (t, r)), each expert's
-// tokens (slot order = token order) and, per (t, r), the union index and the token's slot in that expert.
+// tokens (slot order = token order), per (t, r) the union index and the token's slot, and the first down-partial
+// column of each union expert (its tokens' columns follow in slot order).
 struct Tables {
-  int32_t ue[MAX_U];         // union index -> expert id
-  int8_t ntok[MAX_U];        // tokens of each union expert
-  int8_t tok[MAX_U][MAX_T];  // union expert, slot -> token
-  int8_t pu[MAX_T][MAX_K];   // (t, r) -> union index
-  int8_t ps[MAX_T][MAX_K];   // (t, r) -> slot
-  float w[MAX_T][MAX_K];     // routing weights
+  int32_t ue[MAX_U];
+  int8_t ntok[MAX_U];
+  int8_t tok[MAX_U][MAX_T];
+  int8_t pu[MAX_T][MAX_K];
+  int8_t ps[MAX_T][MAX_K];
+  int16_t col0[MAX_U];
+  float w[MAX_T][MAX_K];
   int U;
   int bad;
 };
-
-// Built in two steps so that the weight stream starts as early as possible.
-// (1) build_union_warp, one warp: the union of the experts in first-appearance order over (t, r) and whether any id
-//     is out of range (match_any / ballot over the T k <= 64 entries, two per lane; no dependent memory chains).
+// (1) one warp: the union in first-appearance order over (t, r) and whether any id is out of range
 __device__ void build_union_warp(Tables& tb, const int32_t (*idx)[MAX_K], int T, int k, int E) {
   const int lane = threadIdx.x & 31;
   const int n = T * k;
@@ -314,10 +360,10 @@ __device__ void build_union_warp(Tables& tb, const int32_t (*idx)[MAX_K], int T,
   const bool bad = __any_sync(0xFFFFFFFFu, (v0 && (e0 < 0 || e0 >= E)) || (v1 && (e1 < 0 || e1 >= E)));
   const int key0 = v0 ? e0 : -1 - lane, key1 = v1 ? e1 : -33 - lane;  // absent entries never match
   const uint32_t lt = (1u << lane) - 1u;
-  // every lane takes part in each warp-wide operation (none sits inside a short-circuit or a branch)
   const uint32_t m0 = __match_any_sync(0xFFFFFFFFu, key0), m1 = __match_any_sync(0xFFFFFFFFu, key1);
-  bool in0 = false;  // entry lane + 32 already appeared among entries 0 .. 31
-  for (int q = 0; q < 32; ++q) in0 |= __shfl_sync(0xFFFFFFFFu, key0, q) == key1;
+  bool in0 = false;  // entry lane + 32 already appeared among entries 0 .. 31 (only when there are more than 32)
+  if (n > 32)
+    for (int q = 0; q < 32; ++q) in0 |= __shfl_sync(0xFFFFFFFFu, key0, q) == key1;
   const bool first0 = v0 && (m0 & lt) == 0;
   const bool first1 = v1 && !in0 && (m1 & lt) == 0;
   const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, first0), b1 = __ballot_sync(0xFFFFFFFFu, first1);
@@ -328,8 +374,7 @@ __device__ void build_union_warp(Tables& tb, const int32_t (*idx)[MAX_K], int T,
     tb.bad = bad ? 1 : 0;
   }
 }
-// (2) build_slots, one thread, while the first weight tiles are in flight: the routing weights, each union expert's
-//     tokens (slot order = token order) and, per (t, r), the union index and the token's slot in that expert.
+// (2) one thread: weights, each union expert's tokens, per (t, r) the union index and slot, the column bases
 __device__ void build_slots(Tables& tb, const int32_t (*idx)[MAX_K], const float (*w)[MAX_K], int T, int k) {
   for (int u = 0; u < tb.U; ++u) tb.ntok[u] = 0;
   for (int t = 0; t < T; ++t)
@@ -345,226 +390,162 @@ __device__ void build_slots(Tables& tb, const int32_t (*idx)[MAX_K], const float
       tb.pu[t][r] = (int8_t)u;
       tb.ps[t][r] = (int8_t)s;
     }
+  int c = 0;
+  for (int u = 0; u < tb.U; ++u) { tb.col0[u] = (int16_t)c; c += tb.ntok[u]; }
 }
 
-// The x parts, split once per call: 32-block j = (token t, k-tile kt, block kb) of x goes to warp j of the grid's
-// epilogue warps (warp ew of CTA b is number 12 b + ew), which splits it into PARTS E2M1 parts (split_parts_n) and
-// writes them into the x-part image in the workspace: k-tile kt at xp + kt * XRES_TILE, row PARTS * t + p, 64 bytes
-// a row, 16-byte chunks in the 64-byte TMA swizzle (chunk c of row r at chunk c ^ ((r >> 1) & 3)) -- the resident
-// B operand as it sits in shared memory -- and the exponents into the permuted blocks at xp + KTG XRES_TILE + 512 kt.
-// Each CTA then copies its K segment's tiles in with two bulk copies.
+// ------------------------------------------------------------------ x parts
+// 32-block j = (token t, k-tile kt, block kb) of x goes to warp j of the grid's epilogue warps, which splits it into
+// PARTS parts and writes them into the x image: k-tile kt at ximg + kt * XIMG = [512 B exponents][W rows x 64 B],
+// row 6 t + p, 16-byte chunk kb at chunk kb ^ ((row >> 1) & 3) (the MMA's 64-byte swizzle). The warp of the last
+// token also clears the padding rows 6T .. W-1 of (kt, kb) (zero codes, exponent 127).
 __device__ __forceinline__ float load_x_block(const Args& a, const Geo& g, int j) {
   const int lane = threadIdx.x & 31;
   if (j >= g.T * g.KTG * 4) return 0.f;
   const int t = j / (g.KTG * 4), rem = j % (g.KTG * 4);
   return __uint_as_float((uint32_t)a.x[(int64_t)t * g.H + rem * 32 + lane] << 16);
 }
-__device__ void split_x_global(const Args& a, const Geo& g, int gw, int nwarps, float xfirst) {
+__device__ void split_x_global(const Args& a, const Geo& g, int gw, int nwarps, float xfirst, uint32_t* cnt) {
   const int lane = threadIdx.x & 31;
   const int nblk = g.T * g.KTG * 4;
-  uint8_t* xp = a.ws + a.L.xp;
-  uint8_t* xpsf = xp + (int64_t)g.KTG * XRES_TILE;
   for (int j = gw; j < nblk; j += nwarps) {
-    float r = j == gw ? xfirst : load_x_block(a, g, j);
+    const float v = j == gw ? xfirst : load_x_block(a, g, j);
     const int t = j / (g.KTG * 4), rem = j % (g.KTG * 4), kt = rem / 4, kb = rem % 4;
-    const float am = warp_amax(r);
-    const bool nonfinite = !(am <= 3.4028235e38f);
-    const int e0 = mx4_exp(am);
-#pragma unroll
-    for (int p = 0; p < PARTS; ++p) {
-      const int e = nonfinite ? 255 : (e0 - 2 * p > 1 ? e0 - 2 * p : 1);
-      const uint32_t c = nonfinite ? 0u : e2m1_code(r * pow2_127m(e));
-      const uint32_t byte = c | (__shfl_down_sync(0xFFFFFFFFu, c, 1) << 4);  // elements (l, l + 1), even l
-      if (!nonfinite) r = r - e2m1_value(c) * pow2_m127(e);
-      // the 16 bytes of the part gathered into four words: word w from the even lanes 8 w .. 8 w + 6
-      uint32_t word = 0;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) word |= (__shfl_sync(0xFFFFFFFFu, byte, (lane & ~7) + 2 * i) & 0xFFu) << (8 * i);
-      const int n = PARTS * t + p;
-      if ((lane & 7) == 0)
-        *reinterpret_cast<uint32_t*>(xp + (int64_t)kt * XRES_TILE + n * 64 + ((kb ^ ((n >> 1) & 3)) << 4) + (lane >> 1)) = word;
-      if (lane == 0) xpsf[kt * 512 + sfb(n, kb)] = (uint8_t)e;
-    }
-    __syncwarp();
-    if (lane == 0) red_release_add(reinterpret_cast<uint32_t*>(a.ws + kCnt) + C_XP, 1u);
-  }
-}
-
-// All G segments of (expert u, row tile rt) are in: g, u of the 64 intermediate indices rt*64 .. +63 (tile rows
-// 0..63 gate, 64..127 up), h = SiLU(g) * u, PARTS E2M1 parts per 32-block into the D operand rows PARTS * s + p.
-// The group's 128 threads take the token slots two at a time.
-__device__ void finalize_h(const Args& a, const Geo& g, const Tables& tb, int u, int rt, int et) {
-  // thread et: row et % 64 of the tile (a warp = one 32-block), token slots et / 64, et / 64 + 2, ...
-  const int row = et & 63, lane = threadIdx.x & 31;
-  const float* gp = reinterpret_cast<const float*>(a.ws + a.L.gpart) + ((int64_t)u * g.RTG + rt) * g.SG * a.ts * 128;
-  const int i = rt * 64 + row, kt = i / 128, kb = (i % 128) / 32;
-  uint8_t* hb = a.ws + a.L.hb + (int64_t)u * HROWS * (g.I / 2);
-  uint8_t* hsf = a.ws + a.L.hsf + ((int64_t)u * g.KTD + kt) * 512;
-  const int nt = tb.ntok[u];
-  for (int s = et >> 6; s < nt; s += 2) {
-    const int t = tb.tok[u][s];
-    float gv = 0.f, uv = 0.f;
-    for (int k0 = 0; k0 < g.SG; k0 += 4) {  // segments in order, loads issued four at a time
-      float gl[4], ul[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (k0 + q < g.SG) {
-          gl[q] = __ldcg(gp + ((int64_t)(k0 + q) * a.ts + t) * 128 + row);
-          ul[q] = __ldcg(gp + ((int64_t)(k0 + q) * a.ts + t) * 128 + 64 + row);
-        }
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (k0 + q < g.SG) { gv += gl[q]; uv += ul[q]; }
-    }
-    const float h = gv / (1.0f + expf(-gv)) * uv;
-    uint32_t c[PARTS];
+    uint8_t* img = a.ws + a.L.ximg + (int64_t)kt * XIMG;
+    uint32_t by[PARTS];
     int ex[PARTS];
-    split_parts(h, c, ex);
+    split_parts(v, by, ex);
 #pragma unroll
     for (int p = 0; p < PARTS; ++p) {
-      if (!(lane & 1)) hb[(int64_t)(PARTS * s + p) * (g.I / 2) + i / 2] = (uint8_t)c[p];
-      if (lane == 0) hsf[sfb(PARTS * s + p, kb)] = (uint8_t)ex[p];
+      const int n = PARTS * t + p;
+      if (!(lane & 1)) img[512 + n * 64 + ((kb ^ ((n >> 1) & 3)) << 4) + (lane >> 1)] = (uint8_t)by[p];
+      if (lane == 0) img[sfb(n, kb)] = (uint8_t)ex[p];
     }
-  }
-}
-
-// All D units of row tile jt are in: y[t][jt*128 + et] = sum_r w[t, r] * (sum over segments of the partial of
-// (expert of rank r, token t)), ranks in order.
-__device__ void combine_rows(const Args& a, const Geo& g, const Tables& tb, int jt, int et) {
-  const float* dp = reinterpret_cast<const float*>(a.ws + a.L.dpart);
-  const int j = jt * 128 + et;
-  for (int t = 0; t < g.T; ++t) {
-    // the partials of every (rank, segment) of the token are loaded before the sums (segments in order per rank,
-    // then ranks in order), four segments at a time
-    float sum[MAX_K];
-#pragma unroll
-    for (int r = 0; r < MAX_K; ++r) sum[r] = 0.f;
-    for (int k0 = 0; k0 < g.SD; k0 += 4) {
-      float pl[MAX_K][4];
-#pragma unroll
-      for (int r = 0; r < MAX_K; ++r) {
-        if (r < g.k) {
-          const float* p = dp + (((int64_t)tb.pu[t][r] * g.RTD + jt) * g.SD * a.ts + tb.ps[t][r]) * 128 + et;
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            if (k0 + q < g.SD) pl[r][q] = __ldcg(p + (int64_t)(k0 + q) * a.ts * 128);
-        }
+    if (t == g.T - 1) {
+      for (int n = PARTS * g.T + lane; n < g.W; n += 32) {
+        *reinterpret_cast<uint4*>(img + 512 + n * 64 + ((kb ^ ((n >> 1) & 3)) << 4)) = make_uint4(0, 0, 0, 0);
+        img[sfb(n, kb)] = 127;
       }
-#pragma unroll
-      for (int r = 0; r < MAX_K; ++r)
-        if (r < g.k)
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            if (k0 + q < g.SD) sum[r] += pl[r][q];
     }
-    float acc = 0.f;
-#pragma unroll
-    for (int r = 0; r < MAX_K; ++r)
-      if (r < g.k) acc = fmaf(tb.w[t][r], sum[r], acc);
-    float* yp = a.y + (int64_t)t * g.H + j;
-    const float out = a.accumulate ? *yp + acc : acc;
-    *yp = out;
-    if (a.yb) a.yb[(int64_t)t * g.H + j] = __float2bfloat16_rn(out);
-  }
-}
-
-__device__ void epilogue(const Args& a, const Geo& g, const Tables& tb, const Order& ord, uint32_t tbase,
-                         uint64_t (*acc_full)[ABUF_MAX], uint64_t (*acc_empty)[ABUF_MAX], uint64_t (*uq_full)[QN], volatile int (*uq)[QN], uint32_t* cnt,
-                         volatile int* s_last, volatile int* s_ok, volatile int* s_unit, volatile int* s_abort) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = warp & 3;
-  const int grp = (warp - EPI_WARP0) / 4;
-  const int bar = 1 + grp;                                      // named barrier of the group
-  const int et = threadIdx.x - (EPI_WARP0 + 4 * grp) * 32;       // 0..127 inside the group
-  const int m = q * 32 + lane;                                   // TMEM lane = weight row of the tile
-  const long long lim = a.wait_ns;
-  float* gpart = reinterpret_cast<float*>(a.ws + a.L.gpart);
-  float* dpart = reinterpret_cast<float*>(a.ws + a.L.dpart);
-  // the units pipeline j = grp took, in order (each accumulator's phases in order)
-  const int j = grp;
-  for (int c = 0;; ++c) {
-    const int ab = c % g.ABUF;
-    // one thread waits; the verdict is shared so that the group's four warps leave (or stay) together
-    if (et == 0) {
-      int st = 0;
-      if (bwait(&uq_full[j][c % QN], (uint32_t)((c / QN) & 1), s_abort, lim)) {
-        const int i = uq[j][c % QN];
-        if (i < 0) st = 2;
-        else { s_unit[grp] = i; st = bwait(&acc_full[j][ab], (uint32_t)((c / g.ABUF) & 1), s_abort, lim) ? 1 : 0; }
-      }
-      s_ok[grp] = st;
-    }
-    named_bar(bar, 128);
-    if (s_ok[grp] != 1) break;
-    tc_fence_after();
-    const int i = s_unit[grp];
-    const Unit un = unit_of((int)blockIdx.x + i * (int)gridDim.x, g, ord);
-    const uint32_t taddr = tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)(g.W * (j * g.ABUF + ab));
-    // column t * PARTS + p = part p of token (or slot) t; sum the parts of each column group in part order
-    float acc[MAX_T];
-#pragma unroll
-    for (int t = 0; t < MAX_T; ++t) acc[t] = 0.f;
-#pragma unroll
-    for (int cb = 0; cb < NB / 16; ++cb) {
-      if (16 * cb >= g.W) break;
-      uint32_t v[16];
-      tc_ld16(taddr + 16 * cb, v);
-      tc_wait_ld();
-#pragma unroll
-      for (int c = 0; c < 16; ++c) acc[(16 * cb + c) / PARTS] += __uint_as_float(v[c]);
-    }
-    tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive_relaxed(&acc_empty[j][ab]);  // TMEM read; no wait for the earlier global stores
-    if (!un.d) {
-      float* gp = gpart + (((int64_t)un.u * g.RTG + un.rt) * g.SG + un.ks) * a.ts * 128 + m;
-#pragma unroll
-      for (int t = 0; t < MAX_T; ++t)
-        if (t < g.T) gp[t * 128] = acc[t];
-    } else {
-      float* dp = dpart + (((int64_t)un.u * g.RTD + un.rt) * g.SD + un.ks) * a.ts * 128 + m;
-      const int nt = tb.ntok[un.u];
-#pragma unroll
-      for (int s = 0; s < MAX_T; ++s)
-        if (s < nt) dp[s * 128] = acc[s];
-    }
-    // count the unit; the one that completes a group of units does the group's follow-up work
-    named_bar(bar, 128);
-    if (et == 0) {
-      uint32_t old, target;
-      if (!un.d) { old = atom_acq_rel_add(cnt + C_G + un.u * g.RTG + un.rt, 1u); target = (uint32_t)g.SG; }
-      else { old = atom_acq_rel_add(cnt + C_D + un.rt, 1u); target = (uint32_t)(g.U * g.SD); }
-      s_last[grp] = (old == target - 1) ? 1 : 0;
-    }
-    named_bar(bar, 128);
-    if (s_last[grp]) {
-      if (!un.d) {
-        finalize_h(a, g, tb, un.u, un.rt, et);
-        named_bar(bar, 128);
-        if (et == 0) red_release_add(cnt + C_HREADY + un.u * 16 + (un.rt * 64) / (128 * g.KSD), 1u);
-      } else {
-        combine_rows(a, g, tb, un.rt, et);
-      }
-    }
+    if (lane == 0) red_release_add(cnt + C_XP, 1u);
   }
 }
 
-__global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constant__ CUtensorMap tm_gu,
-                                                            const __grid_constant__ CUtensorMap tm_dn,
-                                                            const __grid_constant__ CUtensorMap tm_h, const Args a) {
+// ------------------------------------------------------------------ h of a slice
+// The slice's segment partials are in: g and u of its 64 intermediate indices (partial rows 0..63 gate, 64..127
+// up) summed over the SG segments in order, h = SiLU(g) * u, split into PARTS parts per 32-block into an h image
+// [512 B exponents][W rows x 32 B] (row 6 s + p for token slot s, 16-byte half b at half b ^ ((row >> 2) & 1): the
+// MMA's 32-byte swizzle). Rows 6 ntok .. W-1 are padding (zero codes, exponent 127). The partial of (segment sg,
+// token t, row m) is at part[sg * seg_stride + t * 128 + m]; slot s holds token tok[s]. One warp forms one
+// 32-block (block b of slot s, lane = index in the block).
+// h = SiLU(g) * u of one 32-block (lane = index in the block) -> the PARTS rows of slot s in an h image
+__device__ __forceinline__ void h_emit(float gv, float uv, int s, int b, uint8_t* img) {
+  const int lane = threadIdx.x & 31;
+  const float h = __fdividef(gv * uv, 1.0f + __expf(-gv));  // SiLU(g) * u
+  uint32_t by[PARTS];
+  int ex[PARTS];
+  split_parts(h, by, ex);
+#pragma unroll
+  for (int q = 0; q < PARTS; ++q) {
+    const int n = PARTS * s + q;
+    if (!(lane & 1)) img[512 + n * 32 + ((b ^ ((n >> 2) & 1)) << 4) + (lane >> 1)] = (uint8_t)by[q];
+    if (lane == 0) img[sfb(n, b)] = (uint8_t)ex[q];
+  }
+}
+// padding rows 6 ntok .. W-1 of an h image, by `nthr` threads numbered from th
+__device__ __forceinline__ void h_padding(uint8_t* img, int ntok, int W, int th, int nthr) {
+  for (int q = th; q < 2 * (W - PARTS * ntok); q += nthr) {
+    const int n = PARTS * ntok + (q >> 1), c = q & 1;
+    *reinterpret_cast<uint4*>(img + 512 + n * 32 + (c << 4)) = make_uint4(0, 0, 0, 0);
+    img[sfb(n, c)] = 127;
+  }
+}
+// whole slice, by an epilogue group (thread et of 128: warp et / 32 takes blocks (slot, b) = (w / 2, w % 2), then
+// every fourth), partials in shared memory, summed over the segments in order
+__device__ void finalize_local(const float* part, int64_t seg_stride, int SG, int ntok, const int8_t* tok, int W,
+                               uint8_t* img, int et) {
+  const int lane = threadIdx.x & 31;
+  for (int k = et >> 5; k < 2 * ntok; k += 4) {
+    const int s = k >> 1, b = k & 1;
+    const float* p = part + tok[s] * 128 + 32 * b + lane;
+    float gl[MAX_SG], ul[MAX_SG];
+#pragma unroll
+    for (int sg = 0; sg < MAX_SG; ++sg)
+      if (sg < SG) { gl[sg] = p[sg * seg_stride]; ul[sg] = p[sg * seg_stride + 64]; }
+    float gv = 0.f, uv = 0.f;
+#pragma unroll
+    for (int sg = 0; sg < MAX_SG; ++sg)
+      if (sg < SG) { gv += gl[sg]; uv += ul[sg]; }
+    h_emit(gv, uv, s, b, img);
+  }
+  h_padding(img, ntok, W, et, 128);
+}
+// imported slice, by the helper warp, partials in global memory: both blocks of a slot loaded before any sum
+__device__ void finalize_import(const float* part, int64_t seg_stride, int SG, int ntok, const int8_t* tok, int W,
+                                uint8_t* img) {
+  const int lane = threadIdx.x & 31;
+  for (int s = 0; s < ntok; ++s) {
+    const float* p = part + tok[s] * 128 + lane;
+    float gl[2][MAX_SG], ul[2][MAX_SG];
+#pragma unroll
+    for (int b = 0; b < 2; ++b)
+#pragma unroll
+      for (int sg = 0; sg < MAX_SG; ++sg)
+        if (sg < SG) { gl[b][sg] = __ldcg(p + sg * seg_stride + 32 * b); ul[b][sg] = __ldcg(p + sg * seg_stride + 64 + 32 * b); }
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      float gv = 0.f, uv = 0.f;
+#pragma unroll
+      for (int sg = 0; sg < MAX_SG; ++sg)
+        if (sg < SG) { gv += gl[b][sg]; uv += ul[b][sg]; }
+      h_emit(gv, uv, s, b, img);
+    }
+  }
+  h_padding(img, ntok, W, lane, 32);
+}
+
+// ------------------------------------------------------------------ the kernel
+struct Smem {                   // static shared state (the stage ring, h buffers and partials are dynamic)
+  uint64_t full[NSLOT], empty[NSLOT];
+  uint64_t ucomp[NPIPE][8], acc_empty[NPIPE][8];   // unit c of a pipeline done (slot c % 8) / its region drained
+  uint64_t uq_full[NPIPE][QN];
+  uint64_t hready[NHB], hfree[NHB];     // whole slices: h formed / its down chunks done reading it
+  uint64_t iready[NIB], ifree[NIB];     // imported slices: the same
+  uint64_t xstaged[NXB], xfree[NXB];    // export partials staged / copied out
+  uint64_t tab_full, tab2_full, drain[NPIPE];
+  int uq[NPIPE][QN];                    // unit index, and the unit itself (packed), per queue entry
+  uint64_t uqu[NPIPE][QN];
+  int lcnt[NHB];
+  Tables tb;
+  int32_t idx[MAX_T][MAX_K];
+  float wt[MAX_T][MAX_K];
+  uint32_t tmem;
+  int next;
+  int abort;
+  int ok[NGRP][2], last[NGRP], unit[NGRP];
+  int gok;
+};
+// dynamic shared memory: the stage ring, then h images of whole and imported slices, export staging, and the
+// segment partials of whole slices
+inline size_t smem_bytes(int T, int SG, int ring) {
+  return 1024 + (size_t)NPIPE * ring * SLOT_BYTES + (NHB + NIB) * HIMG + (size_t)NXB * T * 128 * 4 +
+         (size_t)NHB * SG * T * 128 * 4;
+}
+
+// TT: the most tokens this instance serves (2: decode and 2-token verify, W = 16; 8: the rest). Only the size of the
+// per-thread arrays differs; the arithmetic of every token is the same in both.
+template <int TT>
+__global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constant__ CUtensorMap tm_gu, const Args a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  __shared__ __align__(8) uint64_t full[NSLOT], empty[NSLOT], acc_full[NPIPE][ABUF_MAX],
-      acc_empty[NPIPE][ABUF_MAX], drain[NPIPE];
-  __shared__ __align__(8) uint64_t uq_full[NPIPE][QN], xres_full, tab_full, tab2_full;
-  uint8_t* xres = smem + NSLOT * SLOT_BYTES;    // resident x parts of this CTA's gate/up K segment
-  uint8_t* xres_sf = xres + 8 * XRES_TILE;
-  __shared__ volatile int uq[NPIPE][QN];
-  __shared__ int s_next;
-  __shared__ Tables tb;
-  __shared__ Order ord;
-  __shared__ uint32_t s_tmem;
-  __shared__ int s_units;
-  __shared__ volatile int s_abort, s_ok[NGRP], s_last[NGRP], s_unit[NGRP];
+  __shared__ Smem S;
+  volatile int* s_abort = &S.abort;
+  const Geo& ga = a.g;
+  uint8_t* hbuf = smem + NPIPE * ga.RING * SLOT_BYTES;                 // [NHB][HIMG] whole slices' h
+  uint8_t* ibuf = hbuf + NHB * HIMG;                                    // [NIB][HIMG] imported slices' h
+  float* xstage = reinterpret_cast<float*>(ibuf + NIB * HIMG);          // [NXB][T][128] export partials
+  float* spart = xstage + NXB * ga.T * 128;                             // [NHB][SG][T][128] whole slices' partials
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   WsHeader* hdr = reinterpret_cast<WsHeader*>(a.ws);
@@ -572,275 +553,493 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
   Geo g = a.g;
   const long long lim = a.wait_ns;
   const int xwarp = (int)blockIdx.x * (4 * NGRP) + (warp - EPI_WARP0), nxwarps = (int)gridDim.x * (4 * NGRP);
-  const float xfirst = warp >= EPI_WARP0 ? load_x_block(a, g, xwarp) : 0.f;  // before the weight stream starts
+  const bool epi = warp >= EPI_WARP0 && warp < HELPER;
+  const float xfirst = epi ? load_x_block(a, g, xwarp) : 0.f;  // before the weight stream starts
+  int32_t pre_idx = 0;                                          // a given routing, fetched before the set-up
+  float pre_w = 0.f;
+  if (!a.wr && threadIdx.x < g.T * g.k) { pre_idx = a.idx[threadIdx.x]; pre_w = a.w[threadIdx.x]; }
+  if (warp < NPIPE && lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_gu) : "memory");
 
   float* lgw = reinterpret_cast<float*>(a.ws + a.L.lg);  // router logit halves [token][half][expert]
   if (a.wr && warp >= 2 && warp < 2 + 2 * NPIPE) {
     // routing, phase 1 (at entry, while thread 0 and warp 1 set the CTA up): the logit halves (expert e, half c),
     // task q = blockIdx.x + gridDim.x * (w + 2 NPIPE i), e = q / 2, c = q % 2, w = warp - 2, spread over the grid
-    for (int q = (int)blockIdx.x + (int)gridDim.x * (warp - 2); q < 2 * a.E; q += (int)gridDim.x * 2 * NPIPE) {
+    for (int q = (int)blockIdx.x + (int)gridDim.x * (warp - 2); q < 2 * g.E; q += (int)gridDim.x * 2 * NPIPE) {
       const int e = q >> 1, c = q & 1;
       float acc[kRouteTPC];
       route_half_logits<8>(a.wr + (size_t)e * g.H, g.H, g.T, [&](int t) { return a.x + (size_t)t * g.H; }, c, acc);
       if (lane == 0)
-        for (int t = 0; t < g.T; ++t) __stcg(lgw + (t * 2 + c) * a.E + e, acc[t]);
+        for (int t = 0; t < g.T; ++t) __stcg(lgw + (t * 2 + c) * g.E + e, acc[t]);
       __syncwarp();
       if (lane == 0) red_release_add(cnt + C_ROUTE, 1u);
     }
   }
-  __shared__ int32_t s_idx[MAX_T][MAX_K];
-  __shared__ float s_wt[MAX_T][MAX_K];
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < NSLOT; ++s) { mbar_init(&full[s], 2); mbar_init(&empty[s], 1); }  // full: both producers arrive
-    for (int j = 0; j < NPIPE; ++j) {
-      for (int b = 0; b < ABUF_MAX; ++b) {
-        mbar_init(&acc_full[j][b], 1);
-        mbar_init(&acc_empty[j][b], 4);  // the 4 warps of one epilogue group
-      }
-      mbar_init(&drain[j], 1);
-      for (int e = 0; e < QN; ++e) mbar_init(&uq_full[j][e], 1);
+  if (warp == 0) {  // barriers, initialised by the lanes of warp 0 in parallel
+    for (int s = lane; s < NSLOT; s += 32) { mbar_init(&S.full[s], 1); mbar_init(&S.empty[s], 1); }
+    for (int q = lane; q < NPIPE * 8; q += 32) {
+      mbar_init(&S.ucomp[q / 8][q % 8], 1);
+      mbar_init(&S.acc_empty[q / 8][q % 8], 4);  // the 4 warps of one epilogue group
     }
-    mbar_init(&xres_full, 1);
-    mbar_init(&tab_full, 1);
-    mbar_init(&tab2_full, 1);
-    s_abort = 0;
-    s_next = 0;
+    for (int q = lane; q < NPIPE * QN; q += 32) mbar_init(&S.uq_full[q / QN][q % QN], 1);
+    __syncwarp();  // before lane 0's fence below
+  }
+  if (threadIdx.x == 0) {
+    for (int j = 0; j < NPIPE; ++j) mbar_init(&S.drain[j], 1);
+    for (int b = 0; b < NHB; ++b) {
+      mbar_init(&S.hready[b], 1);
+      mbar_init(&S.hfree[b], g.NDL);       // one commit per local down unit of the slice
+      S.lcnt[b] = 0;
+    }
+    // ifree: one commit per down chunk of the slice (the helper arrives for the chunks other CTAs hold)
+    for (int b = 0; b < NIB; ++b) { mbar_init(&S.iready[b], 1); mbar_init(&S.ifree[b], g.NQ); }
+    for (int b = 0; b < NXB; ++b) { mbar_init(&S.xstaged[b], 1); mbar_init(&S.xfree[b], 1); }
+    mbar_init(&S.tab_full, 1);
+    mbar_init(&S.tab2_full, 1);
+    S.abort = 0;
+    S.next = 0;
     fence_mbar_init();
   }
-  if (warp == 1) tc_alloc(&s_tmem, TMEM_COLS);
+  if (warp == 1) tc_alloc(&S.tmem, TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tbase = s_tmem;
+  const uint32_t tbase = S.tmem;
+  Tables& tb = S.tb;
+
   if (warp >= EPI_WARP0) {
-    // this CTA's share of the x parts (independent of the routing), while the other warps route and build the
-    // tables; once every share is in, one thread copies the CTA's K segment of the image into the resident
-    // operand; then wait for the tables
-    split_x_global(a, g, xwarp, nxwarps, xfirst);
-    if (warp == EPI_WARP0) {  // (the other lanes wait at the warp barrier, not spinning beside lane 0)
+    // this CTA's share of the x parts (independent of the routing) while the other warps route and build the
+    // tables, then the token tables the epilogues need
+    if (epi) split_x_global(a, g, xwarp, nxwarps, xfirst, cnt);
+    if (!bwait(&S.tab_full, 0, s_abort, lim) && threadIdx.x == EPI_WARP0 * 32) record_error(&hdr->status, MOE_ERR_DEVICE_TIMEOUT);
+    if (warp == EPI_WARP0) {
       if (lane == 0) {
-        if (wait_ge(cnt + C_XP, (uint32_t)(g.T * g.KTG * 4), &s_abort, lim)) {
-          asm volatile("fence.proxy.async.global;" ::: "memory");  // generic-proxy writes -> bulk-copy reads
-          const int ks0 = (int)blockIdx.x % g.SG;
-          const uint8_t* xp = a.ws + a.L.xp;
-          mbar_arrive_expect_tx(&xres_full, (uint32_t)(g.KSG * (XRES_TILE + 512)));
-          bulk_g2s_plain(xres, xp + (int64_t)ks0 * g.KSG * XRES_TILE, (uint32_t)(g.KSG * XRES_TILE), &xres_full);
-          bulk_g2s_plain(xres_sf, xp + (int64_t)g.KTG * XRES_TILE + ks0 * g.KSG * 512, (uint32_t)(g.KSG * 512),
-                         &xres_full);
-        } else {
-          record_error(&hdr->status, MOE_ERR_DEVICE_TIMEOUT);
-        }
+        build_slots(tb, S.idx, S.wt, g.T, g.k);
+        mbar_arrive(&S.tab2_full);
       }
       __syncwarp();
     }
-    if (!bwait(&tab_full, 0, &s_abort, lim) && threadIdx.x == EPI_WARP0 * 32) record_error(&hdr->status, MOE_ERR_DEVICE_TIMEOUT);
-    if (warp == EPI_WARP0) {  // the token tables the epilogues need, while the first tiles stream in
-      if (lane == 0) {
-        build_slots(tb, s_idx, s_wt, g.T, g.k);
-        mbar_arrive(&tab2_full);
-      }
-      __syncwarp();
-    }
-    if (!bwait(&tab2_full, 0, &s_abort, lim) && threadIdx.x == EPI_WARP0 * 32) record_error(&hdr->status, MOE_ERR_DEVICE_TIMEOUT);
+    if (!bwait(&S.tab2_full, 0, s_abort, lim) && threadIdx.x == EPI_WARP0 * 32) record_error(&hdr->status, MOE_ERR_DEVICE_TIMEOUT);
   } else {
     if (a.wr) {
-      // routing, phase 2: every CTA selects each token's experts from all the logits (one warp per token)
-      if (warp < g.T) {
+      // routing, phase 2: every CTA selects each token's experts from all the logits (a warp per token)
+      for (int t = warp; t < g.T; t += EPI_WARP0) {
         bool ok = true;
-        if (lane == 0) ok = wait_ge(cnt + C_ROUTE, (uint32_t)(2 * a.E), &s_abort, lim);
+        if (lane == 0) ok = wait_ge(cnt + C_ROUTE, (uint32_t)(2 * g.E), s_abort, lim);
         ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
         int sid[8];
         float sw[8];
         if (ok) {
-          const float* row = lgw + warp * 2 * a.E;  // half 0, then half 1, of every expert's logit
-          route_topk_warp<kRouteMaxE / 32 / 4>([&](int e) { return __ldcg(row + e) + __ldcg(row + a.E + e); }, a.E, g.k,
+          const float* row = lgw + t * 2 * g.E;  // half 0, then half 1, of every expert's logit
+          route_topk_warp<kRouteMaxE / 32 / 4>([&](int e) { return __ldcg(row + e) + __ldcg(row + g.E + e); }, g.E, g.k,
                                                sid, sw);
         }
         if (lane == 0)
           for (int r = 0; r < g.k; ++r) {
-            s_idx[warp][r] = ok ? sid[r] : -1;
-            s_wt[warp][r] = ok ? sw[r] : 0.f;
+            S.idx[t][r] = ok ? sid[r] : -1;
+            S.wt[t][r] = ok ? sw[r] : 0.f;
             if (blockIdx.x == 0 && ok) {
-              a.idx_out[warp * g.k + r] = sid[r];
-              a.w_out[warp * g.k + r] = sw[r];
+              a.idx_out[t * g.k + r] = sid[r];
+              a.w_out[t * g.k + r] = sw[r];
             }
           }
       }
     } else if (threadIdx.x < g.T * g.k) {
-      s_idx[threadIdx.x / g.k][threadIdx.x % g.k] = a.idx[threadIdx.x];
-      s_wt[threadIdx.x / g.k][threadIdx.x % g.k] = a.w[threadIdx.x];
+      S.idx[threadIdx.x / g.k][threadIdx.x % g.k] = pre_idx;
+      S.wt[threadIdx.x / g.k][threadIdx.x % g.k] = pre_w;
     }
     named_bar(2 + NGRP, EPI_WARP0 * 32);
     if (warp == 0) {
-      build_union_warp(tb, s_idx, g.T, g.k, a.E);
-      __syncwarp();
-      const int U = tb.bad ? 0 : tb.U;
-      build_order_warp(ord, g, U);
+      build_union_warp(tb, S.idx, g.T, g.k, g.E);
       __syncwarp();
       if (lane == 0) {
         // an expert id out of range: no units (every role finds an empty queue), status MOE_ERR_INVALID_ARG
         if (tb.bad && blockIdx.x == 0) record_error(&hdr->status, MOE_ERR_INVALID_ARG);
-        s_units = U * (g.RTG * g.SG + g.RTD * g.SD);
-        mbar_arrive(&tab_full);
+        if (tb.bad) tb.U = 0;
+        mbar_arrive(&S.tab_full);
       }
     }
     named_bar(2 + NGRP, EPI_WARP0 * 32);
   }
-  g.U = tb.U;
-  g.nG = g.U * g.RTG * g.SG;
-  g.nD = g.U * g.RTD * g.SD;
-  const int nunits = s_units;
-  if (nunits == 0) g.nG = g.nD = 0;
-  // this CTA's units: v = blockIdx.x + i * gridDim.x, i = 0 .. my_units - 1 (G units first). Pipelines take the
-  // next i from a shared counter when they start a unit, so a pipeline waiting for h does not hold up the rest;
-  // each publishes the ids it took through its queue uq[j] to its MMA thread and epilogue group.
-  const int my_units = nunits > (int)blockIdx.x ? (nunits - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  make_schedule(g, tb.U);
+  const Mine mine = my_share(g, (int)blockIdx.x);
+  const int nunits = tb.U > 0 ? mine.n : 0;
 
-  if (warp < 2 * NPIPE) {
-    // ---------------- producers, two warps per pipeline j (lane 0 issues): warp j streams the weight tiles of
-    // every stage (no dependency, so weights keep flowing while activations are not ready), warp NPIPE + j adds
-    // the activation parts of each stage once they exist (x split done; h of the expert finalised). Each posts its
-    // own byte count on the stage's barrier.
-    const bool wprod = warp < NPIPE;
-    const int j = wprod ? warp : warp - NPIPE;
+  if (warp < NPIPE) {
+    // ---------------- producer of pipeline j = warp (lane 0 issues): the weights of every stage and, for gate/up
+    // stages, the stage's x parts, all counted on the stage's barrier
+    const int j = warp;
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       int n = 0;  // stages of this pipeline
-      bool ok = true;
-      int h_ok_u = -1;
+      bool ok = true, x_ok = false;
       for (int c = 0; ok; ++c) {
-        int i;
-        if (wprod) {
-          i = atomicAdd(&s_next, 1);
-          // entry c % QN was last read for unit c - QN: the weight producer is at most RING stages ahead of the
-          // MMA, so (units having at least 2 stages) the MMA has started unit c - 3 and the epilogue group has
-          // finished unit c - 3 - ABUF >= c - 7 > c - QN; the activation producer is ahead of the MMA
-          uq[j][c % QN] = i < my_units ? i : -1;
-          mbar_arrive(&uq_full[j][c % QN]);
-        } else {
-          if (!bwait(&uq_full[j][c % QN], (uint32_t)((c / QN) & 1), &s_abort, lim)) { ok = false; break; }
-          i = uq[j][c % QN];
-        }
-        if (i < 0 || i >= my_units) break;
-        const Unit un = unit_of((int)blockIdx.x + i * (int)gridDim.x, g, ord);
+        const int i = atomicAdd(&S.next, 1);
+        const Unit un = unit_at(g, mine, (int)blockIdx.x, i < nunits ? i : 0);
+        // entry c % QN was last read for unit c - QN, long consumed (the producer runs at most RING stages ahead of
+        // the MMA, the MMA at most UREG units ahead of the epilogue)
+        S.uq[j][c % QN] = i < nunits ? i : -1;
+        S.uqu[j][c % QN] = pack_unit(un);
+        mbar_arrive(&S.uq_full[j][c % QN]);
+        if (i >= nunits) break;
         const int e = tb.ue[un.u];
-        const int ks = un.d ? g.KSD : g.KSG;
-        const int KT = un.d ? g.KTD : g.KTG;
-        if (!wprod && un.d && h_ok_u != un.u * 16 + un.ks) {  // down: wait once for h of its K segment
-          const uint32_t* dep_cnt = cnt + C_HREADY + un.u * 16 + un.ks;
-          if (!wait_ge(dep_cnt, (uint32_t)(2 * g.KSD), &s_abort, lim)) { ok = false; break; }
-          asm volatile("fence.proxy.async.global;" ::: "memory");  // generic-proxy writes -> TMA reads
-          h_ok_u = un.u * 16 + un.ks;
-        }
-        for (int kk = 0; kk < ks; ++kk, ++n) {
-          const int slot = j * RING + (n % RING);
-          const uint32_t ph = (uint32_t)((n / RING) & 1);
-          if (!bwait(&empty[slot], ph ^ 1, &s_abort, lim)) { ok = false; break; }
+        const bool d = un.type >= U_DLOCAL;
+        const int nst = d ? (un.type == U_DLOCAL ? g.NC : 1) : g.KSG;
+        for (int kk = 0; kk < nst; ++kk, ++n) {
+          const int slot = j * g.RING + (n % g.RING);
+          const uint32_t ph = (uint32_t)((n / g.RING) & 1);
+          if (!bwait(&S.empty[slot], ph ^ 1, s_abort, lim)) { ok = false; break; }
           uint8_t* st = smem + slot * SLOT_BYTES;
-          const int kt = un.ks * ks + kk;
-          if (wprod) {
-            const int tile = un.rt * KT + kt;
-            const uint8_t* wbase = un.d ? a.dn + (int64_t)e * a.dn_stride : a.gu + (int64_t)e * a.gu_stride;
-            // weights are read once per call: evict-first keeps them from displacing the instructions, partial
-            // sums and activation parts that the dependent steps read back through L2
-            mbar_arrive_expect_tx(&full[slot], A_BYTES + 512);
-            tma_load_4d_hint(st, un.d ? &tm_dn : &tm_gu, 0, 0, tile, e, &full[slot], pol);
-            bulk_g2s(st + A_BYTES + B_BYTES, wbase + (int64_t)tile * kTcTileBytes + 8192, 512, &full[slot], pol);
-          } else if (!un.d) {
-            mbar_arrive(&full[slot]);  // gate/up: the x parts are resident; nothing to copy
-          } else {
-            mbar_arrive_expect_tx(&full[slot], B_BYTES + 512);
-            tma_load_2d(st + A_BYTES, &tm_h, kt * 64, un.u * HROWS, &full[slot]);
-            bulk_g2s_plain(st + A_BYTES + B_BYTES + 512, a.ws + a.L.hsf + ((int64_t)un.u * g.KTD + kt) * 512, 512,
-                           &full[slot]);
+          const uint32_t xbytes = d ? 0u : (uint32_t)(512 + 64 * g.W);
+          mbar_arrive_expect_tx(&S.full[slot], (uint32_t)kTcTileBytes + xbytes);
+          // weights are read once per call: evict-first keeps them from displacing what the dependent steps read
+          // back through L2
+          if (!d) {
+            const int tile = un.s * g.KTG + un.x * g.KSG + kk;
+            tma_load_4d_hint(st, &tm_gu, 0, 0, tile, e, &S.full[slot], pol);
+            bulk_g2s(st + SL_SFA, a.gu + (int64_t)e * a.gu_stride + (int64_t)tile * kTcTileBytes + 8192, 512,
+                     &S.full[slot], pol);
+            if (!x_ok) {  // the x image, built by the epilogue warps of the whole grid at entry
+              if (!wait_ge(cnt + C_XP, (uint32_t)(g.T * g.KTG * 4), s_abort, lim)) { ok = false; break; }
+              asm volatile("fence.proxy.async.global;" ::: "memory");  // generic-proxy writes -> bulk-copy reads
+              x_ok = true;
+            }
+            bulk_g2s_plain(st + SL_SFB, a.ws + a.L.ximg + (int64_t)(un.x * g.KSG + kk) * XIMG, xbytes, &S.full[slot]);
+          } else {  // a down chunk: codes (stored in the operand's swizzle) and exponents in one copy; its h is in
+                    // this CTA's shared memory
+            const int64_t ch = ((int64_t)e * g.NS + un.s) * g.NQ + un.x + kk;
+            bulk_g2s(st, a.dn + ch * kTcTileBytes, (uint32_t)kTcTileBytes, &S.full[slot], pol);
           }
         }
       }
       if (!ok) {
         record_error(&hdr->status, MOE_ERR_DEVICE_TIMEOUT);
-        // a stage may hold the copies of one producer only, so its barrier never completes: give the copies this
-        // warp issued 1 ms to land before the CTA's shared memory is released
+        // a stage may hold only the weight copy, so its barrier never completes: give the copies this warp issued
+        // 1 ms to land before the CTA's shared memory is released
         const long long t0 = globaltimer_ns();
         while (globaltimer_ns() - t0 < 1000000LL) __nanosleep(1000);
       }
     }
     __syncwarp();
-  } else if (warp < 3 * NPIPE) {
-    // ---------------- MMA issuers: lane 0 of warp 2 NPIPE + j, pipeline j
-    const int j = warp - 2 * NPIPE;
+  } else if (warp < 2 * NPIPE) {
+    // ---------------- MMA issuers: lane 0 of warp NPIPE + j, pipeline j
+    const int j = warp - NPIPE;
     if (lane == 0) {
-      int n = 0, c = 0;
-      bool ok = true, xres_ok = false;
-      const uint32_t sfa_col = tbase + SF_COL0;
-      for (;; ++c) {
-        if (!bwait(&uq_full[j][c % QN], (uint32_t)((c / QN) & 1), &s_abort, lim)) { ok = false; break; }
-        const int i = uq[j][c % QN];
+      int n = 0;
+      bool ok = true;
+      for (int c = 0; ok; ++c) {
+        if (!bwait(&S.uq_full[j][c % QN], (uint32_t)((c / QN) & 1), s_abort, lim)) { ok = false; break; }
+        const int i = S.uq[j][c % QN];
         if (i < 0) break;
-        const Unit un = unit_of((int)blockIdx.x + i * (int)gridDim.x, g, ord);
-        const int ab = c % g.ABUF;
-        if (!bwait(&acc_empty[j][ab], ((c / g.ABUF) & 1) ^ 1, &s_abort, lim)) { ok = false; break; }
+        const Unit un = unpack_unit(S.uqu[j][c % QN]);
+        const bool d = un.type >= U_DLOCAL;
+        const int nst = d ? (un.type == U_DLOCAL ? g.NC : 1) : g.KSG;
+        // the unit's accumulators: region c % UREG of the pipeline, W columns per accumulator (a down chunk has
+        // two: its two 128-row halves)
+        const int rg = c % g.UREG;
+        if (!bwait(&S.acc_empty[j][rg], (uint32_t)(((c / g.UREG) & 1) ^ 1), s_abort, lim)) { ok = false; break; }
+        const uint32_t acc0 = tbase + (uint32_t)(g.RC * (j * g.UREG + rg));
+        const int hb = un.li % NHB, ib = un.ib, kb = ib % NIB;
+        if (un.type == U_DLOCAL && !bwait(&S.hready[hb], (uint32_t)((un.li / NHB) & 1), s_abort, lim)) { ok = false; break; }
+        if (un.type == U_DIMPORT && !bwait(&S.iready[kb], (uint32_t)((ib / NIB) & 1), s_abort, lim)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t d_tmem = tbase + (uint32_t)(g.W * (j * g.ABUF + ab));
-        const int ks = un.d ? g.KSD : g.KSG;
-        if (!un.d && !xres_ok) {  // the resident x parts (built by the epilogue warps at start)
-          if (!bwait(&xres_full, 0, &s_abort, lim)) { ok = false; break; }
-          xres_ok = true;
-        }
-        for (int kk = 0; kk < ks; ++kk, ++n) {
-          const int slot = j * RING + (n % RING);
-          if (!bwait(&full[slot], (uint32_t)((n / RING) & 1), &s_abort, lim)) { ok = false; break; }
+        uint32_t sfb_unit = 0;  // down units: the h exponents, copied into the first stage's columns once
+        for (int kk = 0; kk < nst; ++kk, ++n) {
+          const int slot = j * g.RING + (n % g.RING);
+          if (!bwait(&S.full[slot], (uint32_t)((n / g.RING) & 1), s_abort, lim)) { ok = false; break; }
           tc_fence_after();
           uint8_t* st = smem + slot * SLOT_BYTES;
-          const uint32_t sfa = sfa_col + (uint32_t)(slot * 8), sfbc = sfa + 4;
-          // B: gate/up from the resident x parts (k-tile kk of the CTA's segment), down from the stage
-          const uint8_t* bsrc = un.d ? st + A_BYTES : xres + kk * XRES_TILE;
-          const uint8_t* bsf = un.d ? st + A_BYTES + B_BYTES + 512 : xres_sf + kk * 512;
-          tc_cp_sf(sfa, umma_desc_sf(smem_u32(st + A_BYTES + B_BYTES)));
-          tc_cp_sf(sfbc, umma_desc_sf(smem_u32(bsf)));
-          const uint64_t ad = umma_desc_sw64(smem_u32(st)), bd = umma_desc_sw64(smem_u32(bsrc));
+          const uint32_t sfa = tbase + SF_COL0 + (uint32_t)(slot * 8);
+          uint32_t sfbc = sfa + 4;
+          // activation image [512 B exponents][codes]: x in the stage, h of the slice in this CTA's buffers
+          const uint8_t* bimg = un.type == U_DLOCAL ? hbuf + hb * HIMG : (un.type == U_DIMPORT ? ibuf + kb * HIMG : st + SL_SFB);
+          tc_cp_sf(sfa, umma_desc_sf(smem_u32(st + SL_SFA)));
+          if (!d || kk == 0) {
+            tc_cp_sf(sfbc, umma_desc_sf(smem_u32(bimg)));
+            sfb_unit = sfbc;
+          } else {
+            sfbc = sfb_unit;  // that stage's slot is reused only RING >= 3 stages later
+          }
+          if (!d) {
+            // gate/up tile: two K = 64 halves, scale bytes (0, 1) and (2, 3) of A and B
+            const uint64_t ad = umma_desc_sw64(smem_u32(st)), bd = umma_desc_sw64(smem_u32(bimg + 512));
 #pragma unroll
-          for (int kh = 0; kh < 2; ++kh)  // two K = 64 halves of the 128-column tile, scale bytes 2kh, 2kh + 1
-            tc_mma_mxf4(d_tmem, ad + 2 * kh, bd + 2 * kh, idesc_mxf4(128, (uint32_t)g.W, 2 * kh), sfa, sfbc, (kk | kh) != 0);
-          tc_commit(&empty[slot]);
+            for (int kh = 0; kh < 2; ++kh)
+              tc_mma_mxf4(acc0, ad + 2 * kh, bd + 2 * kh, idesc_mxf4_ab((uint32_t)g.W, 2 * kh, 2 * kh), sfa, sfbc,
+                          (kk | kh) != 0);
+          } else {
+            // down chunk: rows 0..127 and 128..255 (A scale bytes (0, 1) and (2, 3)) times the slice's h (K = 64)
+            const uint64_t bd = umma_desc_sw32(smem_u32(bimg + 512));
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              tc_mma_mxf4(acc0 + (uint32_t)(g.W * (2 * kk + h)), umma_desc_sw32(smem_u32(st + 4096 * h)), bd,
+                          idesc_mxf4_ab((uint32_t)g.W, 2 * h, 0), sfa, sfbc, 0);
+          }
+          tc_commit(&S.empty[slot]);
         }
-        if (ok) tc_commit(&acc_full[j][ab]);
+        if (!ok) break;
+        // one completion per unit (a commit costs its issuing thread a few hundred cycles): the epilogue drains all
+        // the unit's accumulators on it. An h buffer that a later slice reuses is released once every chunk that
+        // reads it has been multiplied.
+        tc_commit(&S.ucomp[j][c % 8]);
+        if (un.type == U_DLOCAL && un.li + NHB < g.nw) tc_commit(&S.hfree[hb]);
+        if (un.type == U_DIMPORT && ib + NIB < mine.nis) tc_commit(&S.ifree[kb]);
       }
       if (!ok) record_error(&hdr->status, MOE_ERR_DEVICE_TIMEOUT);
-      tc_commit(&drain[j]);
-      mbar_wait(&drain[j], 0, 100000000LL);
+      tc_commit(&S.drain[j]);
+      mbar_wait(&S.drain[j], 0, 100000000LL);
     }
     __syncwarp();
+  } else if (warp == HELPER) {
+    // ---------------- helper: export partials staged by the epilogue groups -> global memory, counted per split
+    // slice (the store, fence and count wait on global memory, so they are kept off the epilogue groups); then the
+    // h of each slice this CTA imports, from the counted partials, into the import buffers
+    float* gpart = reinterpret_cast<float*>(a.ws + a.L.gpart);
+    bool ok = true;
+    for (int i = 0; i < (nunits ? mine.ne : 0) && ok; ++i) {
+      const int k = i % NXB;
+      int w = 1;
+      if (lane == 0) w = bwait(&S.xstaged[k], (uint32_t)((i / NXB) & 1), s_abort, lim) ? 1 : 0;
+      if (!__shfl_sync(0xFFFFFFFFu, w, 0)) { ok = false; break; }
+      const Unit un = unit_at(g, mine, (int)blockIdx.x, export_pos(g, i));
+      const float* src = xstage + k * g.T * 128;
+      float* dst = gpart + ((int64_t)un.li * g.SG + un.x) * a.ts * 128;
+      for (int t = 0; t < g.T; ++t)
+        reinterpret_cast<float4*>(dst + t * 128)[lane] = reinterpret_cast<const float4*>(src + t * 128)[lane];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.xfree[k]);
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) red_release_add(cnt + C_SPLIT + un.li, 1u);
+    }
+    for (int ib = 0; ib < (nunits ? mine.nis : 0) && ok; ++ib) {
+      const int kb = ib % NIB;
+      const int li = mine.a0 / g.NQ + ib, z = g.Zw + li, u = z / g.NS;
+      int w = 1;
+      if (lane == 0) {
+        // the buffer's previous slice must be done with it, and every segment of this one stored
+        if (ib >= NIB) w = bwait(&S.ifree[kb], (uint32_t)(((ib / NIB) - 1) & 1), s_abort, lim) ? 1 : 0;
+        if (w) w = wait_ge(cnt + C_SPLIT + li, (uint32_t)g.SG, s_abort, lim) ? 1 : 0;
+      }
+      if (!__shfl_sync(0xFFFFFFFFu, w, 0)) { ok = false; break; }
+      finalize_import(gpart + (int64_t)li * g.SG * a.ts * 128, (int64_t)a.ts * 128, g.SG, tb.ntok[u], tb.tok[u], g.W,
+                      ibuf + kb * HIMG);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> the MMA's reads
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&S.iready[kb]);
+        const int lo = mine.a0 > li * g.NQ ? mine.a0 : li * g.NQ;
+        const int hi = mine.a0 + mine.nimp < (li + 1) * g.NQ ? mine.a0 + mine.nimp : (li + 1) * g.NQ;
+        if (ib + NIB < mine.nis && g.NQ - (hi - lo) > 0) mbar_arrive_n(&S.ifree[kb], (uint32_t)(g.NQ - (hi - lo)));
+      }
+    }
+    if (!ok && lane == 0) record_error(&hdr->status, MOE_ERR_DEVICE_TIMEOUT);
   } else {
-    // ---------------- epilogue warps (the resident x parts are done)
-    epilogue(a, g, tb, ord, tbase, acc_full, acc_empty, uq_full, uq, cnt, s_last, s_ok, s_unit, &s_abort);
+    // ---------------- epilogue group j (warps EPI_WARP0 + 4 j ..): drains pipeline j's accumulators in order
+    const int q = warp & 3;
+    const int grp = (warp - EPI_WARP0) / 4, j = grp;
+    const int bar = 1 + grp;                                   // named barrier of the group
+    const int et = threadIdx.x - (EPI_WARP0 + 4 * grp) * 32;    // 0..127 inside the group
+    const int m = q * 32 + lane;                                // TMEM lane = weight row of the tile
+    float* dpart = reinterpret_cast<float*>(a.ws + a.L.dpart);
+    int bc = 0;
+    // thread et == 0 waits and shares the verdict with its group: two flag slots used in turn, so a slot is
+    // rewritten only after every thread has passed the barrier that follows its last read
+    auto shared_ok = [&](int v) -> int {
+      const int sl = bc++ & 1;
+      if (et == 0) S.ok[grp][sl] = v;
+      named_bar(bar, 128);
+      return S.ok[grp][sl];
+    };
+    for (int c = 0;; ++c) {
+      int st = 0;
+      if (et == 0 && bwait(&S.uq_full[j][c % QN], (uint32_t)((c / QN) & 1), s_abort, lim)) {
+        const int i = S.uq[j][c % QN];
+        st = i < 0 ? 2 : 1;
+        S.unit[grp] = i;
+      }
+      if (shared_ok(st) != 1) break;
+      const int ui = S.unit[grp];
+      const Unit un = unpack_unit(S.uqu[j][c % QN]);
+      const bool d = un.type >= U_DLOCAL;
+      const int nt = tb.ntok[un.u];
+      const int nuse = d ? 2 * (un.type == U_DLOCAL ? g.NC : 1) : 1;
+      bool good = true;
+      if (!shared_ok(et != 0 || bwait(&S.ucomp[j][c % 8], (uint32_t)((c / 8) & 1), s_abort, lim))) break;
+      tc_fence_after();
+      const uint32_t rbase = tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)(g.RC * (j * g.UREG + c % g.UREG));
+      // what accumulator h of the unit goes to (its token or slot values acc[]); false if a wait gave up
+      auto put = [&](int h, const float (&acc)[TT]) -> bool {
+        if (un.type == U_EXPORT) {  // staged by token for the helper warp, which stores and counts it
+          const int xo = ui - export_pos(g, 0), k = xo % NXB;
+          if (xo >= NXB && !shared_ok(et != 0 || bwait(&S.xfree[k], (uint32_t)(((xo / NXB) - 1) & 1), s_abort, lim)))
+            return false;
+          float* xp = xstage + k * g.T * 128 + m;
+#pragma unroll
+          for (int t = 0; t < TT; ++t)
+            if (t < g.T) xp[t * 128] = acc[t];
+          named_bar(bar, 128);
+          if (et == 0) mbar_arrive(&S.xstaged[k]);
+        } else if (un.type == U_LOCAL) {
+          const int hb = un.li % NHB;
+          // the buffer's previous slice must be finished with it (normally long since)
+          if (un.li >= NHB &&
+              !shared_ok(et != 0 || bwait(&S.hready[hb], (uint32_t)(((un.li / NHB) - 1) & 1), s_abort, lim)))
+            return false;
+          float* sp = spart + ((int64_t)hb * g.SG + un.x) * g.T * 128 + m;
+#pragma unroll
+          for (int t = 0; t < TT; ++t)
+            if (t < g.T) sp[t * 128] = acc[t];
+        } else {
+          // chunk un.x + h / 2, rows 256 q + 128 (h % 2) + m; the partial goes to column (expert, slot), 32-row
+          // group, slice, row in the group
+          const int row = 256 * (un.x + (h >> 1)) + 128 * (h & 1) + m;
+          float* dp = dpart + ((((int64_t)tb.col0[un.u]) * (g.H / 32) + row / 32) * g.NS + un.s) * 32 + (row & 31);
+#pragma unroll
+          for (int s = 0; s < TT; ++s)
+            if (s < nt) dp[(int64_t)s * (g.H / 32) * g.NS * 32] = acc[s];
+        }
+        return true;
+      };
+      // drain the unit's accumulators (W columns each; column 6 t + p = part p of token or slot t, summed in part
+      // order): two at a time with one wait when W = 16; the region is handed back after its last load
+      const int hstep = g.W == 16 ? 2 : 1;
+      for (int h0 = 0; h0 < nuse && good; h0 += hstep) {
+        const int nh = nuse - h0 < hstep ? nuse - h0 : hstep;
+        float acc0[TT], acc1[TT];
+#pragma unroll
+        for (int t = 0; t < TT; ++t) { acc0[t] = 0.f; acc1[t] = 0.f; }
+        if (g.W == 16) {
+          uint32_t v0[16], v1[16];
+          tc_ld16(rbase + 16 * h0, v0);
+          if (nh == 2) tc_ld16(rbase + 16 * h0 + 16, v1);
+          tc_wait_ld();
+#pragma unroll
+          for (int cc = 0; cc < 16; ++cc)
+            if (cc / PARTS < TT) acc0[cc / PARTS] += __uint_as_float(v0[cc]);
+          if (nh == 2)
+#pragma unroll
+            for (int cc = 0; cc < 16; ++cc)
+              if (cc / PARTS < TT) acc1[cc / PARTS] += __uint_as_float(v1[cc]);
+        } else {
+#pragma unroll
+          for (int cb = 0; cb < WMAX / 16; ++cb) {
+            if (16 * cb >= g.W) break;
+            uint32_t v[16];
+            tc_ld16(rbase + g.W * h0 + 16 * cb, v);
+            tc_wait_ld();
+#pragma unroll
+            for (int cc = 0; cc < 16; ++cc)
+              if ((16 * cb + cc) / PARTS < TT) acc0[(16 * cb + cc) / PARTS] += __uint_as_float(v[cc]);
+          }
+        }
+        if (h0 + nh == nuse) {  // TMEM reads done; no wait for earlier global stores
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_relaxed(&S.acc_empty[j][c % g.UREG]);
+        }
+        if (!put(h0, acc0)) good = false;
+        else if (nh == 2 && !put(h0 + 1, acc1)) good = false;
+      }
+      if (!good) break;
+      if (un.type == U_LOCAL) {
+        // count the segment; the one completing the slice forms its h in this CTA's shared memory
+        const int hb = un.li % NHB;
+        __threadfence_block();
+        named_bar(bar, 128);
+        if (et == 0) {
+          const int old = atomicAdd(&S.lcnt[hb], 1);
+          __threadfence_block();
+          S.last[grp] = old == g.SG - 1 ? 1 : 0;
+        }
+        named_bar(bar, 128);
+        if (S.last[grp]) {
+          // the previous slice of this buffer: its down MMAs must be done reading it
+          if (un.li >= NHB &&
+              !shared_ok(et != 0 || bwait(&S.hfree[hb], (uint32_t)(((un.li / NHB) - 1) & 1), s_abort, lim)))
+            break;
+          finalize_local(spart + (int64_t)hb * g.SG * g.T * 128, (int64_t)g.T * 128, g.SG, nt, tb.tok[un.u], g.W,
+                         hbuf + hb * HIMG, et);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> the MMA's reads
+          named_bar(bar, 128);
+          if (et == 0) { S.lcnt[hb] = 0; mbar_arrive(&S.hready[hb]); }
+        }
+      }
+    }
+    __threadfence();  // the down partials are visible grid-wide before this CTA arrives at the grid barrier
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tc_dealloc(tbase, TMEM_COLS);
+
+  // ---------------- grid barrier, then this CTA's share of the outputs: y[t][32 jb + l] = sum_r w[t, r] *
+  // (sum over the slices of expert pu[t][r], in order, of the partial), ranks in order. One warp per
+  // (t, jb, r) task (lane l = row), the rank sums meet in shared memory.
+  if (tb.U > 0) {
+    if (threadIdx.x == 0) {
+      red_release_add(&hdr->gbar, 1u);
+      S.gok = wait_ge(&hdr->gbar, gridDim.x, s_abort, lim) ? 1 : 0;
+      if (!S.gok) record_error(&hdr->status, MOE_ERR_DEVICE_TIMEOUT);
+    }
+    __syncthreads();
+    if (S.gok && !*s_abort) {
+      const int nb32 = g.H / 32, ntask = g.T * nb32;
+      const int nmine = ntask > (int)blockIdx.x ? (ntask - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+      float* sd = reinterpret_cast<float*>(smem);  // [nmine][k][32] (the stage ring is idle now)
+      const float* dpart = reinterpret_cast<const float*>(a.ws + a.L.dpart);
+      for (int tk = warp; tk < nmine * g.k; tk += THREADS / 32) {
+        const int ln = tk / g.k, r = tk % g.k, task = (int)blockIdx.x + ln * (int)gridDim.x;
+        const int t = task / nb32, jb = task % nb32;
+        const int u = tb.pu[t][r];
+        const int col = tb.col0[u] + tb.ps[t][r];
+        const float* p = dpart + (((int64_t)col * nb32 + jb) * g.NS) * 32 + lane;
+        float sum = 0.f;
+        for (int s0 = 0; s0 < g.NS; s0 += 32) {  // slices in order, loads issued 32 at a time
+          float v[32];
+#pragma unroll
+          for (int qq = 0; qq < 32; ++qq) v[qq] = s0 + qq < g.NS ? __ldcg(p + (int64_t)(s0 + qq) * 32) : 0.f;
+#pragma unroll
+          for (int qq = 0; qq < 32; ++qq)
+            if (s0 + qq < g.NS) sum += v[qq];
+        }
+        sd[(ln * MAX_K + r) * 32 + lane] = sum;
+      }
+      __syncthreads();
+      for (int o = threadIdx.x; o < nmine * 32; o += THREADS) {
+        const int ln = o >> 5, l = o & 31, task = (int)blockIdx.x + ln * (int)gridDim.x;
+        const int t = task / nb32, jb = task % nb32;
+        float acc = 0.f;
+        for (int r = 0; r < g.k; ++r) acc = fmaf(tb.w[t][r], sd[(ln * MAX_K + r) * 32 + l], acc);
+        const int64_t yi = (int64_t)t * g.H + 32 * jb + l;
+        const float out = a.accumulate ? a.y[yi] + acc : acc;
+        a.y[yi] = out;
+        if (a.yb) a.yb[yi] = __float2bfloat16_rn(out);
+      }
+    }
+  }
   // the last CTA to finish resets the per-call counters
   if (threadIdx.x == 0) {
     __threadfence();
-    const uint32_t old = atomicAdd(cnt + C_DONE, 1u);
+    const uint32_t old = atomicAdd(&hdr->done, 1u);
     if (old == gridDim.x - 1) {
       __threadfence();
-      for (int q = 0; q < tb.U * 16; ++q) cnt[C_HREADY + q] = 0;
-      for (int q = 0; q < tb.U * g.RTG; ++q) cnt[C_G + q] = 0;
-      for (int q = 0; q < g.RTD; ++q) cnt[C_D + q] = 0;
-      cnt[C_ROUTE] = 0;
+      for (int r = 0; r < g.R; ++r) cnt[C_SPLIT + r] = 0;
       cnt[C_XP] = 0;
+      cnt[C_ROUTE] = 0;
+      hdr->gbar = 0;
       __threadfence();
-      cnt[C_DONE] = 0;
+      hdr->done = 0;
     }
   }
 }
 
 // ------------------------------------------------------------------ host side
-inline int64_t umax_of(int T, int k) { return (int64_t)(T * k < MAX_U ? T * k : MAX_U); }
+inline int64_t cols_of(int T, int k) { return (int64_t)(T * k < MAX_U ? T * k : MAX_U); }
 
 size_t workspace_bytes(const moe_layer_t* L, int T_max, int k) {
-  return (size_t)ws_layout(L->H, L->I, umax_of(T_max, k), T_max).total;
+  return (size_t)ws_layout(L->H, L->I, cols_of(T_max, k), T_max).total;
 }
+
 
 // The caller (ffn.cu) has checked pointers, T in [1, 8], k in [1, 8], the shape and the device.
 moe_status_t run(const moe_layer_t* L, const void* x, int T, const int32_t* idx, const float* w, int k, float* y,
@@ -854,6 +1053,10 @@ moe_status_t run(const moe_layer_t* L, const void* x, int T, const int32_t* idx,
     if (ws_bytes >= workspace_bytes(L, tm, k)) { tmax = tm; break; }
   if (!tmax) return MOE_ERR_WORKSPACE_TOO_SMALL;
   if (!moe_internal::tmap_available()) return MOE_ERR_CUDA;
+  if (router_w && (L->E > kRouteMaxE / 4 || k > L->E || ((uintptr_t)x & 15) || ((uintptr_t)router_w & 15)))
+    return router_w && L->E > kRouteMaxE / 4 ? MOE_ERR_SHAPE : MOE_ERR_INVALID_ARG;
+  const int nsm = moe_internal::num_sms();
+  if (nsm <= 0 || nsm > RMAX) return MOE_ERR_CUDA;
   Args a;
   a.gu = (const uint8_t*)L->gate_up;
   a.dn = (const uint8_t*)L->down;
@@ -865,50 +1068,63 @@ moe_status_t run(const moe_layer_t* L, const void* x, int T, const int32_t* idx,
   a.wr = (const uint16_t*)router_w;
   a.idx_out = idx_out;
   a.w_out = w_out;
-  if (router_w && (L->E > kRouteMaxE / 4 || k > L->E || ((uintptr_t)x & 15) || ((uintptr_t)router_w & 15)))
-    return router_w && L->E > kRouteMaxE / 4 ? MOE_ERR_SHAPE : MOE_ERR_INVALID_ARG;
   a.y = y;
   a.yb = (__nv_bfloat16*)y_bf16;
   a.accumulate = accumulate;
-  a.E = L->E;
   a.ws = (uint8_t*)ws;
-  const int64_t umax = umax_of(tmax, k);
-  a.L = ws_layout(L->H, L->I, umax, tmax);
+  a.L = ws_layout(L->H, L->I, cols_of(tmax, k), tmax);
   a.ts = tmax;
   a.wait_ns = kDefaultWaitNs;
   Geo& g = a.g;
-  g.H = L->H; g.I = L->I; g.T = T; g.k = k; g.U = 0;
-  g.RTG = 2 * L->I / 128; g.KTG = L->H / 128; g.KSG = ks_for_g(g.KTG); g.SG = g.KTG / g.KSG;
-  g.RTD = L->H / 128;     g.KTD = L->I / 128; g.KSD = ks_for_d(g.KTD); g.SD = g.KTD / g.KSD;
-  g.nG = g.nD = 0;
+  g = Geo{};
+  g.H = L->H; g.I = L->I; g.T = T; g.k = k; g.E = L->E;
   g.W = 16 * ((PARTS * T + 15) / 16);
-  g.ABUF = g.W <= 32 ? 4 : 2;
-  if (NPIPE * g.ABUF * g.W > (int)SF_COL0) return MOE_ERR_SHAPE;
-  CUtensorMap mgu, mdn, mh;
-  const uint64_t hd[2] = {(uint64_t)L->I / 2, (uint64_t)(umax * HROWS)}, hs[1] = {(uint64_t)L->I / 2};
-  const uint32_t hbox[2] = {64, HROWS};
-  if (!moe_internal::tmap_tc_weights_packed(&mgu, L->gate_up, MOE_MAT_GATE_UP, L->H, L->I, L->E) ||
-      !moe_internal::tmap_tc_weights_packed(&mdn, L->down, MOE_MAT_DOWN, L->H, L->I, L->E) ||
-      !moe_internal::tmap_u8(&mh, a.ws + a.L.hb, 2, hd, hs, hbox, 64))
-    return MOE_ERR_CUDA;
+  g.NS = L->I / 64; g.NQ = L->H / 256; g.KTG = L->H / 128; g.SG = sg_for(g.KTG); g.KSG = g.KTG / g.SG;
+  // TMEM: every unit of a pipeline takes one accumulator region; a local down unit of NC chunks needs 2 NC
+  // accumulators of W columns. Two chunks per unit when two such regions still fit in a pipeline's share.
+  const int share = (int)SF_COL0 / NPIPE;
+  g.NC = (share >= 2 * (2 * NC_MAX * g.W) && g.NQ % NC_MAX == 0) ? NC_MAX : 1;
+  g.NDL = g.NQ / g.NC;
+  g.RC = 2 * g.NC * g.W;
+  g.UREG = share / g.RC < 8 ? share / g.RC : 8;
+  g.G = nsm;
+  if (g.SG > MAX_SG || g.UREG < 1) return MOE_ERR_SHAPE;
+  static int smem_max = 0, static_smem = 0;
+  if (!smem_max) {
+    int dev = 0, v = 0;
+    cudaFuncAttributes fa2, fa8;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        cudaFuncGetAttributes(&fa2, decode_kernel<2>) != cudaSuccess || cudaFuncGetAttributes(&fa8, decode_kernel<8>) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    static_smem = (int)(fa2.sharedSizeBytes > fa8.sharedSizeBytes ? fa2.sharedSizeBytes : fa8.sharedSizeBytes);
+    smem_max = v;
+  }
+  g.RING = (int)smem_bytes(T, g.SG, RING_MAX) + static_smem <= smem_max ? RING_MAX : 3;
+  if ((int)smem_bytes(T, g.SG, g.RING) + static_smem > smem_max) return MOE_ERR_SHAPE;
+  CUtensorMap mgu;
+  if (!moe_internal::tmap_tc_weights_packed(&mgu, L->gate_up, MOE_MAT_GATE_UP, L->H, L->I, L->E)) return MOE_ERR_CUDA;
+  const size_t smem = smem_bytes(T, g.SG, g.RING);
   static std::once_flag once;
   static bool attr_ok = false;
   std::call_once(once, [] {
-    attr_ok = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) == cudaSuccess;
+    attr_ok = cudaFuncSetAttribute(decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   smem_max - static_smem) == cudaSuccess &&
+              cudaFuncSetAttribute(decode_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   smem_max - static_smem) == cudaSuccess;
   });
   if (!attr_ok) return MOE_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
-  const int nsm = moe_internal::num_sms();
-  cfg.gridDim = dim3(nsm - nsm % g.SG);  // a multiple of S_G: every gate/up unit of a CTA has the same K segment
+  cfg.gridDim = dim3(nsm);
   cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = SMEM;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = (cudaStream_t)stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, decode_kernel, mgu, mdn, mh, a) != cudaSuccess) return MOE_ERR_CUDA;
+  const cudaError_t le = T <= 2 ? cudaLaunchKernelEx(&cfg, decode_kernel<2>, mgu, a) : cudaLaunchKernelEx(&cfg, decode_kernel<8>, mgu, a);
+  if (le != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }
 

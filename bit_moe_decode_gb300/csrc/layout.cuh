@@ -72,23 +72,30 @@ __host__ __device__ inline CodePos code_pos(int fmt, int tr, int k) {
 }
 
 // ---- MOE_LAYOUT_TC (MXFP4; operands of the block-scaled tcgen05 MMA, used by prefill, decode and verify)
-// A matrix of R rows x K per expert is cut into 128 x 128 tiles, stored tile-major (row tile rt, then column
-// tile kt); every tile is one contiguous run of 8704 bytes:
-//   codes  [128 rows][64 B]: element k of a row in byte k/2, even k in the LOW nibble (the order in which the TMA
-//          engine's 16U4_ALIGN16B type unpacks E2M1 codes into the MMA's shared-memory operand);
-//   scales [512 B] at +8192: the 4 x 128 E8M0 exponents permuted so that byte (l*16 + c*4 + kb) is the exponent of
-//          tile row (l + 32c), 32-block kb; tcgen05.cp .32x128b.warpx4 copies it into four TMEM scale columns.
-// One pipeline stage of the GEMM kernels reads exactly one tile, so weight reads are 8.5 KB sequential runs.
-//   GATE_UP: R = 2I, K = H; row tile b = gate rows 64b..64b+63 followed by up rows 64b..64b+63, so one
-//            128-column accumulator tile holds g and u of the same 64 intermediate indices.
-//   DOWN:    R = H, K = I.
+// Codes hold element k of a row in byte k/2 of the row's run, even k in the LOW nibble (the order in which the TMA
+// engine's 16U4_ALIGN16B type unpacks E2M1 codes into the MMA's shared-memory operand, and the order kind::mxf4
+// reads packed codes in). Every storage unit is one contiguous run of 8704 bytes: 8192 bytes of codes, then a
+// 512-byte block of E8M0 exponents permuted for tcgen05.cp .32x128b.warpx4 (byte l*16 + c*4 + b feeds TMEM lane l,
+// column c, byte b; the MMA reads row m of a 128-row operand from lane m % 32, column m / 32).
+//   GATE_UP (R = 2I rows, K = H): 128 x 128 TILES in (row tile rt, column tile kt) order. Tile rows are 64 gate
+//            rows 64rt..64rt+63 followed by the same 64 up rows, so one accumulator holds g and u of the same 64
+//            intermediate indices (a SLICE). Codes [128 rows][64 B]; exponent byte b = 32-block b of the tile.
+//   DOWN     (R = H rows, K = I): CHUNKS of 256 rows x 64 columns in (slice s = k / 64, row pair q = r / 256)
+//            order: the 64 columns of a chunk are exactly the intermediate indices of one gate/up slice, so the
+//            down projection of a slice reads whole chunks. Codes [256 rows][32 B], stored already in the
+//            32-byte swizzle of the MMA's shared-memory operand (16-byte half h of row r at half h ^ ((r >> 2) & 1)),
+//            so one plain bulk copy of the whole 8704-byte chunk lands a ready operand; exponent byte b holds row
+//            tile (256q + 128(b / 2) + ..) and 32-block b % 2 of the slice: the two 128-row halves of a chunk are two
+//            MMAs that select scale bytes (0, 1) and (2, 3).
 // The per-expert stride R*K*17/32 equals the canonical size (same bits per weight).
 constexpr int64_t kTcTileBytes = 8704;
 struct TcGeom {
-  int64_t R, K, RT, KT, stride;  // rows, columns, row tiles, column tiles, bytes per expert
+  int64_t R, K, RT, KT, stride;  // rows, columns, row tiles (128 rows), column tiles (128 columns), bytes per expert
+  int kind;
 };
 __host__ __device__ inline TcGeom tc_geom(int kind, int64_t H, int64_t I) {
   TcGeom g;
+  g.kind = kind;
   g.R = kind == MOE_MAT_GATE_UP ? 2 * I : H;
   g.K = kind == MOE_MAT_GATE_UP ? H : I;
   g.RT = g.R / 128;
@@ -101,17 +108,21 @@ __host__ __device__ inline int64_t tc_row(int kind, int mi, int64_t row) {
   if (kind != MOE_MAT_GATE_UP) return row;
   return (row / 64) * 128 + mi * 64 + row % 64;
 }
-// byte offset (inside one expert) of the tile holding storage row r, column k
+// byte offset (inside one expert) of the run holding storage row r, column k
 __host__ __device__ inline int64_t tc_tile_off(const TcGeom& g, int64_t r, int64_t k) {
+  if (g.kind == MOE_MAT_DOWN) return ((k / 64) * (g.R / 256) + r / 256) * kTcTileBytes;
   return ((r / 128) * g.KT + k / 128) * kTcTileBytes;
 }
 // byte offset of the code byte of (storage row r, column k) and of the exponent of (r, 32-block of k)
 __host__ __device__ inline int64_t tc_code_off(const TcGeom& g, int64_t r, int64_t k) {
+  if (g.kind == MOE_MAT_DOWN)
+    return tc_tile_off(g, r, k) + (r % 256) * 32 + ((((k % 64) / 32) ^ ((r >> 2) & 1)) << 4) + (k % 32) / 2;
   return tc_tile_off(g, r, k) + (r % 128) * 64 + (k % 128) / 2;
 }
 __host__ __device__ inline int64_t tc_scale_off(const TcGeom& g, int64_t r, int64_t k) {
-  const int64_t rr = r % 128, kb = (k % 128) / 32;
-  return tc_tile_off(g, r, k) + 8192 + (rr % 32) * 16 + (rr / 32) * 4 + kb;
+  const int64_t rr = r % 128;
+  const int64_t b = g.kind == MOE_MAT_DOWN ? 2 * ((r % 256) / 128) + (k % 64) / 32 : (k % 128) / 32;
+  return tc_tile_off(g, r, k) + 8192 + (rr % 32) * 16 + (rr / 32) * 4 + b;
 }
 
 }  // namespace moe

@@ -30,21 +30,33 @@ namespace pf {
 constexpr int BM = 128;       // tokens per tile: MMA M, TMEM lanes
 constexpr int BN = 128;       // weight rows per unit: MMA N, accumulator columns
 constexpr int BK = 128;       // K per pipeline stage (4 MMAs of K = 32)
-constexpr int STAGES = 6;
 constexpr int A_BYTES = BM * BK;          // E4M3 activations, 16 KB
 constexpr int B_BYTES = BN * BK;          // E2M1 weights as unpacked into shared memory (one byte per code)
 constexpr int B_TX = BN * BK / 2;         // bytes the TMA engine reads for them
 constexpr int SF_BYTES = 512;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES + 2 * SF_BYTES;  // 33 KB, a multiple of 1024
-constexpr uint32_t STAGE_TX = A_BYTES + B_TX + 2 * SF_BYTES;
+// A stage: codes of A and B, then the exponent blocks of A and of B. Gate/up: B is one 128 x 128 weight tile, loaded
+// by the TMA engine's 16U4 unpacking. Down: the stage's 128 columns are two 64-column chunks of the DOWN layout
+// (each with its own exponent block); their packed codes are bulk-copied into a staging area and expanded by four
+// converter warps into the same padded, 128-byte-swizzled operand (the unpacking TMA only takes 128-code boxes).
+constexpr int SF_OFF = A_BYTES + B_BYTES;            // exponents: A, B (chunk 0), B (chunk 1)
+constexpr int STAGING_OFF = SF_OFF + 4 * SF_BYTES;   // down only: the two chunks' packed codes, 2 x 4 KB
+template <int PHASE> struct StageCfg;
+template <> struct StageCfg<0> { static constexpr int STAGES = 6, BYTES = SF_OFF + 2 * SF_BYTES; };   // 33 KB
+template <> struct StageCfg<1> { static constexpr int STAGES = 5, BYTES = STAGING_OFF + 8192; };     // 42 KB
+constexpr int MAX_STAGES = 6;
+constexpr uint32_t GU_TX = A_BYTES + B_TX + 2 * SF_BYTES;
+constexpr uint32_t DN_TX = A_BYTES + 3 * SF_BYTES;    // the packed codes count on their own barrier
 constexpr int PRODUCERS = 3;             // TMA-issuing warps (lane 0 of warps 0 .. PRODUCERS - 1)
 constexpr int W_MMA = PRODUCERS;         // the MMA-issuing warp
 constexpr int W_EPI = 4;                 // epilogue warps 4 .. 7 (TMEM lanes 32 (warp % 4) ..)
-constexpr int THREADS = (W_EPI + 4) * 32;
+constexpr int W_CVT = 8;                 // converter warps 8 .. 11 (down only)
+constexpr int THREADS = (W_CVT + 4) * 32;
 static_assert(W_MMA < W_EPI, "warp roles");
-constexpr uint32_t TMEM_COLS = 512;       // accumulators at columns 0 and 128, scale columns from 256
+constexpr uint32_t TMEM_COLS = 512;       // accumulators at columns 0 and 128, scale columns from 256 (12 per stage)
 constexpr uint32_t SF_COL0 = 256;
-constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+static_assert(SF_COL0 + 12 * MAX_STAGES <= TMEM_COLS, "TMEM budget");
+template <int PHASE> constexpr int smem_of() { return StageCfg<PHASE>::STAGES * StageCfg<PHASE>::BYTES + 1024 + 512; }
+static_assert(StageCfg<0>::BYTES % 1024 == 0 && StageCfg<1>::BYTES % 1024 == 0, "stage alignment");
 constexpr int ACT_TILE = A_BYTES + SF_BYTES;  // one 128-row x 128-column activation tile: codes, then exponents
 constexpr int PLACE_CHUNK = 256;          // pairs per CTA of the counting sort
 constexpr int MAX_E = 1024;
@@ -269,20 +281,27 @@ __device__ __forceinline__ bool pf_wait(uint64_t* bar, uint32_t parity, volatile
 template <int PHASE>
 __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                                                           const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
+  constexpr int STAGES = StageCfg<PHASE>::STAGES, STAGE_BYTES = StageCfg<PHASE>::BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  uint64_t* full = bars;                 // [STAGES] TMA -> MMA
+  uint64_t* full = bars;                 // [STAGES] TMA (and, down, the converters) -> MMA
   uint64_t* empty = bars + STAGES;       // [STAGES] MMA -> TMA
   uint64_t* acc_full = bars + 2 * STAGES;       // [2] MMA -> epilogue
   uint64_t* acc_empty = bars + 2 * STAGES + 2;  // [2] epilogue -> MMA
   uint64_t* drain = bars + 2 * STAGES + 4;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  uint64_t* packed = bars + 2 * STAGES + 5;     // [STAGES] down: packed codes landed -> converters
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 5);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    // full: the producer's arrival with its byte count (down: also one arrival per converter warp)
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], PHASE == DOWN ? 5 : 1);
+      mbar_init(&empty[s], 1);
+      mbar_init(&packed[s], 1);
+    }
     for (int s = 0; s < 2; ++s) { mbar_init(&acc_full[s], 1); mbar_init(&acc_empty[s], 4); }
     mbar_init(drain, 1);
     *s_abort = 0;
@@ -313,13 +332,26 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
         if (!pf_wait(&empty[s], ph ^ 1, s_abort, lim)) { ok = false; break; }
         const int tile = (int)(u / a.NB), nb = (int)(u % a.NB);
         const int e = a.tile_e[tile];
-        const uint8_t* wt = a.w + (int64_t)e * a.wstride + ((int64_t)nb * KG + kg) * kTcTileBytes;
         uint8_t* st = smem + s * STAGE_BYTES;
-        mbar_arrive_expect_tx(&full[s], STAGE_TX);
+        mbar_arrive_expect_tx(&full[s], PHASE == DOWN ? DN_TX : GU_TX);
         tma_load_3d(st, &tmA, 0, 0, tile * KG + kg, &full[s]);
-        tma_load_4d(st + A_BYTES, &tmB, 0, 0, nb * KG + kg, e, &full[s]);
-        bulk_g2s_plain(st + A_BYTES + B_BYTES, a.act + act_tile(tile, KG, kg) + A_BYTES, SF_BYTES, &full[s]);
-        bulk_g2s_plain(st + A_BYTES + B_BYTES + SF_BYTES, wt + 8192, SF_BYTES, &full[s]);
+        bulk_g2s_plain(st + SF_OFF, a.act + act_tile(tile, KG, kg) + A_BYTES, SF_BYTES, &full[s]);
+        if (PHASE == GATE_UP) {
+          const uint8_t* wt = a.w + (int64_t)e * a.wstride + ((int64_t)nb * KG + kg) * kTcTileBytes;
+          tma_load_4d(st + A_BYTES, &tmB, 0, 0, nb * KG + kg, e, &full[s]);
+          bulk_g2s_plain(st + SF_OFF + SF_BYTES, wt + 8192, SF_BYTES, &full[s]);
+        } else {
+          // down: weight rows 128 nb .. +127 are half nb % 2 of row pair nb / 2 in the chunks of slices 2 kg and
+          // 2 kg + 1 (64 columns each): 128 rows x 32 B of packed codes, contiguous in each chunk
+          const int NQ = a.H / 256, NS = a.I / 64;
+          mbar_arrive_expect_tx(&packed[s], 8192);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint8_t* ch = a.w + (((int64_t)e * NS + 2 * kg + h) * NQ + nb / 2) * kTcTileBytes;
+            bulk_g2s_plain(st + STAGING_OFF + 4096 * h, ch + 4096 * (nb & 1), 4096, &packed[s]);
+            bulk_g2s_plain(st + SF_OFF + (1 + h) * SF_BYTES, ch + 8192, SF_BYTES, &full[s]);
+          }
+        }
         issued_slot = s;
         issued_ph = ph;
       }
@@ -347,14 +379,26 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
           if (!pf_wait(&full[stage], ph, s_abort, lim)) { ok = false; break; }
           tc_fence_after();
           uint8_t* st = smem + stage * STAGE_BYTES;
-          const uint32_t sfa = tbase + SF_COL0 + (uint32_t)(stage * 8), sfb = sfa + 4;
-          tc_cp_sf(sfa, umma_desc_sf(smem_u32(st + A_BYTES + B_BYTES)));
-          tc_cp_sf(sfb, umma_desc_sf(smem_u32(st + A_BYTES + B_BYTES + SF_BYTES)));
+          const uint32_t sfa = tbase + SF_COL0 + (uint32_t)(stage * 12), sfb = sfa + 4;
+          tc_cp_sf(sfa, umma_desc_sf(smem_u32(st + SF_OFF)));
+          tc_cp_sf(sfb, umma_desc_sf(smem_u32(st + SF_OFF + SF_BYTES)));
           const uint64_t ad = umma_desc_sw128(smem_u32(st)), bd = umma_desc_sw128(smem_u32(st + A_BYTES));
+          if (PHASE == GATE_UP) {
 #pragma unroll
-          for (int kb = 0; kb < 4; ++kb)
-            tc_mma_mxf8f6f4(d_tmem, ad + 2 * kb, bd + 2 * kb, idesc_mxf8f6f4(0, 5, BM, BN, kb, kb), sfa, sfb,
-                            (kg | kb) != 0);
+            for (int kb = 0; kb < 4; ++kb)
+              tc_mma_mxf8f6f4(d_tmem, ad + 2 * kb, bd + 2 * kb, idesc_mxf8f6f4(0, 5, BM, BN, kb, kb), sfa, sfb,
+                              (kg | kb) != 0);
+          } else {
+            // K-blocks 0, 1 come from chunk 0 and 2, 3 from chunk 1, each chunk with its own exponent block; the
+            // weight rows are half nb % 2 of their chunks' row pair, so they read scale bytes 2 (nb % 2) + (0, 1)
+            tc_cp_sf(sfb + 4, umma_desc_sf(smem_u32(st + SF_OFF + 2 * SF_BYTES)));
+            const int nb = (int)(u % a.NB);
+#pragma unroll
+            for (int kb = 0; kb < 4; ++kb)
+              tc_mma_mxf8f6f4(d_tmem, ad + 2 * kb, bd + 2 * kb,
+                              idesc_mxf8f6f4(0, 5, BM, BN, kb, (uint32_t)(2 * (nb & 1) + (kb & 1))), sfa,
+                              sfb + 4 * (kb >> 1), (kg | kb) != 0);
+          }
           tc_commit(&empty[stage]);  // the stage is free once these MMAs have read it
           if (++stage == STAGES) { stage = 0; ph ^= 1; }
         }
@@ -365,6 +409,36 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
       mbar_wait(drain, 0, 100000000LL);
     }
     __syncwarp();
+  } else if (warp >= W_CVT) {
+    // ---------------- down converters: expand each stage's packed codes into the padded operand the MMA reads
+    // (what the TMA engine's 16U4_ALIGN16B type writes: every 8 packed bytes followed by 8 bytes of gap, 128-byte
+    // rows, 16-byte chunk c of row r at chunk c ^ (r % 8)). Chunk c of weight row r holds codes 16c .. 16c + 15 of the
+    // stage's 128 columns: from the staged chunk c / 4, bytes 8 (c % 4) .. +7 of the row's 32 (stored in the layout's
+    // 32-byte swizzle: 16-byte half (c % 4) / 2 of row r sits at half ((c % 4) / 2) ^ ((r >> 2) & 1)).
+    if (PHASE == DOWN) {
+      const int ct = threadIdx.x - W_CVT * 32;
+      int64_t g = 0;
+      bool ok = true;
+      for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x)
+        for (int kg = 0; kg < KG; ++kg, ++g) {
+          const int s = (int)(g % STAGES);
+          uint8_t* st = smem + s * STAGE_BYTES;
+          int w = 1;
+          if (lane == 0) w = pf_wait(&packed[s], (uint32_t)((g / STAGES) & 1), s_abort, lim) ? 1 : 0;
+          if (!__shfl_sync(0xFFFFFFFFu, w, 0)) { ok = false; break; }
+#pragma unroll
+          for (int it = 0; it < 8; ++it) {
+            const int idx = ct + 128 * it, r = idx >> 3, c = idx & 7;
+            const int hh = ((c & 3) >> 1) ^ ((r >> 2) & 1);
+            const uint2 v = *reinterpret_cast<const uint2*>(st + STAGING_OFF + 4096 * (c >> 2) + r * 32 + hh * 16 + (c & 1) * 8);
+            *reinterpret_cast<uint4*>(st + A_BYTES + r * 128 + ((c ^ (r & 7)) << 4)) = make_uint4(v.x, v.y, 0u, 0u);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> the MMA's reads
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full[s]);
+        }
+      if (!ok) record_error(a.status, MOE_ERR_DEVICE_TIMEOUT);
+    }
   } else {
     // ---------------- epilogue: warps 4..7 own TMEM lanes 32*(warp % 4) .. +31
     const int q = warp & 3;
@@ -514,18 +588,18 @@ moe_status_t run(const moe_layer_t* L, const void* x_bf16, int32_t T, const int3
 
   // tensor maps (host encodes; they travel as __grid_constant__ kernel parameters)
   const TcGeom ggu = tc_geom(MOE_MAT_GATE_UP, H, I), gdn = tc_geom(MOE_MAT_DOWN, H, I);
-  CUtensorMap mx, mgu, mh, mdn;
+  CUtensorMap mx, mgu, mh, mdn = {};  // mdn: unused by the down GEMM, which bulk-copies its packed chunks
   if (!map_act(&mx, B + P.o_xq, P.tiles_max * (H / 128)) || !moe_internal::tmap_tc_weights(&mgu, L->gate_up, MOE_MAT_GATE_UP, H, I, E) ||
-      !map_act(&mh, B + P.o_hq, P.tiles_max * (I / 128)) || !moe_internal::tmap_tc_weights(&mdn, L->down, MOE_MAT_DOWN, H, I, E))
+      !map_act(&mh, B + P.o_hq, P.tiles_max * (I / 128)))
     return MOE_ERR_CUDA;
 
   static std::once_flag attr_once;
   static bool attr_ok = false;
   std::call_once(attr_once, [] {
-    attr_ok = cudaFuncSetAttribute(gemm_kernel<GATE_UP>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) ==
-                  cudaSuccess &&
-              cudaFuncSetAttribute(gemm_kernel<DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) ==
-                  cudaSuccess;
+    attr_ok = cudaFuncSetAttribute(gemm_kernel<GATE_UP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   smem_of<GATE_UP>()) == cudaSuccess &&
+              cudaFuncSetAttribute(gemm_kernel<DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   smem_of<DOWN>()) == cudaSuccess;
   });
   if (!attr_ok) return MOE_ERR_CUDA;
 
@@ -553,7 +627,7 @@ moe_status_t run(const moe_layer_t* L, const void* x_bf16, int32_t T, const int3
   ga.H = H;
   ga.status = status;
   ga.wait_ns = kDefaultWaitNs;
-  gemm_kernel<GATE_UP><<<grid, THREADS, SMEM, s>>>(mx, mgu, ga);
+  gemm_kernel<GATE_UP><<<grid, THREADS, smem_of<GATE_UP>(), s>>>(mx, mgu, ga);
   GemmArgs gd = ga;
   gd.w = (const uint8_t*)L->down;
   gd.wstride = gdn.stride;
@@ -561,7 +635,7 @@ moe_status_t run(const moe_layer_t* L, const void* x_bf16, int32_t T, const int3
   gd.NB = (int)(gdn.R / BN);
   gd.act = B + P.o_hq;
   gd.gu_dump = nullptr;
-  gemm_kernel<DOWN><<<grid, THREADS, SMEM, s>>>(mh, mdn, gd);
+  gemm_kernel<DOWN><<<grid, THREADS, smem_of<DOWN>(), s>>>(mh, mdn, gd);
   dim3 cg(T, (H / 4 + 255) / 256);
   combine<<<cg, 256, 0, s>>>(ga.dout, pslot, tile_c0, w, k, H, y, (__nv_bfloat16*)y_bf16);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;

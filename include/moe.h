@@ -110,10 +110,13 @@ moe_status_t moe_encode_blocks(moe_format_t fmt, const float* src, int64_t rows,
  *   encoded on the fly exactly as moe_encode_blocks does.
  *   dst must be 16-byte aligned and hold moe_packed_bytes(...) bytes.
  * Shapes: H and I multiples of 256 (and of the block size), 256 <= H, I <= 4096.
- * Layout MOE_LAYOUT_TC is MXFP4 only: per expert, 128 x 128 tiles in (row tile, column tile) order, each 8704
- * contiguous bytes: codes [128 rows][64 B] (even k in the low nibble), then the 512 E8M0 exponents permuted
- * (byte l*16 + c*4 + kb = row l + 32c, 32-block kb); GATE_UP has R = 2I rows ordered in groups of 128 = 64 gate
- * rows then the same 64 up rows, K = H; DOWN has R = H, K = I. */
+ * Layout MOE_LAYOUT_TC is MXFP4 only; every run is 8704 contiguous bytes: 8192 bytes of codes (even k in the low
+ * nibble) then 512 E8M0 exponents permuted for the tensor cores (byte l*16 + c*4 + b = operand row l + 32c, byte b).
+ *   GATE_UP (R = 2I rows in groups of 128 = 64 gate rows then the same 64 up rows, K = H): 128 x 128 tiles in
+ *   (row tile, column tile) order, codes [128 rows][64 B], b = 32-block of the tile.
+ *   DOWN (R = H, K = I): chunks of 256 rows x 64 columns in (column block k / 64, row pair r / 256) order, codes
+ *   [256 rows][32 B]; b = 2 * (128-row half of the chunk) + 32-block of the 64 columns. The 64 columns of a chunk
+ *   are the 64 intermediate indices one gate/up tile row produces. */
 moe_status_t moe_pack_weights(moe_format_t fmt, moe_src_t src_kind, moe_layout_t layout, moe_matrix_t kind,
                               int64_t n_experts, int64_t H, int64_t I, const void* src_a, const void* src_b,
                               void* dst, size_t dst_bytes, void* stream);
