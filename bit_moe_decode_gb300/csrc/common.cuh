@@ -74,6 +74,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// The same with a suspend-time hint: the thread sleeps until the phase completes or about `hint_ns` passed, so a
+// waiting warp takes neither issue slots nor shared-memory bandwidth from the warps that work meanwhile.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* b, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(b)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+// Non-blocking test of an mbarrier phase (mbarrier.test_wait never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Bounded wait on an mbarrier phase. Returns false if `limit_ns` nanoseconds passed first.
 __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, long long limit_ns) {
   if (mbar_try_wait(b, parity)) return true;
@@ -104,6 +125,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 // Named barrier among `nthreads` threads (multiple of 32) with id `id` (1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Arrive at named barrier `id` without waiting (the waiting threads use bar.sync with the same count); the
+// arriving threads' earlier memory accesses are ordered before the waiters' later ones.
+__device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ------------------------------------------------------------------ global-memory flag helpers

@@ -22,13 +22,13 @@
 //   y[t] = sum_r w[t, r] * (sum over the expert's slices, in slice order, of the partials), ranks in order.
 // Only WHICH CTA does which slice depends on the call. Every CTA owns nw = floor(slices / CTAs) WHOLE slices: it
 // runs all their segments, forms h in its own shared memory and runs their down chunks, with no global hand-off.
-// The remaining R < CTAs slices are SPLIT: their segments (exports) are spread over the CTAs and run first; their
+// The remaining R < CTAs slices are SPLIT: their segments (exports) are spread over the CTAs and run early; their
 // partials go to global memory and are counted. Their down chunks (imports) are dealt in contiguous runs, so a CTA
 // imports from one or two split slices, forms each one's h itself from the counted partials, and runs the chunks
 // last; the runs are sized so that every CTA streams the same number of weight bytes to within one tile. Each
-// CTA's order: the first whole slice's segments, the exports (they stream while that slice's h is formed), the
-// other whole slices (W1 D0 W2 D1 ... so that forming h of a slice overlaps the next slice's stream), imports. A grid barrier then lets every CTA sum the down partials of its share of the outputs (one warp
-// per (token, 32 rows, rank): a lane per row, the slices in order).
+// CTA's order: the exports, the whole slices (W0 W1 D0 W2 D1 ..: forming h of a slice overlaps the next slice's
+// stream), the imports. A grid barrier then lets every CTA sum the down partials of its share of the outputs (one
+// warp per (token, 32 rows, rank): a lane per row, the slices in order).
 //
 // Inside a CTA, three independent pipelines take the CTA's units as they free up: a copy-issuing warp, an
 // MMA-issuing warp, a three-slot shared-memory ring, TMEM accumulators and a group of
@@ -77,6 +77,9 @@ constexpr int NGRP = NPIPE;              // of its own: issuing lanes of one war
 constexpr int QN = 32;                   // groups of 4 warps (group j drains pipeline j), then the helper warp;
 constexpr int HELPER = EPI_WARP0 + 4 * NGRP;  // unit-queue entries per pipeline
 constexpr int THREADS = (HELPER + 1) * 32;
+// named barriers: 0 the CTA, 1..NGRP the epilogue groups, NB_ROUTE warps 0..EPI_WARP0-1 (routing), NB_TAB / NB_TAB2
+// the routing tables handed from warp 0 to the other warps
+constexpr int NB_ROUTE = 2 + NGRP, NB_TAB = NB_ROUTE + 1, NB_TAB2 = NB_ROUTE + 2;
 constexpr uint32_t TMEM_COLS = 512;      // accumulators below SF_COL0, 8 scale columns per slot from there
 constexpr uint32_t SF_COL0 = TMEM_COLS - 8 * NSLOT;
 static_assert(SF_COL0 + 8 * NSLOT <= TMEM_COLS, "TMEM budget");
@@ -156,10 +159,10 @@ __host__ __device__ inline Mine my_share(const Geo& g, int c) {
   m.n = m.ne + m.nloc + m.nimp;
   return m;
 }
-// Position of export segment xo (0 .. ne - 1) in the CTA's order: after the first whole slice's segments, so that
-// they stream while that slice's h is formed (first of all when the CTA has no whole slice); their importers run
-// their chunks last.
-__host__ __device__ inline int export_pos(const Geo& g, int xo) { return g.nw > 0 ? g.SG + xo : xo; }
+// A CTA's order: its export segments first (their partials travel through global memory to the importing CTAs, so
+// they get the most time), then the whole slices as W0 W1 D0 W2 D1 .. W(nw-1) D(nw-2) D(nw-1) (forming h of a slice
+// overlaps the stream of the next slice's segments; the stage ring covers the last one), then the imports.
+__host__ __device__ inline int export_pos(const Geo& g, int xo) { return xo; }
 __device__ inline Unit unit_at(const Geo& g, const Mine& mi, int c, int i) {
   Unit r;
   r.ib = 0;
@@ -171,7 +174,7 @@ __device__ inline Unit unit_at(const Geo& g, const Mine& mi, int c, int i) {
     return r;
   }
   if (i >= e0) i -= mi.ne;
-  if (i < mi.nloc) {                                // whole slices: W0 W1 D0 W2 D1 ... W(nw-1) D(nw-2) D(nw-1)
+  if (i < mi.nloc) {                                // whole slices
     int m, isd, x;
     if (i < g.SG) { m = 0; isd = 0; x = i; }
     else {
@@ -309,14 +312,15 @@ __device__ __forceinline__ bool wait_ge(const uint32_t* p, uint32_t target, vola
     if (globaltimer_ns() - t0 > lim) { *abort_flag = 1; return false; }
   }
 }
-// Spinning threads back off briefly between polls so that warps doing arithmetic on the same SM keep their issue
-// slots.
+// Bounded wait on an mbarrier phase by one thread: non-blocking tests with short sleeps in between. A thread parked
+// in mbarrier.try_wait was measured to slow the shuffles of the other warps on its SM several-fold, so no thread of
+// this kernel waits that way.
 __device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, long long lim) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   const long long t0 = globaltimer_ns();
   while (true) {
-    __nanosleep(20);
-    if (mbar_try_wait(bar, parity)) return true;
+    __nanosleep(32);
+    if (mbar_test_wait(bar, parity)) return true;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > lim) { *abort_flag = 1; return false; }
   }
@@ -513,7 +517,7 @@ struct Smem {                   // static shared state (the stage ring, h buffer
   uint64_t hready[NHB], hfree[NHB];     // whole slices: h formed / its down chunks done reading it
   uint64_t iready[NIB], ifree[NIB];     // imported slices: the same
   uint64_t xstaged[NXB], xfree[NXB];    // export partials staged / copied out
-  uint64_t tab_full, tab2_full, drain[NPIPE];
+  uint64_t drain[NPIPE];
   int uq[NPIPE][QN];                    // unit index, and the unit itself (packed), per queue entry
   uint64_t uqu[NPIPE][QN];
   int lcnt[NHB];
@@ -593,8 +597,6 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
     // ifree: one commit per down chunk of the slice (the helper arrives for the chunks other CTAs hold)
     for (int b = 0; b < NIB; ++b) { mbar_init(&S.iready[b], 1); mbar_init(&S.ifree[b], g.NQ); }
     for (int b = 0; b < NXB; ++b) { mbar_init(&S.xstaged[b], 1); mbar_init(&S.xfree[b], 1); }
-    mbar_init(&S.tab_full, 1);
-    mbar_init(&S.tab2_full, 1);
     S.abort = 0;
     S.next = 0;
     fence_mbar_init();
@@ -610,15 +612,13 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
     // this CTA's share of the x parts (independent of the routing) while the other warps route and build the
     // tables, then the token tables the epilogues need
     if (epi) split_x_global(a, g, xwarp, nxwarps, xfirst, cnt);
-    if (!bwait(&S.tab_full, 0, s_abort, lim) && threadIdx.x == EPI_WARP0 * 32) record_error(&hdr->status, MOE_ERR_DEVICE_TIMEOUT);
+    // hardware barriers: warp 0 arrives once the union is built, then the first epilogue warp builds the slots
+    named_bar(NB_TAB, 32 + THREADS - EPI_WARP0 * 32);
     if (warp == EPI_WARP0) {
-      if (lane == 0) {
-        build_slots(tb, S.idx, S.wt, g.T, g.k);
-        mbar_arrive(&S.tab2_full);
-      }
+      if (lane == 0) build_slots(tb, S.idx, S.wt, g.T, g.k);
       __syncwarp();
     }
-    if (!bwait(&S.tab2_full, 0, s_abort, lim) && threadIdx.x == EPI_WARP0 * 32) record_error(&hdr->status, MOE_ERR_DEVICE_TIMEOUT);
+    named_bar(NB_TAB2, THREADS - EPI_WARP0 * 32);
   } else {
     if (a.wr) {
       // routing, phase 2: every CTA selects each token's experts from all the logits (a warp per token)
@@ -634,7 +634,9 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
                                                sid, sw);
         }
         if (lane == 0)
-          for (int r = 0; r < g.k; ++r) {
+#pragma unroll
+          for (int r = 0; r < MAX_K; ++r) {
+            if (r >= g.k) break;
             S.idx[t][r] = ok ? sid[r] : -1;
             S.wt[t][r] = ok ? sw[r] : 0.f;
             if (blockIdx.x == 0 && ok) {
@@ -647,7 +649,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
       S.idx[threadIdx.x / g.k][threadIdx.x % g.k] = pre_idx;
       S.wt[threadIdx.x / g.k][threadIdx.x % g.k] = pre_w;
     }
-    named_bar(2 + NGRP, EPI_WARP0 * 32);
+    named_bar(NB_ROUTE, EPI_WARP0 * 32);
     if (warp == 0) {
       build_union_warp(tb, S.idx, g.T, g.k, g.E);
       __syncwarp();
@@ -655,10 +657,11 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
         // an expert id out of range: no units (every role finds an empty queue), status MOE_ERR_INVALID_ARG
         if (tb.bad && blockIdx.x == 0) record_error(&hdr->status, MOE_ERR_INVALID_ARG);
         if (tb.bad) tb.U = 0;
-        mbar_arrive(&S.tab_full);
       }
+      __syncwarp();
+      named_bar_arrive(NB_TAB, 32 + THREADS - EPI_WARP0 * 32);
     }
-    named_bar(2 + NGRP, EPI_WARP0 * 32);
+    named_bar(NB_ROUTE, EPI_WARP0 * 32);
   }
   make_schedule(g, tb.U);
   const Mine mine = my_share(g, (int)blockIdx.x);
@@ -786,7 +789,9 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
       }
       if (!ok) record_error(&hdr->status, MOE_ERR_DEVICE_TIMEOUT);
       tc_commit(&S.drain[j]);
-      mbar_wait(&S.drain[j], 0, 100000000LL);
+      // every MMA of this pipeline has completed before TMEM is released (bounded: 100 ms)
+      const long long t0 = globaltimer_ns();
+      while (!mbar_test_wait(&S.drain[j], 0) && globaltimer_ns() - t0 < 100000000LL) __nanosleep(64);
     }
     __syncwarp();
   } else if (warp == HELPER) {
@@ -805,11 +810,13 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
       float* dst = gpart + ((int64_t)un.li * g.SG + un.x) * a.ts * 128;
       for (int t = 0; t < g.T; ++t)
         reinterpret_cast<float4*>(dst + t * 128)[lane] = reinterpret_cast<const float4*>(src + t * 128)[lane];
+      // __syncwarp orders the lanes' stores before lane 0's release, which publishes them with the count (a
+      // release costs one store round trip; a full fence here measured several times that while the weights stream)
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.xfree[k]);
-      __threadfence();
-      __syncwarp();
-      if (lane == 0) red_release_add(cnt + C_SPLIT + un.li, 1u);
+      if (lane == 0) {
+        mbar_arrive(&S.xfree[k]);
+        red_release_add(cnt + C_SPLIT + un.li, 1u);
+      }
     }
     for (int ib = 0; ib < (nunits ? mine.nis : 0) && ok; ++ib) {
       const int kb = ib % NIB;
@@ -821,6 +828,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
         if (w) w = wait_ge(cnt + C_SPLIT + li, (uint32_t)g.SG, s_abort, lim) ? 1 : 0;
       }
       if (!__shfl_sync(0xFFFFFFFFu, w, 0)) { ok = false; break; }
+      __syncwarp();  // lane 0's acquire -> the other lanes' loads of the partials
       finalize_import(gpart + (int64_t)li * g.SG * a.ts * 128, (int64_t)a.ts * 128, g.SG, tb.ntok[u], tb.tok[u], g.W,
                       ibuf + kb * HIMG);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> the MMA's reads
@@ -965,7 +973,6 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
         }
       }
     }
-    __threadfence();  // the down partials are visible grid-wide before this CTA arrives at the grid barrier
   }
   tc_fence_before();
   __syncthreads();
@@ -977,6 +984,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
   // (t, jb, r) task (lane l = row), the rank sums meet in shared memory.
   if (tb.U > 0) {
     if (threadIdx.x == 0) {
+      // the CTA barrier above orders every thread's down partials before this release (cumulative at gpu scope)
       red_release_add(&hdr->gbar, 1u);
       S.gok = wait_ge(&hdr->gbar, gridDim.x, s_abort, lim) ? 1 : 0;
       if (!S.gok) record_error(&hdr->status, MOE_ERR_DEVICE_TIMEOUT);

@@ -71,10 +71,12 @@ route_kernel(const uint16_t* __restrict__ wr, const uint16_t* __restrict__ x, in
         },
         E, k, sid, sw);
     if (lane == 0)
-      for (int r = 0; r < k; ++r) {
-        idx_out[(size_t)(t0 + t) * k + r] = sid[r];
-        w_out[(size_t)(t0 + t) * k + r] = sw[r];
-      }
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+        if (r < k) {
+          idx_out[(size_t)(t0 + t) * k + r] = sid[r];
+          w_out[(size_t)(t0 + t) * k + r] = sw[r];
+        }
   }
   cluster.sync();  // keep every CTA's logits alive until CTA 0 has read them
 }

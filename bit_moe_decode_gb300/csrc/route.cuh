@@ -91,8 +91,14 @@ __device__ __forceinline__ void route_topk_warp(Logit logit, int E, int k, int (
     const int e = lane + 32 * j;
     v[j] = e < E ? logit(e) : -__int_as_float(0x7f800000);
   }
+  // the rounds are unrolled to the largest k so that sel, sid and sw stay in registers (a dynamically indexed
+  // array would live in local memory, whose round trips are slow while the weights stream)
   float sel[8];
-  for (int r = 0; r < k; ++r) {
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    sel[r] = 0.f;
+    sid[r] = 0;
+    if (r >= k) continue;
     float best = -__int_as_float(0x7f800000);
     int bi = 0x7fffffff;
 #pragma unroll
@@ -113,8 +119,11 @@ __device__ __forceinline__ void route_topk_warp(Logit logit, int E, int k, int (
       if (lane + 32 * j == bi) v[j] = -__int_as_float(0x7f800000);
   }
   float den = 0.f;
-  for (int r = 0; r < k; ++r) den += expf(sel[r] - sel[0]);
-  for (int r = 0; r < k; ++r) sw[r] = expf(sel[r] - sel[0]) / den;
+#pragma unroll
+  for (int r = 0; r < 8; ++r)
+    if (r < k) den += expf(sel[r] - sel[0]);
+#pragma unroll
+  for (int r = 0; r < 8; ++r) sw[r] = r < k ? expf(sel[r] - sel[0]) / den : 0.f;
 }
 
 }  // namespace moe
