@@ -5,7 +5,11 @@ expert FFN (gate+up, SiLU*up, down, weighted combine), one token at a time, as a
 
 Prints one JSON line. value = tokens/s of the whole step; roofline = the fused FFN kernel's algorithmic bytes
 (packed bytes of the token's 6 active experts) / its measured average launch time, against the measured HBM copy
-bandwidth. `--impl reference` times the CPU oracle on the host cores instead (a bounded sample of the workload).
+bandwidth. The same run measures the other expert formats on the same weights and tokens (`formats`: INT4 g32,
+Q2_K and MXFP4 in the mat-vec layout, each a router launch plus an FFN launch per token) and is the parity run:
+the first 32 timed tokens' outputs (16 per extra format) are compared with the CPU oracle on the same seeds
+(`parity`); a breach prints the line and exits with status 1. `--impl reference` times the CPU oracle on the host
+cores instead (a bounded sample of the workload).
 """
 from __future__ import annotations
 
@@ -59,6 +63,9 @@ def parse():
     p.add_argument("--layout", default="auto", choices=["auto", "tc", "decode"],
                    help="weight layout of the decode path: tc (MXFP4, tcgen05 kernels) or decode (mat-vec kernels); "
                         "auto = tc for MXFP4, decode otherwise")
+    p.add_argument("--no-formats", action="store_true", help="measure only the --fmt / --layout path")
+    p.add_argument("--no-parity", action="store_true", help="skip the oracle comparison of the timed tokens")
+    p.add_argument("--parity-tokens", type=int, default=32)
     p.add_argument("--prefill-tokens", type=int, default=4096,
                    help="tokens of the prefill grouped-GEMM measurement (MXFP4 only; 0 = skip)")
     return p.parse_args()
@@ -139,11 +146,6 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------------------------ GPU arm
-# dram__bytes_read.sum + dram__bytes_write.sum per launch of the tensor-core decode kernel as it stands, from the
-# ncu capture summarised in profiles/decode_kernel_mxfp4_ds4_t1.md (routing given, small expert pool, same 6-expert bytes)
-TC_TRAFFIC = 82944512
-
-
 def run_ours(args):
     import torch
     import bit_moe_decode_gb300 as m
@@ -170,6 +172,13 @@ def run_ours(args):
     layer_tc = m.Layer(fmt, H, I, E, layout=m.MOE_LAYOUT_TC, device=dev) if (use_tc or do_prefill) else None
     layer = layer_tc if use_tc else m.Layer(fmt, H, I, E, device=dev)
     layer_p = layer_tc if do_prefill else None
+    # the other formats, measured on the same weights and tokens (single GPU only: the scaling runs time the headline)
+    extra = {}
+    if not args.no_formats and world == 1:
+        for name, fid in FMT_IDS.items():
+            if name == args.fmt and not use_tc:
+                continue
+            extra[name if name != "mxfp4" else "mxfp4_matvec_layout"] = m.Layer(fid, H, I, E, device=dev)
     t0 = time.time()
     batch = 16
     pool = cf.ThreadPoolExecutor(2)
@@ -187,6 +196,8 @@ def run_ours(args):
         layer.pack(m.MOE_SRC_F32, gd, ud, dd, e0=e0)
         if layer_tc is not None and layer_tc is not layer:
             layer_tc.pack(m.MOE_SRC_F32, gd, ud, dd, e0=e0)
+        for lx in extra.values():
+            lx.pack(m.MOE_SRC_F32, gd, ud, dd, e0=e0)
     torch.cuda.synchronize()
     setup_s = time.time() - t0
 
@@ -280,6 +291,10 @@ def run_ours(args):
     status = m.moe_get_device_status(ws, stream)
     if status != 0:
         raise RuntimeError("device status %d after timed region" % status)
+    npar = 0 if args.no_parity else min(args.parity_tokens, T)
+    checks = []
+    if npar and rank == 0:   # the timed step's own outputs (every step computes the same y)
+        checks.append((None, fmt, y[:npar].cpu().numpy(), idx[:npar].cpu().numpy(), w[:npar].cpu().numpy()))
 
     # ---- the dominant kernel alone (routing fixed): average launch duration
     for _ in range(2):
@@ -329,6 +344,11 @@ def run_ours(args):
     e2e_ms = s0.elapsed_time(s1) / e2e_steps
     e2e_ms = max_over_ranks(e2e_ms, dist, dev)
 
+    formats = {}
+    for key, lx in extra.items():
+        formats[key], rows = bench_format(m, torch, args, dev, stream, lx, wr, x, x_host, min(npar, 16))
+        if rows is not None:
+            checks.append((key, lx.fmt) + rows)
     prefill = bench_prefill(m, torch, args, dev, stream, layer_p, E) if do_prefill else None
     verify = bench_verify(m, torch, args, dev, stream, layer, wr, x_host, E, per_expert) if (use_tc and not args.no_verify) else None
     spec = bench_spec(m, torch, dev, stream) if not args.no_verify else None
@@ -363,15 +383,15 @@ def run_ours(args):
             "mean_unique_experts": float(uniq),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4),
-                         # dram__bytes_read + dram__bytes_write per launch from the ncu capture summarised in
-                         # profiles/decode_kernel_mxfp4_ds4_t1.md (the tensor-core MXFP4 kernel as it stands)
-                         "traffic": TC_TRAFFIC if use_tc else None,
+                         # DRAM bytes per launch come from an ncu capture of the kernel, not from this run
+                         "traffic": None,
                          "kernel": "decode_kernel (tcgen05)" if use_tc else "ffn_kernel<%s>" % args.fmt,
                          "bytes_per_launch": alg_bytes,
                          "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if hbm_measured else "fallback"},
             "e2e": {"value": round(world * T / (e2e_ms * 1e-3), 1), "unit": "tok/s",
                     "h2d_bytes_per_step": int(T * H * 2), "d2h_bytes_per_step": int(T * H * 4)},
             "clocks": clk,
+            "formats": formats,
             "prefill": prefill,
             "verify": verify,
             "spec_accept": spec,
@@ -380,7 +400,89 @@ def run_ours(args):
         }
     if dist:
         dist.destroy_process_group()
-    return out
+    return out, checks
+
+
+def bench_format(m, torch, args, dev, stream, layer, wr, x, x_host, npar):
+    """One more expert format on the same weights and tokens, in the mat-vec (DECODE) layout: a step is, per token,
+    the router launch (moe_route_topk) and the FFN launch (moe_expert_ffn_decode), replayed as a CUDA graph. Reports
+    the step, the FFN launch alone (routing fixed) against the HBM roofline, and the step end to end with host
+    buffers; returns the first npar tokens' (y, idx, w) for the oracle comparison."""
+    T = x.shape[0]
+    fid = layer.fmt
+    ws = layer.workspace(1, K_TOP)
+    idx = torch.zeros((T, K_TOP), dtype=torch.int32, device=dev)
+    w = torch.zeros((T, K_TOP), dtype=torch.float32, device=dev)
+    y = torch.zeros((T, H), dtype=torch.float32, device=dev)
+
+    def step_launch():
+        for t in range(T):
+            m.moe_route_topk(wr, x[t], 1, H, E, K_TOP, None, None, 0, idx[t], w[t], stream=stream)
+            m.moe_expert_ffn_decode(layer, x[t], idx[t], w[t], K_TOP, y[t], None, False, ws, stream=stream)
+
+    def ffn_launch():
+        for t in range(T):
+            m.moe_expert_ffn_decode(layer, x[t], idx[t], w[t], K_TOP, y[t], None, False, ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        step_launch()
+    stream.synchronize()
+    if m.moe_get_device_status(ws, stream) != 0:
+        raise RuntimeError("device status after the warm-up of format %d" % fid)
+    g_step, g_ffn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step, stream=stream):
+        step_launch()
+    with torch.cuda.graph(g_ffn, stream=stream):
+        ffn_launch()
+
+    def timed(g, reps):
+        with torch.cuda.stream(stream):
+            for _ in range(max(1, args.warmup)):
+                g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(reps):
+                g.replay()
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    reps = max(1, args.steps)
+    ms_step = timed(g_step, reps)
+    ffn_us = timed(g_ffn, reps) * 1e3 / T
+    # end to end: the tokens from pinned host memory and the outputs back, inside the timed region
+    xh = torch.from_numpy(x_host.view(np.int16)).pin_memory()
+    yh = torch.empty((T, H), dtype=torch.float32).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_e2e = max(1, min(reps, 3))
+    e0.record(stream)
+    for _ in range(n_e2e):
+        with torch.cuda.stream(stream):
+            x.copy_(xh, non_blocking=True)
+            g_step.replay()
+            yh.copy_(y, non_blocking=True)
+    e1.record(stream)
+    e1.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    if m.moe_get_device_status(ws, stream) != 0:
+        raise RuntimeError("device status after format %d" % fid)
+    idx_np = idx.cpu().numpy()
+    per_expert = m.moe_packed_bytes(fid, 0, 0, 1, H, I) + m.moe_packed_bytes(fid, 0, 1, 1, H, I)
+    alg = float(np.mean([len(set(r)) for r in idx_np])) * per_expert
+    peak = peak_of(measured_peaks(), "hbm_gbs")
+    achieved = alg / (ffn_us * 1e-6) / 1e9
+    res = {"layout": "matvec (DECODE)", "kernel": "ffn_kernel<%s>" % {1: "mxfp4", 2: "int4g32", 3: "q2k"}[fid],
+           "step_kernels": "moe_route_topk + moe_expert_ffn_decode",
+           "tok_s": round(T / (ms_step * 1e-3), 1), "ms_per_step": round(ms_step, 4),
+           "ffn_kernel_us": round(ffn_us, 3), "gpu_launches": 2 * T * reps,
+           "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak or 6800.0, "unit": "GB/s",
+                        "frac": round(achieved / (peak or 6800.0), 4), "traffic": None, "bytes_per_launch": alg,
+                        "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if peak else "fallback"},
+           "e2e": {"value": round(T / (e2e_ms * 1e-3), 1), "unit": "tok/s", "h2d_bytes_per_step": int(T * H * 2),
+                   "d2h_bytes_per_step": int(T * H * 4)}}
+    rows = (y[:npar].cpu().numpy(), idx[:npar].cpu().numpy(), w[:npar].cpu().numpy()) if npar else None
+    return res, rows
 
 
 def bench_verify(m, torch, args, dev, stream, layer, wr, x_host, E, per_expert):
@@ -535,40 +637,91 @@ def bench_prefill(m, torch, args, dev, stream, layer_p, E):
 
 # ------------------------------------------------------------------------------------------------ CPU oracle
 class CpuOracle:
-    """The oracle as it stands, on the host cores: one token per thread, tokens of the same layer and routing
-    rule. The sampled tokens' expert weights are encoded once, before any timing."""
+    """The oracle as it stands, on the host cores, for the first n tokens of the bench's workload (same seeds, same
+    layer): its own routing of them, encoded experts per format (built once, before any timing), the timed sample
+    of the CPU baseline and the parity check of the GPU's outputs."""
 
-    def __init__(self, fmt_name, seed):
+    def __init__(self, seed, n):
         import oracle
-        from moe_inputs import expert_matrix_f32, router_f16_bits, x_bf16_bits
+        from moe_inputs import router_f16_bits, x_bf16_bits
         self.oracle = oracle
-        self.fmt = FMT_IDS[fmt_name]
+        self.seed = seed
         self.cores = os.cpu_count() or 1
-        self.n = self.cores
+        self.n = max(int(n), self.cores)
         wr = router_f16_bits(seed, 0, E, H)
         self.x = x_bf16_bits(seed, range(self.n), H)
-        self.idx, self.w, _, _ = oracle.route_topk(wr, self.x, K_TOP)
-        self.cache = {}
-        for e in np.unique(self.idx):
-            for which in range(3):
-                self.cache[(int(e), which)] = oracle.encode(self.fmt, expert_matrix_f32(seed, 0, int(e), which, H, I))
+        self.idx, self.w, self.logits, self.absl = oracle.route_topk(wr, self.x, K_TOP)
+        self.enc = {}
 
-    def _one(self, t):
-        c = self.cache
-        self.oracle.moe_tokens(self.fmt, H, I, lambda e: c[(int(e), 0)], lambda e: c[(int(e), 1)],
-                               lambda e: c[(int(e), 2)], self.idx[t:t + 1], self.w[t:t + 1], self.x[t:t + 1])
+    def _encode(self, fmt, experts):
+        from moe_inputs import expert_matrix_f32
+        todo = [(int(e), wh) for e in sorted(set(int(v) for v in np.ravel(experts))) for wh in range(3)
+                if (fmt, int(e), wh) not in self.enc]
 
-    def run(self, seconds):
+        def one(key):
+            e, wh = key
+            self.enc[(fmt, e, wh)] = self.oracle.encode(fmt, expert_matrix_f32(self.seed, 0, e, wh, H, I))
+        with cf.ThreadPoolExecutor(self.cores) as ex:
+            list(ex.map(one, todo))
+
+    def _moe(self, fmt, idx, w, x):
+        c = self.enc
+        return self.oracle.moe_tokens(fmt, H, I, lambda e: c[(fmt, int(e), 0)], lambda e: c[(fmt, int(e), 1)],
+                                      lambda e: c[(fmt, int(e), 2)], idx, w, x)
+
+    def timed(self, fmt_name, seconds):
+        """Tokens per second of the oracle, one token per thread, over the first `cores` tokens."""
+        fmt = FMT_IDS[fmt_name]
+        nt = self.cores
+        self._encode(fmt, self.idx[:nt])
         done = 0
         t0 = time.time()
         with cf.ThreadPoolExecutor(self.cores) as ex:
             while time.time() - t0 < seconds or done == 0:
-                list(ex.map(self._one, range(self.n)))
-                done += self.n
+                list(ex.map(lambda t: self._moe(fmt, self.idx[t:t + 1], self.w[t:t + 1], self.x[t:t + 1]), range(nt)))
+                done += nt
         el = time.time() - t0
         return {"value": round(done / el, 3), "unit": "tok/s", "cores": self.cores, "kind": "oracle",
                 "sample": "%d tokens (%d per thread) of the same layer and routing rule in %.1f s wall; fp64 C oracle, "
                           "one token per thread" % (done, done // self.cores, el)}
+
+    def _near_tie(self, t, got):
+        """The GPU's top-k list of token t differs from the oracle's only by swaps of experts whose exact logits lie
+        within the fp32 summation error bound of each other (H * 2^-24 * sum|terms| each)."""
+        ref = self.idx[t]
+        if np.array_equal(got, ref):
+            return True
+        lg, tol = self.logits[t], H * 2.0 ** -24 * self.absl[t]
+        chosen = [int(e) for e in got]
+        if len(set(chosen)) != K_TOP or min(chosen) < 0 or max(chosen) >= E:
+            return False
+        others = [e for e in range(E) if e not in chosen]
+        for r in range(K_TOP):
+            a = chosen[r]
+            for b in chosen[r + 1:] + others:
+                if lg[a] < lg[b] - (tol[a] + tol[b]):
+                    return False
+        return True
+
+    def parity(self, fmt, y_gpu, idx_gpu, w_gpu):
+        """Compare the GPU's first tokens with the oracle: routing exactly (or up to proven near-ties), and y element
+        by element within 1e-3 * sum|terms| + 1e-6 (the FFN of the GPU's own routing, so that a near-tie swap does
+        not mask the FFN's check). NaN must match NaN."""
+        n = len(y_gpu)
+        exact = sum(int(np.array_equal(idx_gpu[t], self.idx[t])) for t in range(n))
+        ties = sum(int(not np.array_equal(idx_gpu[t], self.idx[t]) and self._near_tie(t, idx_gpu[t])) for t in range(n))
+        self._encode(fmt, idx_gpu)
+        with cf.ThreadPoolExecutor(self.cores) as ex:
+            res = list(ex.map(lambda t: self._moe(fmt, idx_gpu[t:t + 1], w_gpu[t:t + 1], self.x[t:t + 1]), range(n)))
+        y_ref = np.concatenate([r[0] for r in res])
+        ab = np.concatenate([r[1] for r in res])
+        y = np.asarray(y_gpu, dtype=np.float64)
+        nan_ok = bool(np.array_equal(np.isnan(y), np.isnan(y_ref)))
+        fin = ~np.isnan(y_ref)
+        ratio = float(np.max(np.abs(y[fin] - y_ref[fin]) / (1e-3 * ab[fin] + 1e-6))) if fin.any() else 0.0
+        ok = nan_ok and ratio <= 1.0 and exact + ties == n
+        return {"tokens": n, "max_err_over_bound": round(ratio, 5), "routing_exact": exact, "routing_near_ties": ties,
+                "tolerance": "|y - y_oracle| <= 1e-3 * sum|terms| + 1e-6 per element", "ok": ok}
 
 
 def main():
@@ -579,10 +732,10 @@ def main():
             return
         t0 = time.time()
         per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
-        co = CpuOracle(args.fmt, args.seed)
+        co = CpuOracle(args.seed, 0)
         for _ in range(args.warmup):
-            co.run(per_step / 4)
-        vals = [co.run(per_step) for _ in range(args.steps)]
+            co.timed(args.fmt, per_step / 4)
+        vals = [co.timed(args.fmt, per_step) for _ in range(args.steps)]
         v = float(np.median([r["value"] for r in vals]))
         cb = dict(vals[0])
         cb["value"] = v
@@ -596,11 +749,25 @@ def main():
                "wall_s": round(time.time() - t0, 1)}
         print(json.dumps(out))
         return
-    out = run_ours(args)
-    if out is not None:
-        if not args.no_cpu_baseline and int(os.environ.get("WORLD_SIZE", "1")) == 1:
-            out["cpu_baseline"] = CpuOracle(args.fmt, args.seed).run(args.cpu_seconds)
-        print(json.dumps(out))
+    out, checks = run_ours(args)
+    if out is None:
+        return
+    single = int(os.environ.get("WORLD_SIZE", "1")) == 1
+    breach = False
+    if single and (checks or not args.no_cpu_baseline):
+        co = CpuOracle(args.seed, max([len(c[2]) for c in checks] + [0]))
+        for key, fmt, y_rows, idx_rows, w_rows in checks:
+            par = co.parity(fmt, y_rows, idx_rows, w_rows)
+            breach |= not par["ok"]
+            if key is None:
+                out["parity"] = par
+            else:
+                out["formats"][key]["parity"] = par
+        if not args.no_cpu_baseline:
+            out["cpu_baseline"] = co.timed(args.fmt, args.cpu_seconds)
+    print(json.dumps(out))
+    if breach:
+        sys.exit(1)
 
 
 if __name__ == "__main__":

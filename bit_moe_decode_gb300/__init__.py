@@ -22,7 +22,7 @@ MOE_MAT_GATE_UP, MOE_MAT_DOWN = 0, 1
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_SHAPE", 3: "MOE_ERR_UNSUPPORTED_FORMAT",
           4: "MOE_ERR_UNSUPPORTED_ARCH", 5: "MOE_ERR_WORKSPACE_TOO_SMALL", 6: "MOE_ERR_CUDA",
-          7: "MOE_ERR_DEVICE_TIMEOUT", 8: "MOE_ERR_FAULT_INJECTED", 9: "MOE_ERR_DEVICE_NAN"}
+          7: "MOE_ERR_DEVICE_TIMEOUT", 8: "MOE_ERR_FAULT_INJECTED"}
 # canonical block geometry: (weights per block, bytes per block)
 BLOCK = {MOE_FMT_MXFP4: (32, 17), MOE_FMT_INT4G32: (32, 18), MOE_FMT_Q2K: (256, 84)}
 

@@ -111,7 +111,6 @@ extern "C" const char* moe_status_string(moe_status_t s) {
     case MOE_ERR_CUDA: return "CUDA runtime error";
     case MOE_ERR_DEVICE_TIMEOUT: return "a device-side wait ran out of time";
     case MOE_ERR_FAULT_INJECTED: return "fault injected (MOE_FAULT)";
-    case MOE_ERR_DEVICE_NAN: return "NaN detected";
   }
   return "unknown status";
 }

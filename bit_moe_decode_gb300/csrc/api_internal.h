@@ -4,8 +4,17 @@
 #include <cstdint>
 
 #include <cuda.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "../../include/moe.h"
+
+// An NVTX range named after the API call around its host-side body (launches included), for timeline tools; with
+// no tool attached a push / pop costs a function-pointer test.
+struct MoeNvtxRange {
+  explicit MoeNvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~MoeNvtxRange() { nvtxRangePop(); }
+};
+#define MOE_NVTX(name) MoeNvtxRange moe_nvtx_range_(name)
 
 namespace moe_internal {
 

@@ -701,6 +701,7 @@ static moe_status_t ffn_common(const char* site, const moe_layer_t* L, const voi
 extern "C" moe_status_t moe_expert_ffn_decode(const moe_layer_t* L, const void* x_bf16, const int32_t* idx,
                                               const float* w, int32_t k, float* y, void* y_bf16, int32_t accumulate,
                                               void* ws, size_t ws_bytes, void* stream) {
+  MOE_NVTX("moe_expert_ffn_decode");
   return ffn_common("decode", L, x_bf16, 1, idx, w, k, y, y_bf16, accumulate, ws, ws_bytes, stream);
 }
 
@@ -710,6 +711,7 @@ extern "C" moe_status_t moe_expert_ffn_decode(const moe_layer_t* L, const void* 
 extern "C" moe_status_t moe_route_expert_ffn(const moe_layer_t* L, const void* router_w_f16, const void* x_bf16, int32_t T,
                                             int32_t k, int32_t* idx, float* w, float* y, void* y_bf16,
                                             int32_t accumulate, void* ws, size_t ws_bytes, void* stream) {
+  MOE_NVTX("moe_route_expert_ffn");
   if (moe_internal::fault("route_ffn")) return MOE_ERR_FAULT_INJECTED;
   if (!L || !router_w_f16 || !x_bf16 || !idx || !w || !y || !ws) return MOE_ERR_INVALID_ARG;
   if (L->layout != MOE_LAYOUT_TC || L->fmt != MOE_FMT_MXFP4) return MOE_ERR_UNSUPPORTED_FORMAT;
@@ -729,6 +731,7 @@ extern "C" moe_status_t moe_route_expert_ffn(const moe_layer_t* L, const void* r
 extern "C" moe_status_t moe_expert_ffn_verify(const moe_layer_t* L, const void* x_bf16, int32_t T, const int32_t* idx,
                                               const float* w, int32_t k, float* y, void* y_bf16, int32_t accumulate,
                                               void* ws, size_t ws_bytes, void* stream) {
+  MOE_NVTX("moe_expert_ffn_verify");
   return ffn_common("verify", L, x_bf16, T, idx, w, k, y, y_bf16, accumulate, ws, ws_bytes, stream);
 }
 
@@ -769,6 +772,7 @@ moe_status_t static_scratch(void** out) {
 extern "C" moe_status_t moe_expert_ffn_decode_static(const moe_layer_t* L, const void* x_bf16, const int32_t* idx,
                                                      const float* w, int32_t k, float* y, void* y_bf16,
                                                      int32_t accumulate, void* stream) {
+  MOE_NVTX("moe_expert_ffn_decode_static");
   if (moe_internal::fault("decode")) return MOE_ERR_FAULT_INJECTED;
   if (!L || !x_bf16 || !idx || !w || !y) return MOE_ERR_INVALID_ARG;
   if (k < 1 || k > kMaxK || !moe_internal::shape_ok(L->H, L->I)) return MOE_ERR_SHAPE;

@@ -347,6 +347,7 @@ static int grid_for(int64_t n, int threads) {
 
 extern "C" moe_status_t moe_encode_blocks(moe_format_t fmt, const float* src, int64_t rows, int64_t k, void* dst,
                                           void* stream) {
+  MOE_NVTX("moe_encode_blocks");
   if (moe_internal::fault("encode")) return MOE_ERR_FAULT_INJECTED;
   if (fmt < MOE_FMT_MXFP4 || fmt > MOE_FMT_Q2K) return MOE_ERR_UNSUPPORTED_FORMAT;
   if (!src || !dst || rows < 0 || k < 0) return MOE_ERR_INVALID_ARG;
@@ -368,6 +369,7 @@ extern "C" moe_status_t moe_encode_blocks(moe_format_t fmt, const float* src, in
 extern "C" moe_status_t moe_pack_weights(moe_format_t fmt, moe_src_t src_kind, moe_layout_t layout, moe_matrix_t kind,
                                          int64_t n_e, int64_t H, int64_t I, const void* src_a, const void* src_b,
                                          void* dst, size_t dst_bytes, void* stream) {
+  MOE_NVTX("moe_pack_weights");
   if (moe_internal::fault("pack")) return MOE_ERR_FAULT_INJECTED;
   if (fmt < MOE_FMT_MXFP4 || fmt > MOE_FMT_Q2K) return MOE_ERR_UNSUPPORTED_FORMAT;
   if (src_kind != MOE_SRC_BLOCKS && src_kind != MOE_SRC_F32) return MOE_ERR_INVALID_ARG;

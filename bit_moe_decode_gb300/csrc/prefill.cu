@@ -655,6 +655,7 @@ extern "C" size_t moe_prefill_workspace_bytes(const moe_layer_t* L, int32_t T_ma
 extern "C" moe_status_t moe_expert_grouped_gemm_prefill(const moe_layer_t* layer, const void* x_bf16, int32_t T,
                                                         const int32_t* idx, const float* w, int32_t k, float* y,
                                                         void* y_bf16, void* ws, size_t ws_bytes, void* stream) {
+  MOE_NVTX("moe_expert_grouped_gemm_prefill");
   return pf::run(layer, x_bf16, T, idx, w, k, y, y_bf16, ws, ws_bytes, nullptr, stream);
 }
 

@@ -104,6 +104,7 @@ using namespace moe;
 extern "C" moe_status_t moe_route_topk(const void* router_w_f16, const void* x_bf16, int32_t T, int32_t H, int32_t E,
                                        int32_t k, const int32_t* token_ids, const int32_t* tid2eid, int32_t V,
                                        int32_t* idx, float* weights, void* stream) {
+  MOE_NVTX("moe_route_topk");
   if (moe_internal::fault("route")) return MOE_ERR_FAULT_INJECTED;
   if (!idx || !weights) return MOE_ERR_INVALID_ARG;
   if (T < 1 || k < 1 || k > 8) return MOE_ERR_SHAPE;

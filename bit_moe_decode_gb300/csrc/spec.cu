@@ -207,6 +207,7 @@ using namespace moe;
 
 extern "C" moe_status_t moe_spec_accept(const float* p, const float* q, int32_t K, int32_t V, const int32_t* draft,
                                         const float* u, int32_t* result, void* stream) {
+  MOE_NVTX("moe_spec_accept");
   if (moe_internal::fault("spec")) return MOE_ERR_FAULT_INJECTED;
   if (!p || !u || !result || (K > 0 && (!q || !draft))) return MOE_ERR_INVALID_ARG;
   if (((uintptr_t)p & 3) || ((uintptr_t)q & 3) || ((uintptr_t)u & 3) || ((uintptr_t)draft & 3) ||

@@ -63,8 +63,7 @@ typedef enum {
   MOE_ERR_WORKSPACE_TOO_SMALL = 5,
   MOE_ERR_CUDA = 6,                /* a CUDA runtime call or launch failed */
   MOE_ERR_DEVICE_TIMEOUT = 7,      /* a bounded device-side wait ran out (see moe_get_device_status) */
-  MOE_ERR_FAULT_INJECTED = 8,      /* MOE_FAULT named this call */
-  MOE_ERR_DEVICE_NAN = 9           /* reserved */
+  MOE_ERR_FAULT_INJECTED = 8       /* MOE_FAULT named this call */
 } moe_status_t;
 
 const char* moe_status_string(moe_status_t s);
@@ -159,9 +158,17 @@ moe_status_t moe_get_device_status(void* ws, void* stream);
 /* Decode, one token: y[H] (=, or += if accumulate) sum_r w[r] * FFN_{idx[r]}(x).
  *   x_bf16 [H] bf16; idx [k] int32 (expert ids < E); w [k] fp32; y [H] fp32; y_bf16 [H] bf16 or NULL
  *   (round-to-nearest-even copy of y). Equivalent to moe_expert_ffn_verify with T = 1.
- * Numerics: x is rescaled per token by a power of two and held in binary16 (exact for every element within
- * 2^-28 of the token's largest |x|); weights are exact; h is fp32, rescaled per (expert, token) by a power of two
- * into binary16 for the down projection; sums are fp32 on tensor cores. */
+ * Numerics depend on the layer's layout; in both the weights are exact and the sums are fp32.
+ *   MOE_LAYOUT_DECODE (mat-vec kernels, every format): x is rescaled per token by a power of two and held in
+ *   binary16 (exact for every element within 2^-28 of the token's largest |x|); h is fp32, rescaled per (expert,
+ *   token) by a power of two into binary16 for the down projection.
+ *   MOE_LAYOUT_TC (MXFP4, block-scaled tcgen05 MMAs, "quantization" glossary, "MXFP4"): x, and h = SiLU(g) * u
+ *   formed in fp32, are each carried as the sum of 6 E2M1 parts per 32-block with their own E8M0 exponents
+ *   (part p at exponent e0 - 2p quantises what parts 0..p-1 left). The error of an element is below 1/3072 of the
+ *   largest |value| of ITS 32-block, not of the element: in a block with one outlier, the other 31 elements carry
+ *   errors up to ~outlier/3072. The parity tests hold y to 1e-3 * sum|terms| per element on N(0,1) x, on x with
+ *   one element per block scaled by 2^8 .. 2^12 (also over zero weight columns), Student-t(3) x, and x with
+ *   exact zeros and bf16 subnormals. A block holding NaN or infinity makes its parts NaN (E8M0 exponent 255). */
 moe_status_t moe_expert_ffn_decode(const moe_layer_t* layer, const void* x_bf16, const int32_t* idx, const float* w,
                                    int32_t k, float* y, void* y_bf16, int32_t accumulate, void* ws, size_t ws_bytes,
                                    void* stream);
