@@ -64,6 +64,8 @@ def parse():
                    help="weight layout of the decode path: tc (MXFP4, tcgen05 kernels) or decode (mat-vec kernels); "
                         "auto = tc for MXFP4, decode otherwise")
     p.add_argument("--no-formats", action="store_true", help="measure only the --fmt / --layout path")
+    p.add_argument("--no-stack", action="store_true", help="skip the 43-layer stack measurement")
+    p.add_argument("--stack-tokens", type=int, default=64, help="tokens per timed pass of the 43-layer stack")
     p.add_argument("--no-parity", action="store_true", help="skip the oracle comparison of the timed tokens")
     p.add_argument("--parity-tokens", type=int, default=32)
     p.add_argument("--prefill-tokens", type=int, default=4096,
@@ -350,6 +352,9 @@ def run_ours(args):
         if rows is not None:
             checks.append((key, lx.fmt) + rows)
     prefill = bench_prefill(m, torch, args, dev, stream, layer_p, E) if do_prefill else None
+    stack = None
+    if not args.no_stack and world == 1 and fmt == 1:
+        stack = bench_stack(m, torch, args, dev, stream)
     verify = bench_verify(m, torch, args, dev, stream, layer, wr, x_host, E, per_expert) if (use_tc and not args.no_verify) else None
     spec = bench_spec(m, torch, dev, stream) if not args.no_verify else None
 
@@ -392,6 +397,7 @@ def run_ours(args):
                     "h2d_bytes_per_step": int(T * H * 2), "d2h_bytes_per_step": int(T * H * 4)},
             "clocks": clk,
             "formats": formats,
+            "stack": stack,
             "prefill": prefill,
             "verify": verify,
             "spec_accept": spec,
@@ -483,6 +489,98 @@ def bench_format(m, torch, args, dev, stream, layer, wr, x, x_host, npar):
                    "d2h_bytes_per_step": int(T * H * 4)}}
     rows = (y[:npar].cpu().numpy(), idx[:npar].cpu().numpy(), w[:npar].cpu().numpy()) if npar else None
     return res, rows
+
+
+def bench_stack(m, torch, args, dev, stream, n_layers=43, n_hash=3, vocab=32768):
+    """The whole routed-expert stack: 43 layers x 256 MXFP4 experts in the tensor-core layout (147 GB, generated on
+    the GPU: seeded N(0, 0.02) fp32 per expert, packed by the library's encoder), layers 0-2 routed by a seeded
+    tid2eid table (vocab 32768, 6 distinct experts, w = 1/6), layers 3-42 by their own fp16 router (fused into the
+    FFN launch); layer L + 1's x = bf16(y_L). Decode: args.stack_tokens tokens one at a time, all layers, as a CUDA
+    graph; verify: the same tokens in batches of T = 2, 4, 8 (independent routing: each layer sweeps the union of
+    the batch's experts). Algorithmic bytes = packed bytes of each layer's union of experts, summed over layers."""
+    from bit_moe_decode_gb300.stack import RoutedStack
+    from moe_inputs import tid2eid, token_ids, x_bf16_bits
+    per_expert = m.moe_packed_bytes(1, 1, 0, 1, H, I) + m.moe_packed_bytes(1, 1, 1, 1, H, I)
+    need = n_layers * E * per_expert
+    free, _ = torch.cuda.mem_get_info(dev)
+    if free < need + (8 << 30):
+        return {"skipped": "needs %.1f GB of free device memory, %.1f GB free" % (need / 1e9, free / 1e9)}
+    t0 = time.time()
+    st = RoutedStack(H, I, E, K_TOP, n_layers, n_hash, vocab, T_max=8, device=dev)
+    gen = torch.Generator(device=dev)
+    batch = 32
+    for L in range(n_layers):
+        gen.manual_seed(args.seed * 1000 + L)
+        for e0 in range(0, E, batch):
+            g = torch.randn((batch, I, H), generator=gen, device=dev).mul_(0.02)
+            u = torch.randn((batch, I, H), generator=gen, device=dev).mul_(0.02)
+            d = torch.randn((batch, H, I), generator=gen, device=dev).mul_(0.02)
+            st.layers[L].pack(m.MOE_SRC_F32, g, u, d, e0=e0, stream=torch.cuda.current_stream(dev))
+        if L < n_hash:
+            st.tid2eid[L] = torch.from_numpy(tid2eid(args.seed, L, vocab, E, K_TOP)).to(dev)
+        else:
+            st.router[L] = (torch.randn((E, H), generator=gen, device=dev) * 0.02).half().view(torch.int16)
+    del g, u, d
+    torch.cuda.synchronize()
+    setup_s = time.time() - t0
+    N = max(8, (args.stack_tokens // 8) * 8)
+    toks = torch.from_numpy(token_ids(args.seed, N, vocab)).to(dev)
+    xs = torch.from_numpy(x_bf16_bits(args.seed + 31, range(N), H).view(np.int16)).to(dev)
+
+    res, unions = {}, {}
+    for T in (1, 2, 4, 8):
+        def launch(T=T):
+            for j in range(N // T):
+                st.run(T, token_ids=toks[j * T:(j + 1) * T], x0=xs[j * T:(j + 1) * T], stream=stream)
+        # the routing of every pass (eager, once): each layer's union of experts over the batch
+        us = []
+        for j in range(N // T):
+            with torch.cuda.stream(stream):
+                st.run(T, token_ids=toks[j * T:(j + 1) * T], x0=xs[j * T:(j + 1) * T], stream=stream)
+            stream.synchronize()
+            us.append([len(np.unique(st.idx[L][:T].cpu().numpy())) for L in range(n_layers)])
+        unions[T] = float(np.mean(np.sum(us, axis=1)))   # union sizes summed over the layers, per pass
+        if m.moe_get_device_status(st.ws, stream) != 0:
+            raise RuntimeError("device status after the stack's eager pass (T = %d)" % T)
+        g_ = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_, stream=stream):
+            launch()
+        times = []
+        for _ in range(max(1, args.warmup)):
+            with torch.cuda.stream(stream):
+                g_.replay()
+        for _ in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            with torch.cuda.stream(stream):
+                g_.replay()
+            e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+        res[T] = float(np.median(times)) / (N // T)   # ms per pass of T tokens
+        if m.moe_get_device_status(st.ws, stream) != 0:
+            raise RuntimeError("device status after the stack (T = %d)" % T)
+    peak = peak_of(measured_peaks(), "hbm_gbs") or 6800.0
+    t1 = res[1]
+    bytes1 = unions[1] * per_expert
+    out = {"workload": "%d layers x %d MXFP4 experts (%.1f GB resident, generated on the GPU), layers 0-%d hash-routed "
+                       "(tid2eid, vocab %d), the rest softmax top-%d (router fused), layer L+1's x = bf16(y_L); %d "
+                       "tokens per timed pass" % (n_layers, E, st.packed_bytes() / 1e9, n_hash - 1, vocab, K_TOP, N),
+           "decode": {"tok_s": round(1e3 / t1, 2), "us_per_token": round(t1 * 1e3, 2),
+                      "bytes_per_token": bytes1, "gbs": round(bytes1 / (t1 * 1e-3) / 1e9, 1),
+                      "roofline": {"bound": "hbm", "achieved": round(bytes1 / (t1 * 1e-3) / 1e9, 1), "peak": peak,
+                                   "unit": "GB/s", "frac": round(bytes1 / (t1 * 1e-3) / 1e9 / peak, 4),
+                                   "traffic": None},
+                      "gpu_launches_per_token": st.launches_per_run()},
+           "verify": {"us_per_pass": {str(T): round(res[T] * 1e3, 2) for T in res},
+                      "tok_s": {str(T): round(T * 1e3 / res[T], 2) for T in res},
+                      "union_experts_over_layers": {str(T): round(unions[T], 1) for T in res},
+                      "raw_ratio": {str(T): round(res[T] / t1, 3) for T in res},
+                      "per_union_byte_ratio": {str(T): round(res[T] / (t1 * unions[T] / unions[1]), 3) for T in res}},
+           "setup_s": round(setup_s, 1)}
+    del st
+    torch.cuda.empty_cache()
+    return out
 
 
 def bench_verify(m, torch, args, dev, stream, layer, wr, x_host, E, per_expert):

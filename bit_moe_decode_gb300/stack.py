@@ -1,0 +1,65 @@
+"""A stack of routed-expert layers run in sequence through the C ABI: the whole routed-expert path of a
+DeepSeek-V4-Flash-shaped model for decode and verify ("Mixed-precision compression of DeepSeek-V4-Flash",
+"The recipe": 43 layers x 256 experts, top-6; "quant surgery", section 4: the first layers route by a token-id
+hash table, tid2eid).
+
+Per layer L of a call with T tokens (1 <= T <= 8):
+  hash layers (L < n_hash):  moe_route_topk in hash mode (idx = tid2eid[token id], w = 1/k), then
+                             moe_expert_ffn_verify;
+  softmax layers:            moe_route_expert_ffn (router top-k and FFN in one launch).
+Layer L + 1's x is the bf16 (round-to-nearest-even) copy of layer L's y, which the FFN call writes itself; there
+is no attention or residual in between (they are not on the routed-expert path). Everything here only orders
+library calls on one stream; all arithmetic runs in the library's kernels.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (MOE_FMT_MXFP4, MOE_LAYOUT_TC, Layer, moe_expert_ffn_verify, moe_route_expert_ffn,
+               moe_route_topk)
+
+
+class RoutedStack:
+    """n_layers MXFP4 layers in the tensor-core layout (H, I, E experts each), hash routing in the first n_hash.
+
+    Buffers (device): x[L] bf16 [T_max, H] for L = 0..n_layers (x[0] is the default input, x[L + 1] the output of
+    layer L), idx[L] int32 / w[L] fp32 [T_max, k] (the routing each layer used), y[L] fp32 [T_max, H] (each layer's
+    fp32 output), one shared workspace (the calls run one after another on the stream)."""
+
+    def __init__(self, H: int, I: int, E: int, k: int, n_layers: int, n_hash: int, vocab: int, T_max: int = 8,
+                 device="cuda"):
+        assert 0 <= n_hash <= n_layers and 1 <= T_max <= 8
+        self.H, self.I, self.E, self.k, self.n, self.n_hash, self.vocab, self.T_max = \
+            H, I, E, k, n_layers, n_hash, vocab, T_max
+        self.layers = [Layer(MOE_FMT_MXFP4, H, I, E, layout=MOE_LAYOUT_TC, device=device) for _ in range(n_layers)]
+        self.router = [None] * n_layers          # fp16 bits [E, H] (int16 tensors) of the softmax layers
+        self.tid2eid = [None] * n_layers         # int32 [vocab, k] of the hash layers
+        self.x = [torch.zeros((T_max, H), dtype=torch.int16, device=device) for _ in range(n_layers + 1)]
+        self.idx = [torch.zeros((T_max, k), dtype=torch.int32, device=device) for _ in range(n_layers)]
+        self.w = [torch.zeros((T_max, k), dtype=torch.float32, device=device) for _ in range(n_layers)]
+        self.y = [torch.zeros((T_max, H), dtype=torch.float32, device=device) for _ in range(n_layers)]
+        self.ws = self.layers[0].workspace(T_max, k) if n_layers else None
+
+    def packed_bytes(self) -> int:
+        return sum(L.gate_up.numel() + L.down.numel() for L in self.layers)
+
+    def run(self, T: int, token_ids=None, x0=None, stream=None):
+        """One decode (T = 1) or verify (T <= 8) pass of T tokens through every layer: the first layer reads x0
+        (bf16 [T, H], device) or, if None, x[0][:T]. token_ids (int32 [T], device) is needed when the stack has
+        hash layers."""
+        assert 1 <= T <= self.T_max
+        for L in range(self.n):
+            xin = x0 if (L == 0 and x0 is not None) else self.x[L][:T]
+            xout = self.x[L + 1][:T]
+            idx, w = self.idx[L][:T], self.w[L][:T]
+            if L < self.n_hash:
+                moe_route_topk(None, None, T, self.H, self.E, self.k, token_ids, self.tid2eid[L], self.vocab, idx, w,
+                               stream=stream)
+                moe_expert_ffn_verify(self.layers[L], xin, T, idx, w, self.k, self.y[L][:T], xout, False, self.ws,
+                                      stream=stream)
+            else:
+                moe_route_expert_ffn(self.layers[L], self.router[L], xin, T, self.k, idx, w, self.y[L][:T], xout,
+                                     False, self.ws, stream=stream)
+
+    def launches_per_run(self) -> int:
+        return 2 * self.n_hash + (self.n - self.n_hash)
