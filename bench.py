@@ -423,7 +423,7 @@ def bench_format(m, torch, args, dev, stream, layer, wr, x, x_host, npar):
 
     def step_launch():
         for t in range(T):
-            m.moe_route_topk(wr, x[t], 1, H, E, K_TOP, None, None, 0, idx[t], w[t], stream=stream)
+            m.moe_route_topk(wr, x[t], 1, H, layer.E, K_TOP, None, None, 0, idx[t], w[t], stream=stream)
             m.moe_expert_ffn_decode(layer, x[t], idx[t], w[t], K_TOP, y[t], None, False, ws, stream=stream)
 
     def ffn_launch():
@@ -739,14 +739,15 @@ class CpuOracle:
     layer): its own routing of them, encoded experts per format (built once, before any timing), the timed sample
     of the CPU baseline and the parity check of the GPU's outputs."""
 
-    def __init__(self, seed, n):
+    def __init__(self, seed, n, n_experts=E):
         import oracle
         from moe_inputs import router_f16_bits, x_bf16_bits
         self.oracle = oracle
         self.seed = seed
+        self.E = n_experts
         self.cores = os.cpu_count() or 1
         self.n = max(int(n), self.cores)
-        wr = router_f16_bits(seed, 0, E, H)
+        wr = router_f16_bits(seed, 0, self.E, H)
         self.x = x_bf16_bits(seed, range(self.n), H)
         self.idx, self.w, self.logits, self.absl = oracle.route_topk(wr, self.x, K_TOP)
         self.enc = {}
@@ -791,9 +792,9 @@ class CpuOracle:
             return True
         lg, tol = self.logits[t], H * 2.0 ** -24 * self.absl[t]
         chosen = [int(e) for e in got]
-        if len(set(chosen)) != K_TOP or min(chosen) < 0 or max(chosen) >= E:
+        if len(set(chosen)) != K_TOP or min(chosen) < 0 or max(chosen) >= self.E:
             return False
-        others = [e for e in range(E) if e not in chosen]
+        others = [e for e in range(self.E) if e not in chosen]
         for r in range(K_TOP):
             a = chosen[r]
             for b in chosen[r + 1:] + others:
@@ -830,7 +831,7 @@ def main():
             return
         t0 = time.time()
         per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
-        co = CpuOracle(args.seed, 0)
+        co = CpuOracle(args.seed, 0, args.experts)
         for _ in range(args.warmup):
             co.timed(args.fmt, per_step / 4)
         vals = [co.timed(args.fmt, per_step) for _ in range(args.steps)]
@@ -853,7 +854,7 @@ def main():
     single = int(os.environ.get("WORLD_SIZE", "1")) == 1
     breach = False
     if single and (checks or not args.no_cpu_baseline):
-        co = CpuOracle(args.seed, max([len(c[2]) for c in checks] + [0]))
+        co = CpuOracle(args.seed, max([len(c[2]) for c in checks] + [0]), args.experts)
         for key, fmt, y_rows, idx_rows, w_rows in checks:
             par = co.parity(fmt, y_rows, idx_rows, w_rows)
             breach |= not par["ok"]

@@ -570,10 +570,12 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
     // task q = blockIdx.x + gridDim.x * (w + 2 NPIPE i), e = q / 2, c = q % 2, w = warp - 2, spread over the grid
     for (int q = (int)blockIdx.x + (int)gridDim.x * (warp - 2); q < 2 * g.E; q += (int)gridDim.x * 2 * NPIPE) {
       const int e = q >> 1, c = q & 1;
-      float acc[kRouteTPC];
-      route_half_logits<8>(a.wr + (size_t)e * g.H, g.H, g.T, [&](int t) { return a.x + (size_t)t * g.H; }, c, acc);
+      float acc[TT];
+      route_half_logits<8, TT>(a.wr + (size_t)e * g.H, g.H, g.T, [&](int t) { return a.x + (size_t)t * g.H; }, c, acc);
       if (lane == 0)
-        for (int t = 0; t < g.T; ++t) __stcg(lgw + (t * 2 + c) * g.E + e, acc[t]);
+#pragma unroll
+        for (int t = 0; t < TT; ++t)
+          if (t < g.T) __stcg(lgw + (t * 2 + c) * g.E + e, acc[t]);
       __syncwarp();
       if (lane == 0) red_release_add(cnt + C_ROUTE, 1u);
     }
@@ -910,24 +912,32 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
       };
       // drain the unit's accumulators (W columns each; column 6 t + p = part p of token or slot t, summed in part
       // order): two at a time with one wait when W = 16; the region is handed back after its last load
-      const int hstep = g.W == 16 ? 2 : 1;
+      const int hstep = TT <= 2 ? 2 : 1;  // accumulators drained per TMEM-load wait
       for (int h0 = 0; h0 < nuse && good; h0 += hstep) {
         const int nh = nuse - h0 < hstep ? nuse - h0 : hstep;
         float acc0[TT], acc1[TT];
 #pragma unroll
         for (int t = 0; t < TT; ++t) { acc0[t] = 0.f; acc1[t] = 0.f; }
-        if (g.W == 16) {
-          uint32_t v0[16], v1[16];
-          tc_ld16(rbase + 16 * h0, v0);
-          if (nh == 2) tc_ld16(rbase + 16 * h0 + 16, v1);
+        if constexpr (TT <= 2) {
+          // W = 16 and columns 0..11 at most hold parts (T <= 2): 8 + 4 columns per accumulator, the padding is
+          // not read
+          uint32_t a0[8], b0[4], a1[8], b1[4];
+          tc_ld8(rbase + 16 * h0, a0);
+          if (g.T == 2) tc_ld4(rbase + 16 * h0 + 8, b0);
+          if (nh == 2) {
+            tc_ld8(rbase + 16 * h0 + 16, a1);
+            if (g.T == 2) tc_ld4(rbase + 16 * h0 + 24, b1);
+          }
           tc_wait_ld();
 #pragma unroll
-          for (int cc = 0; cc < 16; ++cc)
-            if (cc / PARTS < TT) acc0[cc / PARTS] += __uint_as_float(v0[cc]);
+          for (int cc = 0; cc < 12; ++cc)  // part order, as for the wider accumulators
+            if (cc / PARTS < TT && (cc < 6 || g.T == 2))
+              acc0[cc / PARTS] += __uint_as_float(cc < 8 ? a0[cc & 7] : b0[cc & 3]);
           if (nh == 2)
 #pragma unroll
-            for (int cc = 0; cc < 16; ++cc)
-              if (cc / PARTS < TT) acc1[cc / PARTS] += __uint_as_float(v1[cc]);
+            for (int cc = 0; cc < 12; ++cc)
+              if (cc / PARTS < TT && (cc < 6 || g.T == 2))
+                acc1[cc / PARTS] += __uint_as_float(cc < 8 ? a1[cc & 7] : b1[cc & 3]);
         } else {
 #pragma unroll
           for (int cb = 0; cb < WMAX / 16; ++cb) {

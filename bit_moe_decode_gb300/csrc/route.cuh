@@ -18,14 +18,15 @@ constexpr int kRouteMaxE = 1024;
 // pieces at h = 8 l + 256 i for i in [c P2, min(P, (c + 1) P2)), P = H / 256, P2 = ceil(P / 2), with fused
 // multiply-adds; then a fixed butterfly (xor 16, 8, 4, 2, 1) adds the lanes. The logit is half 0 + half 1, so the
 // two halves can be computed by different warps. xrow(t) points at token t's x (shared or global memory); BATCH
-// pieces per lane are loaded before they are used (it changes when the loads are issued, not the sums).
-template <int BATCH, typename XRow>
+// pieces per lane are loaded before they are used (it changes when the loads are issued, not the sums). NT is the
+// most tokens a caller passes (nt <= NT): it only sizes the unrolled code, not any token's sum.
+template <int BATCH, int NT, typename XRow>
 __device__ __forceinline__ void route_half_logits(const uint16_t* __restrict__ row, int H, int nt, XRow xrow, int c,
-                                                  float (&acc)[kRouteTPC]) {
+                                                  float (&acc)[NT]) {
   const int lane = threadIdx.x & 31;
   const int P = H / 256, P2 = (P + 1) / 2, i_beg = c * P2, i_end = min(P, (c + 1) * P2);
 #pragma unroll
-  for (int t = 0; t < kRouteTPC; ++t) acc[t] = 0.f;
+  for (int t = 0; t < NT; ++t) acc[t] = 0.f;
   for (int i0 = i_beg; i0 < i_end; i0 += BATCH) {
     uint4 wv[BATCH];
 #pragma unroll
@@ -45,7 +46,7 @@ __device__ __forceinline__ void route_half_logits(const uint16_t* __restrict__ r
         wf[2 * j + 1] = __half2float(__ushort_as_half((unsigned short)(ww[j] >> 16)));
       }
 #pragma unroll
-      for (int t = 0; t < kRouteTPC; ++t) {
+      for (int t = 0; t < NT; ++t) {
         if (t < nt) {
           const uint4 xv = *reinterpret_cast<const uint4*>(xrow(t) + h);
           const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
@@ -59,7 +60,7 @@ __device__ __forceinline__ void route_half_logits(const uint16_t* __restrict__ r
     }
   }
 #pragma unroll
-  for (int t = 0; t < kRouteTPC; ++t) {
+  for (int t = 0; t < NT; ++t) {
     float v = acc[t];
     v += __shfl_xor_sync(0xffffffffu, v, 16);
     v += __shfl_xor_sync(0xffffffffu, v, 8);
@@ -74,8 +75,8 @@ template <int BATCH, typename XRow>
 __device__ __forceinline__ void route_row_logits(const uint16_t* __restrict__ row, int H, int nt, XRow xrow,
                                                  float (&acc)[kRouteTPC]) {
   float h1[kRouteTPC];
-  route_half_logits<BATCH>(row, H, nt, xrow, 0, acc);
-  route_half_logits<BATCH>(row, H, nt, xrow, 1, h1);
+  route_half_logits<BATCH, kRouteTPC>(row, H, nt, xrow, 0, acc);
+  route_half_logits<BATCH, kRouteTPC>(row, H, nt, xrow, 1, h1);
 #pragma unroll
   for (int t = 0; t < kRouteTPC; ++t) acc[t] = acc[t] + h1[t];
 }
