@@ -31,9 +31,10 @@
 // warp per (token, 32 rows, rank): a lane per row, the slices in order).
 //
 // Inside a CTA, three independent pipelines take the CTA's units as they free up: a copy-issuing warp, an
-// MMA-issuing warp, a three-slot shared-memory ring, TMEM accumulators and a group of
-// four epilogue warps. A helper warp does the work that waits on global memory (storing and counting export
-// partials, forming the h of imported slices) so that no epilogue group stalls on it. One issuing thread sustains only about one wait-and-issue round per 330 ns (TMA) or one
+// MMA-issuing warp, a shared-memory ring of three or four stage slots, TMEM accumulators and a group of four
+// epilogue warps. Two helper warps do the work that waits on global memory (storing and counting export partials;
+// forming the h of imported slices, which they share) so that no epilogue group stalls on it. One issuing thread
+// sustains only about one wait-and-issue round per 330 ns (TMA) or one
 // stage of MMAs plus commit per ~600 cycles (tcgen05), while one SM must consume an 8.5 KB weight tile every
 // ~180 ns to keep pace with HBM. Every wait is bounded; on a timeout the kernel records MOE_ERR_DEVICE_TIMEOUT, lets
 // its own copies land, frees TMEM and returns. With a router (moe_route_expert_ffn), warps 2..7 of every CTA first
@@ -74,12 +75,13 @@ constexpr int MAX_SG = 8;                // segments per slice at most
 constexpr int RMAX = 256;                // split slices at most (fewer than the CTAs)
 constexpr int EPI_WARP0 = 2 * NPIPE;     // warps: NPIPE producers, NPIPE MMA issuers (each issuing thread has a warp
 constexpr int NGRP = NPIPE;              // of its own: issuing lanes of one warp run one after another), then the epilogue
-constexpr int QN = 32;                   // groups of 4 warps (group j drains pipeline j), then the helper warp;
+constexpr int QN = 32;                   // groups of 4 warps (group j drains pipeline j), then the helper warps;
 constexpr int HELPER = EPI_WARP0 + 4 * NGRP;  // unit-queue entries per pipeline
-constexpr int THREADS = (HELPER + 1) * 32;
+constexpr int NHELP = 2;                 // helper warps (20 warps in all: 96 registers a thread)
+constexpr int THREADS = (HELPER + NHELP) * 32;
 // named barriers: 0 the CTA, 1..NGRP the epilogue groups, NB_ROUTE warps 0..EPI_WARP0-1 (routing), NB_TAB / NB_TAB2
-// the routing tables handed from warp 0 to the other warps
-constexpr int NB_ROUTE = 2 + NGRP, NB_TAB = NB_ROUTE + 1, NB_TAB2 = NB_ROUTE + 2;
+// the routing tables handed from warp 0 to the other warps, NB_HELP the helper warps
+constexpr int NB_ROUTE = 2 + NGRP, NB_TAB = NB_ROUTE + 1, NB_TAB2 = NB_ROUTE + 2, NB_HELP = NB_ROUTE + 3;
 constexpr uint32_t TMEM_COLS = 512;      // accumulators below SF_COL0, 8 scale columns per slot from there
 constexpr uint32_t SF_COL0 = TMEM_COLS - 8 * NSLOT;
 static_assert(SF_COL0 + 8 * NSLOT <= TMEM_COLS, "TMEM budget");
@@ -351,6 +353,7 @@ struct Tables {
   int8_t pu[MAX_T][MAX_K];
   int8_t ps[MAX_T][MAX_K];
   int16_t col0[MAX_U];
+  uint32_t tmask[MAX_U];   // bit t: token t routes to union expert u
   float w[MAX_T][MAX_K];
   int U;
   int bad;
@@ -378,24 +381,56 @@ __device__ void build_union_warp(Tables& tb, const int32_t (*idx)[MAX_K], int T,
     tb.bad = bad ? 1 : 0;
   }
 }
-// (2) one thread: weights, each union expert's tokens, per (t, r) the union index and slot, the column bases
-__device__ void build_slots(Tables& tb, const int32_t (*idx)[MAX_K], const float (*w)[MAX_K], int T, int k) {
-  for (int u = 0; u < tb.U; ++u) tb.ntok[u] = 0;
-  for (int t = 0; t < T; ++t)
-    for (int r = 0; r < k; ++r) {
-      tb.w[t][r] = w[t][r];
-      const int e = idx[t][r];
-      int u = 0;
-      while (u < tb.U && tb.ue[u] != e) ++u;
-      if (u == tb.U) { tb.pu[t][r] = 0; tb.ps[t][r] = 0; continue; }  // an invalid id (no units run)
-      int s = 0;
-      while (s < tb.ntok[u] && tb.tok[u][s] != t) ++s;
-      if (s == tb.ntok[u]) { tb.tok[u][s] = (int8_t)t; tb.ntok[u] = (int8_t)(s + 1); }
-      tb.pu[t][r] = (int8_t)u;
-      tb.ps[t][r] = (int8_t)s;
-    }
-  int c = 0;
-  for (int u = 0; u < tb.U; ++u) { tb.col0[u] = (int16_t)c; c += tb.ntok[u]; }
+// (2) one warp: weights, each union expert's tokens, per (t, r) the union index and slot, the column bases. A lane
+// per (t, r) entry (two when T k > 32): its union index by search, the union experts' token sets as bit masks, a
+// token's slot = the number of earlier tokens in its expert's set (slot order = token order).
+__device__ void build_slots_warp(Tables& tb, const int32_t (*idx)[MAX_K], const float (*w)[MAX_K], int T, int k) {
+  const int lane = threadIdx.x & 31;
+  const int n = T * k, U = tb.U;
+  for (int u = lane; u < MAX_U; u += 32) tb.tmask[u] = 0u;
+  __syncwarp();
+  int uu[2] = {0, 0};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int i = lane + 32 * h;
+    if (i >= n) continue;
+    const int t = i / k, r = i % k, e = idx[t][r];
+    int u = 0;
+    while (u < U && tb.ue[u] != e) ++u;
+    uu[h] = u;
+    tb.w[t][r] = w[t][r];
+    if (u < U) atomicOr(&tb.tmask[u], 1u << t);
+  }
+  __syncwarp();
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int i = lane + 32 * h;
+    if (i >= n) continue;
+    const int t = i / k, r = i % k, u = uu[h];
+    const bool valid = u < U;  // an invalid id: no units run
+    tb.pu[t][r] = (int8_t)(valid ? u : 0);
+    tb.ps[t][r] = (int8_t)(valid ? __popc(tb.tmask[u] & ((1u << t) - 1u)) : 0);
+  }
+  // per union expert: its token count and tokens; the column bases are the exclusive prefix sums of the counts
+  int cnt[2] = {0, 0};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int u = lane + 32 * h;
+    if (u >= U) continue;
+    uint32_t m = tb.tmask[u];
+    cnt[h] = __popc(m);
+    tb.ntok[u] = (int8_t)cnt[h];
+    for (int s = 0; m; ++s, m &= m - 1u) tb.tok[u][s] = (int8_t)(__ffs(m) - 1);
+  }
+  int x0 = cnt[0], x1 = cnt[1];  // inclusive scans of the two halves
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y0 = __shfl_up_sync(0xFFFFFFFFu, x0, o), y1 = __shfl_up_sync(0xFFFFFFFFu, x1, o);
+    if (lane >= o) { x0 += y0; x1 += y1; }
+  }
+  const int total0 = __shfl_sync(0xFFFFFFFFu, x0, 31);
+  if (lane < U) tb.col0[lane] = (int16_t)(x0 - cnt[0]);
+  if (lane + 32 < U) tb.col0[lane + 32] = (int16_t)(total0 + x1 - cnt[1]);
 }
 
 // ------------------------------------------------------------------ x parts
@@ -485,28 +520,25 @@ __device__ void finalize_local(const float* part, int64_t seg_stride, int SG, in
   }
   h_padding(img, ntok, W, et, 128);
 }
-// imported slice, by the helper warp, partials in global memory: both blocks of a slot loaded before any sum
+// imported slice, by the helper warps (helper hw of NHELP takes the 32-blocks q = 2 slot + half with q = hw mod
+// NHELP), partials in global memory
 __device__ void finalize_import(const float* part, int64_t seg_stride, int SG, int ntok, const int8_t* tok, int W,
-                                uint8_t* img) {
+                                uint8_t* img, int hw) {
   const int lane = threadIdx.x & 31;
-  for (int s = 0; s < ntok; ++s) {
-    const float* p = part + tok[s] * 128 + lane;
-    float gl[2][MAX_SG], ul[2][MAX_SG];
+  for (int q = hw; q < 2 * ntok; q += NHELP) {
+    const int s = q >> 1, b = q & 1;
+    const float* p = part + tok[s] * 128 + 32 * b + lane;
+    float gl[MAX_SG], ul[MAX_SG];
 #pragma unroll
-    for (int b = 0; b < 2; ++b)
+    for (int sg = 0; sg < MAX_SG; ++sg)
+      if (sg < SG) { gl[sg] = __ldcg(p + sg * seg_stride); ul[sg] = __ldcg(p + sg * seg_stride + 64); }
+    float gv = 0.f, uv = 0.f;
 #pragma unroll
-      for (int sg = 0; sg < MAX_SG; ++sg)
-        if (sg < SG) { gl[b][sg] = __ldcg(p + sg * seg_stride + 32 * b); ul[b][sg] = __ldcg(p + sg * seg_stride + 64 + 32 * b); }
-#pragma unroll
-    for (int b = 0; b < 2; ++b) {
-      float gv = 0.f, uv = 0.f;
-#pragma unroll
-      for (int sg = 0; sg < MAX_SG; ++sg)
-        if (sg < SG) { gv += gl[b][sg]; uv += ul[b][sg]; }
-      h_emit(gv, uv, s, b, img);
-    }
+    for (int sg = 0; sg < MAX_SG; ++sg)
+      if (sg < SG) { gv += gl[sg]; uv += ul[sg]; }
+    h_emit(gv, uv, s, b, img);
   }
-  h_padding(img, ntok, W, lane, 32);
+  h_padding(img, ntok, W, lane + 32 * hw, 32 * NHELP);
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -528,6 +560,7 @@ struct Smem {                   // static shared state (the stage ring, h buffer
   int next;
   int abort;
   int ok[NGRP][2], last[NGRP], unit[NGRP];
+  int hok[NHELP];
   int gok;
 };
 // dynamic shared memory: the stage ring, then h images of whole and imported slices, export staging, and the
@@ -616,10 +649,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
     if (epi) split_x_global(a, g, xwarp, nxwarps, xfirst, cnt);
     // hardware barriers: warp 0 arrives once the union is built, then the first epilogue warp builds the slots
     named_bar(NB_TAB, 32 + THREADS - EPI_WARP0 * 32);
-    if (warp == EPI_WARP0) {
-      if (lane == 0) build_slots(tb, S.idx, S.wt, g.T, g.k);
-      __syncwarp();
-    }
+    if (warp == EPI_WARP0) build_slots_warp(tb, S.idx, S.wt, g.T, g.k);
     named_bar(NB_TAB2, THREADS - EPI_WARP0 * 32);
   } else {
     if (a.wr) {
@@ -796,13 +826,15 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
       while (!mbar_test_wait(&S.drain[j], 0) && globaltimer_ns() - t0 < 100000000LL) __nanosleep(64);
     }
     __syncwarp();
-  } else if (warp == HELPER) {
-    // ---------------- helper: export partials staged by the epilogue groups -> global memory, counted per split
-    // slice (the store, fence and count wait on global memory, so they are kept off the epilogue groups); then the
-    // h of each slice this CTA imports, from the counted partials, into the import buffers
+  } else if (warp >= HELPER) {
+    // ---------------- helpers: export partials staged by the epilogue groups -> global memory, counted per split
+    // slice (the store, fence and count wait on global memory, so they are kept off the epilogue groups; helper 0
+    // alone); then the h of each slice this CTA imports, from the counted partials, into the import buffers (both
+    // helpers, meeting on a named barrier before and after each slice)
+    const int hw = warp - HELPER;
     float* gpart = reinterpret_cast<float*>(a.ws + a.L.gpart);
     bool ok = true;
-    for (int i = 0; i < (nunits ? mine.ne : 0) && ok; ++i) {
+    for (int i = 0; i < (nunits && hw == 0 ? mine.ne : 0) && ok; ++i) {
       const int k = i % NXB;
       int w = 1;
       if (lane == 0) w = bwait(&S.xstaged[k], (uint32_t)((i / NXB) & 1), s_abort, lim) ? 1 : 0;
@@ -820,22 +852,27 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
         red_release_add(cnt + C_SPLIT + un.li, 1u);
       }
     }
-    for (int ib = 0; ib < (nunits ? mine.nis : 0) && ok; ++ib) {
+    for (int ib = 0; ib < (nunits ? mine.nis : 0); ++ib) {
       const int kb = ib % NIB;
       const int li = mine.a0 / g.NQ + ib, z = g.Zw + li, u = z / g.NS;
-      int w = 1;
+      int w = ok ? 1 : 0;
       if (lane == 0) {
         // the buffer's previous slice must be done with it, and every segment of this one stored
-        if (ib >= NIB) w = bwait(&S.ifree[kb], (uint32_t)(((ib / NIB) - 1) & 1), s_abort, lim) ? 1 : 0;
+        if (w && ib >= NIB) w = bwait(&S.ifree[kb], (uint32_t)(((ib / NIB) - 1) & 1), s_abort, lim) ? 1 : 0;
         if (w) w = wait_ge(cnt + C_SPLIT + li, (uint32_t)g.SG, s_abort, lim) ? 1 : 0;
+        S.hok[hw] = w;
       }
-      if (!__shfl_sync(0xFFFFFFFFu, w, 0)) { ok = false; break; }
-      __syncwarp();  // lane 0's acquire -> the other lanes' loads of the partials
+      named_bar(NB_HELP, 32 * NHELP);
+      bool all = true;
+#pragma unroll
+      for (int h = 0; h < NHELP; ++h) all = all && S.hok[h] != 0;
+      if (!all) { ok = false; break; }  // both helpers leave together
+      // lane 0's acquire (and the barrier) -> the lanes' loads of the partials
       finalize_import(gpart + (int64_t)li * g.SG * a.ts * 128, (int64_t)a.ts * 128, g.SG, tb.ntok[u], tb.tok[u], g.W,
-                      ibuf + kb * HIMG);
+                      ibuf + kb * HIMG, hw);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> the MMA's reads
-      __syncwarp();
-      if (lane == 0) {
+      named_bar(NB_HELP, 32 * NHELP);
+      if (hw == 0 && lane == 0) {
         mbar_arrive(&S.iready[kb]);
         const int lo = mine.a0 > li * g.NQ ? mine.a0 : li * g.NQ;
         const int hi = mine.a0 + mine.nimp < (li + 1) * g.NQ ? mine.a0 + mine.nimp : (li + 1) * g.NQ;
@@ -879,7 +916,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
       const uint32_t rbase = tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)(g.RC * (j * g.UREG + c % g.UREG));
       // what accumulator h of the unit goes to (its token or slot values acc[]); false if a wait gave up
       auto put = [&](int h, const float (&acc)[TT]) -> bool {
-        if (un.type == U_EXPORT) {  // staged by token for the helper warp, which stores and counts it
+        if (un.type == U_EXPORT) {  // staged by token for helper 0, which stores and counts it
           const int xo = ui - export_pos(g, 0), k = xo % NXB;
           if (xo >= NXB && !shared_ok(et != 0 || bwait(&S.xfree[k], (uint32_t)(((xo / NXB) - 1) & 1), s_abort, lim)))
             return false;
