@@ -71,7 +71,7 @@ template <int FMT> struct Cfg {
   static constexpr int NS = FMT == MOE_FMT_Q2K ? 13 : 8;                   // ring stages
   static constexpr int NCH = 4096 / F::CK / CW;                            // max chunks per warp per tile
   static constexpr int NPS = F::CPS / CW;                                  // chunks per warp per stage
-  static constexpr int SXF = FMT == MOE_FMT_Q2K ? CW * NCH * F::STEPS * kMaxT : 0;   // group sums of x (floats)
+  static constexpr int SXF = 0;
   static constexpr int RED = kNR * CW * 32 * 4;                            // reduction slots (floats)
   static constexpr size_t SMEM = (size_t)NS * SB + (size_t)(RED + SXF) * 4;
 };
@@ -133,6 +133,8 @@ __device__ __forceinline__ void chunk_mma(const uint8_t* cp, int lane, const uin
       acc[3] = fmaf(c[3], sr8, acc[3]);
     }
   } else {  // Q2_K: one chunk = one 256-weight super-block per row, 16 groups of 16 = 16 mma steps
+    // w = d sc q - dmin m per group: the MMA sums (sc q) . x and m . x over the super-block (sc q <= 45 and m <= 15
+    // are exact in fp16, every product exact in fp32), then d and dmin scale the two sums once per chunk
     const uint4 cw0 = *reinterpret_cast<const uint4*>(cp + lane * 32);
     const uint4 cw1 = *reinterpret_cast<const uint4*>(cp + lane * 32 + 16);
     const uint32_t words[8] = {cw0.x, cw0.y, cw0.z, cw0.w, cw1.x, cw1.y, cw1.z, cw1.w};
@@ -146,24 +148,36 @@ __device__ __forceinline__ void chunk_mma(const uint8_t* cp, int lane, const uin
     // 2-bit code at bit 2b of a half's low byte -> fp16 1024 + 4^b q -> exact fma -> q
     const uint32_t mul[4] = {0x3C003C00u, 0x34003400u, 0x2C002C00u, 0x24002400u};
     const uint32_t add[4] = {0xE400E400u, 0xDC00DC00u, 0xD400D400u, 0xCC00CC00u};
-    const int q = lane & 3;
+    const uint32_t k1024 = 0x64006400u, sixteenth = 0x2C002C00u, m64 = 0xD400D400u, one = 0x3C003C00u;
+    const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+    float cq[4] = {0.f, 0.f, 0.f, 0.f}, cm[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int s = 0; s < 16; ++s) {
       const uint32_t W = (s & 1) ? (words[s >> 1] >> 8) : words[s >> 1];
+      // the group's scale byte of rows r and r + 8 in both halves of a word: sc = low nibble, m = high nibble
+      const uint32_t sel = (uint32_t)(s & 3) | 0x4040u | ((uint32_t)(s & 3) << 8);
+      uint32_t br, br8;
+      asm("prmt.b32 %0, %1, 0, %2;" : "=r"(br) : "r"(s_r[s >> 2]), "r"(sel));
+      asm("prmt.b32 %0, %1, 0, %2;" : "=r"(br8) : "r"(s_r8[s >> 2]), "r"(sel));
+      const uint32_t sc_r = hfma2(lop3_and_xor(br, 0x000F000Fu, k1024), one, 0xE400E400u);      // sc, exact
+      const uint32_t sc_r8 = hfma2(lop3_and_xor(br8, 0x000F000Fu, k1024), one, 0xE400E400u);
+      const uint32_t m_r = hfma2(lop3_and_xor(br, 0x00F000F0u, k1024), sixteenth, m64);         // m, exact
+      const uint32_t m_r8 = hfma2(lop3_and_xor(br8, 0x00F000F0u, k1024), sixteenth, m64);
       uint32_t a[4];
 #pragma unroll
       for (int b = 0; b < 4; ++b) a[b] = hfma2(lop3_and_xor(W, 0x00030003u << (2 * b), 0x64006400u), mul[b], add[b]);
-      float c[4];
-      mma_f16(c, a[0], a[1], a[2], a[3], bx[s][0], bx[s][1], zero);
-      const uint32_t br = (s_r[s >> 2] >> (8 * (s & 3))) & 255u, br8 = (s_r8[s >> 2] >> (8 * (s & 3))) & 255u;
-      const float A_r = d_r * (float)(br & 15u), B_r = dm_r * (float)(br >> 4);
-      const float A_r8 = d_r8 * (float)(br8 & 15u), B_r8 = dm_r8 * (float)(br8 >> 4);
-      const float sx0 = sx[s * kMaxT + 2 * q], sx1 = sx[s * kMaxT + 2 * q + 1];
-      acc[0] = fmaf(-B_r, sx0, fmaf(c[0], A_r, acc[0]));
-      acc[1] = fmaf(-B_r, sx1, fmaf(c[1], A_r, acc[1]));
-      acc[2] = fmaf(-B_r8, sx0, fmaf(c[2], A_r8, acc[2]));
-      acc[3] = fmaf(-B_r8, sx1, fmaf(c[3], A_r8, acc[3]));
+      // registers 0, 2: row r; 1, 3: row r + 8
+      const uint32_t z = 0u;
+      mma_f16(cq, hfma2(a[0], sc_r, z), hfma2(a[1], sc_r8, z), hfma2(a[2], sc_r, z), hfma2(a[3], sc_r8, z),
+              bx[s][0], bx[s][1], cq);
+      mma_f16(cm, m_r, m_r8, m_r, m_r8, bx[s][0], bx[s][1], cm);
     }
+    (void)zero;
+    (void)sx;
+    acc[0] = fmaf(-dm_r, cm[0], fmaf(cq[0], d_r, acc[0]));
+    acc[1] = fmaf(-dm_r, cm[1], fmaf(cq[1], d_r, acc[1]));
+    acc[2] = fmaf(-dm_r8, cm[2], fmaf(cq[2], d_r8, acc[2]));
+    acc[3] = fmaf(-dm_r8, cm[3], fmaf(cq[3], d_r8, acc[3]));
   }
 }
 
@@ -227,20 +241,6 @@ __device__ __forceinline__ void load_h_fragments(const FfnArgs& a, int u, int nc
       bh[n][j][0] = v[0];
       bh[n][j][1] = v[1];
     }
-  }
-  if constexpr (FMT == MOE_FMT_Q2K) {
-#pragma unroll
-    for (int n = 0; n < C::NCH; ++n)
-#pragma unroll
-      for (int j = 0; j < F::STEPS; ++j) {
-        const __half2 h0 = *reinterpret_cast<const __half2*>(&bh[n][j][0]);
-        const __half2 h1 = *reinterpret_cast<const __half2*>(&bh[n][j][1]);
-        float s = (__low2float(h0) + __high2float(h0)) + (__low2float(h1) + __high2float(h1));
-        s += __shfl_xor_sync(0xffffffffu, s, 1);
-        s += __shfl_xor_sync(0xffffffffu, s, 2);
-        if (q == 0) sxw[(n * F::STEPS + j) * kMaxT + col] = s;
-      }
-    __syncwarp();
   }
 }
 
@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(Cfg<FMT>::THREADS, 1) ffn_kernel(const FfnArgs
     // ================= consumers (warps 0..7): tensor-core mat-vec over their K slices
     uint32_t it = 0, ri = 0;
     const int col = lane >> 2, q = lane & 3;
-    float* sxw = (FMT == MOE_FMT_Q2K) ? sx + warp * (C::NCH * F::STEPS * kMaxT) : nullptr;
+    float* sxw = nullptr;  // no format needs per-group sums of the activations
     auto hand_over = [&](const float (&acc)[4]) {
       const int slot = (int)(ri % kNR);
       if (ri >= (uint32_t)kNR) {
@@ -540,21 +540,6 @@ __global__ void __launch_bounds__(Cfg<FMT>::THREADS, 1) ffn_kernel(const FfnArgs
             const __half2 hv = __floats2half2_rn(bf16_bits_to_f32(v & 0xFFFFu) * sc, bf16_bits_to_f32(v >> 16) * sc);
             bx[n][j][h] = *reinterpret_cast<const uint32_t*>(&hv);
           }
-      if constexpr (FMT == MOE_FMT_Q2K) {
-        // per-group sums of the rescaled x (the min term of Q2_K), one column per lane quad
-#pragma unroll
-        for (int n = 0; n < C::NCH; ++n)
-#pragma unroll
-          for (int j = 0; j < F::STEPS; ++j) {
-            const __half2 h0 = *reinterpret_cast<const __half2*>(&bx[n][j][0]);
-            const __half2 h1 = *reinterpret_cast<const __half2*>(&bx[n][j][1]);
-            float s = (__low2float(h0) + __high2float(h0)) + (__low2float(h1) + __high2float(h1));
-            s += __shfl_xor_sync(0xffffffffu, s, 1);
-            s += __shfl_xor_sync(0xffffffffu, s, 2);
-            if (q == 0) sxw[(n * F::STEPS + j) * kMaxT + col] = s;
-          }
-        __syncwarp();
-      }
 
       for (int64_t gu = g0; gu < g1; ++gu) {
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
