@@ -54,7 +54,8 @@ namespace moe {
 namespace dtc {
 
 constexpr int NPIPE = 3;                 // pipelines per CTA
-constexpr int RING_MAX = 4;              // stage slots per pipeline: 4 when shared memory allows (T <= 4), else 3
+constexpr int RING_MAX = 4;              // stage slots per pipeline at most (as many as shared memory allows, >= 3;
+                                         // five measured no faster: deeper rings lengthen every copy's latency)
 constexpr int NSLOT = NPIPE * RING_MAX;
 constexpr int NC_MAX = 2;                // down chunks per local down unit at most
 constexpr int PARTS = 6;                 // E2M1 parts per activation value
@@ -62,8 +63,10 @@ constexpr int MAX_T = 8, MAX_K = 8, MAX_U = MAX_T * MAX_K;
 constexpr int WMAX = 48;                 // B rows (MMA N) at most: PARTS x 8 tokens
 // a stage slot: [0, 8192) weight codes (gate/up tile 128 rows x 64 B, 64-byte swizzle; down chunk 256 rows x 32 B,
 // 32-byte swizzle), [8192, 8704) weight exponents (a down chunk is one 8704-byte copy); [8704, 9216) activation
-// exponents, [9216, 12288) activation codes (x parts W x 64 B, swizzled like the weights)
-constexpr int SL_SFA = 8192, SL_SFB = 8704, SLOT_BYTES = 12288;  // activation codes at SL_SFB + 512
+// exponents, [9216, 9216 + 64 W) activation codes (x parts W x 64 B, swizzled like the weights)
+constexpr int SL_SFA = 8192, SL_SFB = 8704;  // activation codes at SL_SFB + 512
+// bytes of a stage slot for W activation rows, a multiple of 1024 (10 KB for W = 16, 12 KB for W = 48)
+__host__ __device__ inline int slot_bytes(int W) { return ((SL_SFB + 512 + 64 * W + 1023) / 1024) * 1024; }
 // activation images: [512 B exponent block][W rows of codes, pre-arranged in the MMA's swizzle], so one bulk copy
 // (x, from global memory) or none (h, formed in shared memory) gives a stage its whole activation operand
 constexpr int XIMG = 512 + WMAX * 64;    // per gate/up k-tile (x parts), in the workspace
@@ -91,7 +94,7 @@ enum { U_EXPORT = 0, U_LOCAL = 1, U_DLOCAL = 2, U_DIMPORT = 3 };
 
 // ------------------------------------------------------------------ geometry and schedule of one call
 struct Geo {
-  int H, I, T, k, E, W, RING;
+  int H, I, T, k, E, W, RING, SLOT;  // ..., stage slots per pipeline, bytes per slot
   int RC, UREG;                 // TMEM columns of one unit's accumulator region, regions per pipeline
   int NC, NDL;                  // down chunks per local down unit, local down units per slice
   int NS, NQ, KTG, KSG, SG;     // slices per expert, row pairs of Down, k-tiles of gate/up, k-tiles per segment, segments
@@ -565,8 +568,8 @@ struct Smem {                   // static shared state (the stage ring, h buffer
 };
 // dynamic shared memory: the stage ring, then h images of whole and imported slices, export staging, and the
 // segment partials of whole slices
-inline size_t smem_bytes(int T, int SG, int ring) {
-  return 1024 + (size_t)NPIPE * ring * SLOT_BYTES + (NHB + NIB) * HIMG + (size_t)NXB * T * 128 * 4 +
+inline size_t smem_bytes(int T, int SG, int ring, int slot) {
+  return 1024 + (size_t)NPIPE * ring * slot + (NHB + NIB) * HIMG + (size_t)NXB * T * 128 * 4 +
          (size_t)NHB * SG * T * 128 * 4;
 }
 
@@ -579,7 +582,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
   __shared__ Smem S;
   volatile int* s_abort = &S.abort;
   const Geo& ga = a.g;
-  uint8_t* hbuf = smem + NPIPE * ga.RING * SLOT_BYTES;                 // [NHB][HIMG] whole slices' h
+  uint8_t* hbuf = smem + NPIPE * ga.RING * ga.SLOT;                   // [NHB][HIMG] whole slices' h
   uint8_t* ibuf = hbuf + NHB * HIMG;                                    // [NIB][HIMG] imported slices' h
   float* xstage = reinterpret_cast<float*>(ibuf + NIB * HIMG);          // [NXB][T][128] export partials
   float* spart = xstage + NXB * ga.T * 128;                             // [NHB][SG][T][128] whole slices' partials
@@ -723,7 +726,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
           const int slot = j * g.RING + (n % g.RING);
           const uint32_t ph = (uint32_t)((n / g.RING) & 1);
           if (!bwait(&S.empty[slot], ph ^ 1, s_abort, lim)) { ok = false; break; }
-          uint8_t* st = smem + slot * SLOT_BYTES;
+          uint8_t* st = smem + slot * g.SLOT;
           const uint32_t xbytes = d ? 0u : (uint32_t)(512 + 64 * g.W);
           mbar_arrive_expect_tx(&S.full[slot], (uint32_t)kTcTileBytes + xbytes);
           // weights are read once per call: evict-first keeps them from displacing what the dependent steps read
@@ -782,7 +785,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
           const int slot = j * g.RING + (n % g.RING);
           if (!bwait(&S.full[slot], (uint32_t)((n / g.RING) & 1), s_abort, lim)) { ok = false; break; }
           tc_fence_after();
-          uint8_t* st = smem + slot * SLOT_BYTES;
+          uint8_t* st = smem + slot * g.SLOT;
           const uint32_t sfa = tbase + SF_COL0 + (uint32_t)(slot * 8);
           uint32_t sfbc = sfa + 4;
           // activation image [512 B exponents][codes]: x in the stage, h of the slice in this CTA's buffers
@@ -1154,11 +1157,13 @@ moe_status_t run(const moe_layer_t* L, const void* x, int T, const int32_t* idx,
     static_smem = (int)(fa2.sharedSizeBytes > fa8.sharedSizeBytes ? fa2.sharedSizeBytes : fa8.sharedSizeBytes);
     smem_max = v;
   }
-  g.RING = (int)smem_bytes(T, g.SG, RING_MAX) + static_smem <= smem_max ? RING_MAX : 3;
-  if ((int)smem_bytes(T, g.SG, g.RING) + static_smem > smem_max) return MOE_ERR_SHAPE;
+  g.SLOT = slot_bytes(g.W);
+  g.RING = RING_MAX;  // the deepest ring that fits
+  while (g.RING > 3 && (int)smem_bytes(T, g.SG, g.RING, g.SLOT) + static_smem > smem_max) --g.RING;
+  if ((int)smem_bytes(T, g.SG, g.RING, g.SLOT) + static_smem > smem_max) return MOE_ERR_SHAPE;
   CUtensorMap mgu;
   if (!moe_internal::tmap_tc_weights_packed(&mgu, L->gate_up, MOE_MAT_GATE_UP, L->H, L->I, L->E)) return MOE_ERR_CUDA;
-  const size_t smem = smem_bytes(T, g.SG, g.RING);
+  const size_t smem = smem_bytes(T, g.SG, g.RING, g.SLOT);
   static std::once_flag once;
   static bool attr_ok = false;
   std::call_once(once, [] {
