@@ -324,7 +324,7 @@ __device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, volatile i
   if (mbar_test_wait(bar, parity)) return true;
   const long long t0 = globaltimer_ns();
   while (true) {
-    __nanosleep(32);
+    __nanosleep(32);  // 128 and 512 ns measured slower
     if (mbar_test_wait(bar, parity)) return true;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > lim) { *abort_flag = 1; return false; }

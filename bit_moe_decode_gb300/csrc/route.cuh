@@ -86,38 +86,37 @@ __device__ __forceinline__ void route_row_logits(const uint16_t* __restrict__ ro
 template <int NE, typename Logit>
 __device__ __forceinline__ void route_topk_warp(Logit logit, int E, int k, int (&sid)[8], float (&sw)[8]) {
   const int lane = threadIdx.x & 31;
-  float v[NE];
+  // every logit as an order-preserving key, computed once: larger key = larger logit; NaN, -inf and absent
+  // experts get key 0 and are never chosen (as with comparisons), -0 gets the key of +0
+  uint32_t key[NE];
 #pragma unroll
   for (int j = 0; j < NE; ++j) {
     const int e = lane + 32 * j;
-    v[j] = e < E ? logit(e) : -__int_as_float(0x7f800000);
+    const float v = e < E ? logit(e) : -__int_as_float(0x7f800000);
+    const uint32_t u = __float_as_uint(v) == 0x80000000u ? 0u : __float_as_uint(v);
+    key[j] = v > -__int_as_float(0x7f800000) ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
   }
   // the rounds are unrolled to the largest k so that sel, sid and sw stay in registers (a dynamically indexed
-  // array would live in local memory, whose round trips are slow while the weights stream)
+  // array would live in local memory, whose round trips are slow while the weights stream). A round is two warp
+  // reductions: the largest key, then the lowest expert index among the lanes holding it (ties to the lower index).
   float sel[8];
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
     sel[r] = 0.f;
     sid[r] = 0;
     if (r >= k) continue;
-    float best = -__int_as_float(0x7f800000);
-    int bi = 0x7fffffff;
+    uint32_t bk = 0u;  // this lane's best key and its expert (the lowest j among equal keys)
+    int be = 0x7fffffff;
 #pragma unroll
-    for (int j = 0; j < NE; ++j) {
-      const int e = lane + 32 * j;
-      if (e < E && (v[j] > best || (v[j] == best && e < bi))) { best = v[j]; bi = e; }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ob = __shfl_xor_sync(0xffffffffu, best, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
-    }
-    sel[r] = best;
+    for (int j = 0; j < NE; ++j)
+      if (key[j] > bk) { bk = key[j]; be = lane + 32 * j; }
+    const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+    const int bi = mk ? (int)__reduce_min_sync(0xffffffffu, bk == mk ? (uint32_t)be : 0xffffffffu) : 0x7fffffff;
+    sel[r] = mk ? __uint_as_float((mk & 0x80000000u) ? (mk & 0x7fffffffu) : ~mk) : -__int_as_float(0x7f800000);
     sid[r] = bi;
 #pragma unroll
     for (int j = 0; j < NE; ++j)  // remove the winner
-      if (lane + 32 * j == bi) v[j] = -__int_as_float(0x7f800000);
+      if (lane + 32 * j == bi) key[j] = 0u;
   }
   float den = 0.f;
 #pragma unroll
