@@ -24,16 +24,18 @@
 // runs all their segments, forms h in its own shared memory and runs their down chunks, with no global hand-off.
 // The remaining R < CTAs slices are SPLIT: their segments (exports) are spread over the CTAs and run early; their
 // partials go to global memory and are counted. Their down chunks (imports) are dealt in contiguous runs, so a CTA
-// imports from one or two split slices, forms each one's h itself from the counted partials, and runs the chunks
-// last; the runs are sized so that every CTA streams the same number of weight bytes to within one tile. Each
+// imports from one or two split slices and runs the chunks last; the runs are sized so that every CTA streams the
+// same number of weight bytes to within one tile. Up to two tokens, every importer forms the h of its slices from
+// the counted partials; with more, the slice's exporters each form a share of its h blocks once, into an image in
+// global memory that the importers copy. Each
 // CTA's order: the exports, the whole slices (W0 W1 D0 W2 D1 ..: forming h of a slice overlaps the next slice's
 // stream), the imports. A grid barrier then lets every CTA sum the down partials of its share of the outputs (one
 // warp per (token, 32 rows, rank): a lane per row, the slices in order).
 //
 // Inside a CTA, three independent pipelines take the CTA's units as they free up: a copy-issuing warp, an
 // MMA-issuing warp, a shared-memory ring of three or four stage slots, TMEM accumulators and a group of four
-// epilogue warps. Two helper warps do the work that waits on global memory (storing and counting export partials;
-// forming the h of imported slices, which they share) so that no epilogue group stalls on it. One issuing thread
+// epilogue warps. Two helper warps do the work that waits on global memory (storing and counting export partials,
+// forming the split slices' h) so that no epilogue group stalls on it. One issuing thread
 // sustains only about one wait-and-issue round per 330 ns (TMA) or one
 // stage of MMAs plus commit per ~600 cycles (tcgen05), while one SM must consume an 8.5 KB weight tile every
 // ~180 ns to keep pace with HBM. Every wait is bounded; on a timeout the kernel records MOE_ERR_DEVICE_TIMEOUT, lets
@@ -203,20 +205,22 @@ __device__ inline Unit unit_at(const Geo& g, const Mine& mi, int c, int i) {
 
 // ------------------------------------------------------------------ workspace (byte offsets from the base)
 // [0, 256)   WsHeader (status word, done, grid barrier)
-// [256, ..)  counters (uint32): x parts done, router logits done, then per split slice: its segments stored
-// then gpart [RMAX * MAX_SG][TS][128] fp32 (split slices' segment partials, by token), ximg [KTG][XIMG] (x parts),
-//      dpart [cols][H / 32][NS][32] fp32 (down partials: a column per (expert, token) pair of the call),
-//      lg [tokens][2][E] router logit halves.
+// [256, ..)  counters (uint32): x parts done, router logits done, then per split slice: its segments stored, then
+//            per split slice: its segments' exporters done writing their blocks of its h image
+// then gpart [RMAX * MAX_SG][TS][128] fp32 (split slices' segment partials, by token), himg [RMAX][HIMG] (split
+//      slices' h images), ximg [KTG][XIMG] (x parts), dpart [cols][H / 32][NS][32] fp32 (down partials: a column
+//      per (expert, token) pair of the call), lg [tokens][2][E] router logit halves.
 constexpr int64_t kCnt = 256;
-constexpr int C_XP = 0, C_ROUTE = 1, C_SPLIT = 2, C_END = C_SPLIT + RMAX;
+constexpr int C_XP = 0, C_ROUTE = 1, C_SPLIT = 2, C_HREADY = C_SPLIT + RMAX, C_END = C_HREADY + RMAX;
 struct Ws {
-  int64_t gpart, ximg, dpart, lg, total;
+  int64_t gpart, himg, ximg, dpart, lg, total;
 };
 inline int64_t al1k(int64_t v) { return (v + 1023) & ~(int64_t)1023; }
 inline Ws ws_layout(int64_t H, int64_t I, int64_t cols, int64_t TS) {
   Ws w;
   int64_t o = al1k(kCnt + (int64_t)C_END * 4);
   w.gpart = o; o = al1k(o + (int64_t)RMAX * MAX_SG * TS * 128 * 4);
+  w.himg = o;  o = al1k(o + (int64_t)RMAX * HIMG);
   w.ximg = o;  o = al1k(o + (H / 128) * XIMG);
   w.dpart = o; o = al1k(o + cols * H * (I / 64) * 4);
   w.lg = o;    o = al1k(o + (int64_t)kRouteTPC * 2 * kRouteMaxE * 4);
@@ -544,6 +548,28 @@ __device__ void finalize_import(const float* part, int64_t seg_stride, int SG, i
   h_padding(img, ntok, W, lane + 32 * hw, 32 * NHELP);
 }
 
+// The blocks of a split slice's h that the exporter of segment x forms (q = 2 slot + half, q = x mod SG; helper hw
+// of NHELP takes every NHELP-th of them), from all the segments' partials in global memory, written straight into
+// the slice's h image in global memory; exporter 0 also writes the padding rows.
+__device__ void form_blocks(const float* part, int64_t seg_stride, int SG, int x, int ntok, const int8_t* tok, int W,
+                            uint8_t* img, int hw) {
+  const int lane = threadIdx.x & 31;
+  for (int q = x + SG * hw; q < 2 * ntok; q += SG * NHELP) {
+    const int s = q >> 1, b = q & 1;
+    const float* p = part + tok[s] * 128 + 32 * b + lane;
+    float gl[MAX_SG], ul[MAX_SG];
+#pragma unroll
+    for (int sg = 0; sg < MAX_SG; ++sg)
+      if (sg < SG) { gl[sg] = __ldcg(p + sg * seg_stride); ul[sg] = __ldcg(p + sg * seg_stride + 64); }
+    float gv = 0.f, uv = 0.f;
+#pragma unroll
+    for (int sg = 0; sg < MAX_SG; ++sg)
+      if (sg < SG) { gv += gl[sg]; uv += ul[sg]; }
+    h_emit(gv, uv, s, b, img);
+  }
+  if (x == 0) h_padding(img, ntok, W, lane + 32 * hw, 32 * NHELP);
+}
+
 // ------------------------------------------------------------------ the kernel
 struct Smem {                   // static shared state (the stage ring, h buffers and partials are dynamic)
   uint64_t full[NSLOT], empty[NSLOT];
@@ -830,12 +856,16 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
     }
     __syncwarp();
   } else if (warp >= HELPER) {
-    // ---------------- helpers: export partials staged by the epilogue groups -> global memory, counted per split
-    // slice (the store, fence and count wait on global memory, so they are kept off the epilogue groups; helper 0
-    // alone); then the h of each slice this CTA imports, from the counted partials, into the import buffers (both
-    // helpers, meeting on a named barrier before and after each slice)
+    // ---------------- helpers. Helper 0 stores the export partials staged by the epilogue groups and counts them
+    // per split slice (the store, fence and count wait on global memory, so they are kept off the epilogue groups).
+    // Then the h of the slices this CTA imports. Up to two tokens (at most 4 blocks a slice) both helpers form it
+    // from the counted partials into the import buffers. With more tokens, for each of this CTA's exports, once the
+    // slice's segments are all counted, both helpers form that exporter's share of the slice's blocks straight into
+    // the slice's h image in global memory and count that; helper 0 then copies the finished image of each slice
+    // this CTA imports (one bulk copy, counted on the buffer's ready barrier).
     const int hw = warp - HELPER;
     float* gpart = reinterpret_cast<float*>(a.ws + a.L.gpart);
+    uint8_t* himg = a.ws + a.L.himg;
     bool ok = true;
     for (int i = 0; i < (nunits && hw == 0 ? mine.ne : 0) && ok; ++i) {
       const int k = i % NXB;
@@ -855,31 +885,74 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
         red_release_add(cnt + C_SPLIT + un.li, 1u);
       }
     }
-    for (int ib = 0; ib < (nunits ? mine.nis : 0); ++ib) {
-      const int kb = ib % NIB;
-      const int li = mine.a0 / g.NQ + ib, z = g.Zw + li, u = z / g.NS;
-      int w = ok ? 1 : 0;
-      if (lane == 0) {
-        // the buffer's previous slice must be done with it, and every segment of this one stored
-        if (w && ib >= NIB) w = bwait(&S.ifree[kb], (uint32_t)(((ib / NIB) - 1) & 1), s_abort, lim) ? 1 : 0;
-        if (w) w = wait_ge(cnt + C_SPLIT + li, (uint32_t)g.SG, s_abort, lim) ? 1 : 0;
-        S.hok[hw] = w;
-      }
-      named_bar(NB_HELP, 32 * NHELP);
-      bool all = true;
+    if constexpr (TT <= 2) {
+      // up to two tokens: an imported slice has at most 4 h blocks, so every importer forms them itself
+      for (int ib = 0; ib < (nunits ? mine.nis : 0); ++ib) {
+        const int kb = ib % NIB;
+        const int li = mine.a0 / g.NQ + ib, z = g.Zw + li, u = z / g.NS;
+        int w = ok ? 1 : 0;
+        if (lane == 0) {
+          // the buffer's previous slice must be done with it, and every segment of this one stored
+          if (w && ib >= NIB) w = bwait(&S.ifree[kb], (uint32_t)(((ib / NIB) - 1) & 1), s_abort, lim) ? 1 : 0;
+          if (w) w = wait_ge(cnt + C_SPLIT + li, (uint32_t)g.SG, s_abort, lim) ? 1 : 0;
+          S.hok[hw] = w;
+        }
+        named_bar(NB_HELP, 32 * NHELP);
+        bool all = true;
 #pragma unroll
-      for (int h = 0; h < NHELP; ++h) all = all && S.hok[h] != 0;
-      if (!all) { ok = false; break; }  // both helpers leave together
-      // lane 0's acquire (and the barrier) -> the lanes' loads of the partials
-      finalize_import(gpart + (int64_t)li * g.SG * a.ts * 128, (int64_t)a.ts * 128, g.SG, tb.ntok[u], tb.tok[u], g.W,
-                      ibuf + kb * HIMG, hw);
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> the MMA's reads
-      named_bar(NB_HELP, 32 * NHELP);
-      if (hw == 0 && lane == 0) {
-        mbar_arrive(&S.iready[kb]);
-        const int lo = mine.a0 > li * g.NQ ? mine.a0 : li * g.NQ;
-        const int hi = mine.a0 + mine.nimp < (li + 1) * g.NQ ? mine.a0 + mine.nimp : (li + 1) * g.NQ;
-        if (ib + NIB < mine.nis && g.NQ - (hi - lo) > 0) mbar_arrive_n(&S.ifree[kb], (uint32_t)(g.NQ - (hi - lo)));
+        for (int h = 0; h < NHELP; ++h) all = all && S.hok[h] != 0;
+        if (!all) { ok = false; break; }  // both helpers leave together
+        // lane 0's acquire (and the barrier) -> the lanes' loads of the partials
+        finalize_import(gpart + (int64_t)li * g.SG * a.ts * 128, (int64_t)a.ts * 128, g.SG, tb.ntok[u], tb.tok[u], g.W,
+                        ibuf + kb * HIMG, hw);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> the MMA's reads
+        named_bar(NB_HELP, 32 * NHELP);
+        if (hw == 0 && lane == 0) {
+          mbar_arrive(&S.iready[kb]);
+          const int lo = mine.a0 > li * g.NQ ? mine.a0 : li * g.NQ;
+          const int hi = mine.a0 + mine.nimp < (li + 1) * g.NQ ? mine.a0 + mine.nimp : (li + 1) * g.NQ;
+          if (ib + NIB < mine.nis && g.NQ - (hi - lo) > 0) mbar_arrive_n(&S.ifree[kb], (uint32_t)(g.NQ - (hi - lo)));
+        }
+      }
+    } else {
+      // more tokens: each exporter forms its share of the slice's blocks once, the importers copy the image
+      for (int i = 0; i < (nunits ? mine.ne : 0); ++i) {
+        const Unit un = unit_at(g, mine, (int)blockIdx.x, export_pos(g, i));
+        const int z = g.Zw + un.li, u = z / g.NS;
+        int w = ok ? 1 : 0;
+        if (lane == 0) {
+          if (w) w = wait_ge(cnt + C_SPLIT + un.li, (uint32_t)g.SG, s_abort, lim) ? 1 : 0;
+          S.hok[hw] = w;
+        }
+        named_bar(NB_HELP, 32 * NHELP);  // also orders helper 0's exports before helper 1 goes on
+        bool all = true;
+#pragma unroll
+        for (int h = 0; h < NHELP; ++h) all = all && S.hok[h] != 0;
+        if (!all) { ok = false; break; }  // both helpers leave together
+        form_blocks(gpart + (int64_t)un.li * g.SG * a.ts * 128, (int64_t)a.ts * 128, g.SG, un.x, tb.ntok[u], tb.tok[u],
+                    g.W, himg + (int64_t)un.li * HIMG, hw);
+        named_bar(NB_HELP, 32 * NHELP);  // every store of the block before the count's release
+        if (hw == 0 && lane == 0) red_release_add(cnt + C_HREADY + un.li, 1u);
+      }
+      for (int ib = 0; ib < (nunits && hw == 0 && ok ? mine.nis : 0); ++ib) {
+        const int kb = ib % NIB;
+        const int li = mine.a0 / g.NQ + ib;
+        int w = 1;
+        if (lane == 0) {
+          // the buffer's previous slice must be done with it, and every exporter of this one done with its h blocks
+          if (ib >= NIB) w = bwait(&S.ifree[kb], (uint32_t)(((ib / NIB) - 1) & 1), s_abort, lim) ? 1 : 0;
+          if (w) w = wait_ge(cnt + C_HREADY + li, (uint32_t)g.SG, s_abort, lim) ? 1 : 0;
+          if (w) {
+            asm volatile("fence.proxy.async.global;" ::: "memory");  // the acquire -> the bulk copy's reads
+            const uint32_t nbytes = (uint32_t)(512 + 32 * g.W);     // exponent block + W rows of 32 B
+            mbar_arrive_expect_tx(&S.iready[kb], nbytes);
+            bulk_g2s_plain(ibuf + kb * HIMG, himg + (int64_t)li * HIMG, nbytes, &S.iready[kb]);
+            const int lo = mine.a0 > li * g.NQ ? mine.a0 : li * g.NQ;
+            const int hi = mine.a0 + mine.nimp < (li + 1) * g.NQ ? mine.a0 + mine.nimp : (li + 1) * g.NQ;
+            if (ib + NIB < mine.nis && g.NQ - (hi - lo) > 0) mbar_arrive_n(&S.ifree[kb], (uint32_t)(g.NQ - (hi - lo)));
+          }
+        }
+        if (!__shfl_sync(0xFFFFFFFFu, w, 0)) { ok = false; break; }
       }
     }
     if (!ok && lane == 0) record_error(&hdr->status, MOE_ERR_DEVICE_TIMEOUT);
@@ -1081,7 +1154,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const __grid_constan
     const uint32_t old = atomicAdd(&hdr->done, 1u);
     if (old == gridDim.x - 1) {
       __threadfence();
-      for (int r = 0; r < g.R; ++r) cnt[C_SPLIT + r] = 0;
+      for (int r = 0; r < g.R; ++r) { cnt[C_SPLIT + r] = 0; cnt[C_HREADY + r] = 0; }
       cnt[C_XP] = 0;
       cnt[C_ROUTE] = 0;
       hdr->gbar = 0;
