@@ -5,7 +5,8 @@ The CUDA library never calls it and shares no code with it. The arithmetic lives
 fp64 accumulation, built with -O2 -ffp-contract=off); this file only builds it and marshals numpy arrays.
 
 Formats: fmt 1 = MXFP4 (17-byte blocks of 32), 2 = INT4 group-32 (18-byte blocks), 3 = Q2_K (84-byte blocks
-of 256). A matrix [rows, K] is rows*K/bs consecutive canonical blocks (blocks run along K).
+of 256), 4 = Q8_0 (34-byte blocks of 32, the shared expert's format as this build defines it). A matrix
+[rows, K] is rows*K/bs consecutive canonical blocks (blocks run along K).
 
 Parity pins: every function here is pinned by tests/test_oracle_*.py against values the pages print
 (E2M1 table, E8M0 rule, block sizes), closed forms, brute force on tiny inputs or library routines.
@@ -25,8 +26,8 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-MXFP4, INT4G32, Q2K = 1, 2, 3
-BLOCK = {MXFP4: (32, 17), INT4G32: (32, 18), Q2K: (256, 84)}
+MXFP4, INT4G32, Q2K, Q8_0 = 1, 2, 3, 4
+BLOCK = {MXFP4: (32, 17), INT4G32: (32, 18), Q2K: (256, 84), Q8_0: (32, 34)}
 
 
 def build(force: bool = False) -> str:
@@ -58,9 +59,11 @@ def bind(path: str) -> C.CDLL:
         "orc_decode_mxfp4": (None, [P, i64, P]),
         "orc_decode_int4": (None, [P, i64, P]),
         "orc_decode_q2k": (None, [P, i64, P]),
+        "orc_decode_q8_0": (None, [P, i64, P]),
         "orc_encode_mxfp4": (None, [P, i64, P]),
         "orc_encode_int4": (None, [P, i64, P]),
         "orc_encode_q2k": (None, [P, i64, P]),
+        "orc_encode_q8_0": (None, [P, i64, P]),
         "orc_quant_mxfp8": (None, [P, i64, P, P]),
         "orc_mxfp4_half_lut": (None, [P]),
         "orc_router_logits": (None, [P, P, i32, i32, i32, P, P]),
@@ -147,7 +150,8 @@ def decode(fmt: int, blocks: np.ndarray) -> np.ndarray:
     b = _c(blocks, np.uint8).reshape(-1)
     n = b.size // nb
     out = np.empty(n * bs, dtype=np.float32)
-    fn = {MXFP4: lib().orc_decode_mxfp4, INT4G32: lib().orc_decode_int4, Q2K: lib().orc_decode_q2k}[fmt]
+    fn = {MXFP4: lib().orc_decode_mxfp4, INT4G32: lib().orc_decode_int4, Q2K: lib().orc_decode_q2k,
+          Q8_0: lib().orc_decode_q8_0}[fmt]
     fn(_p(b), n, _p(out))
     return out
 
@@ -160,7 +164,8 @@ def encode(fmt: int, w: np.ndarray) -> np.ndarray:
     assert shape[-1] % bs == 0
     n = a.size // bs
     out = np.empty(n * nb, dtype=np.uint8)
-    fn = {MXFP4: lib().orc_encode_mxfp4, INT4G32: lib().orc_encode_int4, Q2K: lib().orc_encode_q2k}[fmt]
+    fn = {MXFP4: lib().orc_encode_mxfp4, INT4G32: lib().orc_encode_int4, Q2K: lib().orc_encode_q2k,
+          Q8_0: lib().orc_encode_q8_0}[fmt]
     fn(_p(a), n, _p(out))
     return out.reshape(*shape[:-1], shape[-1] // bs * nb)
 

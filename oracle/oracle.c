@@ -480,15 +480,57 @@ void orc_route_hash(const int32_t* tok, const int32_t* tid2eid, int T, int k, in
 }
 
 /* ------------------------------------------------------------------------------------------------
+ * Q8_0: the shared expert's 8-bit format ("Mixed-precision compression of DeepSeek-V4-Flash", "The recipe"
+ * names Q8 for it and gives no layout; this build's definition): 34 bytes per 32 weights, bytes 0..1 a binary16
+ * scale d (little-endian), bytes 2..33 signed 8-bit codes q_j; w_j = d * q_j.
+ * ------------------------------------------------------------------------------------------------ */
+
+static double q8_scale(const uint8_t* blk) { return orc_f16_to_f64(rd16(blk)); }
+static int q8_code(const uint8_t* blk, int j) { return (int)(int8_t)blk[2 + j]; }
+static double q8_weight(const uint8_t* blk, int j) { return q8_code(blk, j) * q8_scale(blk); }
+
+void orc_decode_q8_0(const uint8_t* blocks, int64_t nblk, float* out) {
+  for (int64_t b = 0; b < nblk; ++b)
+    for (int j = 0; j < 32; ++j) out[b * 32 + j] = (float)q8_weight(blocks + b * 34, j);
+}
+
+/* Q8_0 encoder: amax = max |w| (fp32); d = fp16 RNE of amax / 127 (fp32 division); q_j = round_half_even(w_j / d)
+ * (fp32 division by the fp16 value of d) clamped to [-127, 127]; q = 0 when d = 0 and for NaN quotients. */
+void orc_encode_q8_0(const float* w, int64_t nblk, uint8_t* out) {
+#pragma omp parallel for schedule(static)
+  for (int64_t b = 0; b < nblk; ++b) {
+    const float* x = w + b * 32;
+    uint8_t* blk = out + b * 34;
+    float amax = 0.0f;
+    for (int j = 0; j < 32; ++j) { float a = fabsf(x[j]); if (a > amax) amax = a; }
+    const uint16_t dbits = orc_f32_to_f16_rne(amax / 127.0f);
+    const float d = (float)orc_f16_to_f64(dbits);
+    blk[0] = (uint8_t)(dbits & 255);
+    blk[1] = (uint8_t)(dbits >> 8);
+    for (int j = 0; j < 32; ++j) {
+      float qq = 0.0f;
+      if (d != 0.0f) {
+        qq = rne_int(x[j] / d);
+        if (qq != qq) qq = 0.0f;
+        if (qq < -127.0f) qq = -127.0f;
+        if (qq > 127.0f) qq = 127.0f;
+      }
+      blk[2 + j] = (uint8_t)(int8_t)(int)qq;
+    }
+  }
+}
+
+/* ------------------------------------------------------------------------------------------------
  * Expert FFN, SwiGLU form [P5 "Q4_K routed experts" bullets: a fused gate+up mat-vec, then the down
  * projection accumulated into the output]:
  *   g = Gate x, u = Up x, h = SiLU(g) * u = g / (1 + exp(-g)) * u, d = Down h, y = sum_r w_r d_r.
- * fmt: 1 = MXFP4 (17-byte blocks of 32), 2 = INT4 g32 (18-byte blocks), 3 = Q2_K (84-byte blocks of 256).
+ * fmt: 1 = MXFP4 (17-byte blocks of 32), 2 = INT4 g32 (18-byte blocks), 3 = Q2_K (84-byte blocks of 256),
+ * 4 = Q8_0 (34-byte blocks of 32).
  * A matrix [rows, K] is rows * K/bs consecutive canonical blocks.
  * ------------------------------------------------------------------------------------------------ */
 
 static int fmt_bs(int fmt) { return fmt == 3 ? 256 : 32; }
-static int fmt_bytes(int fmt) { return fmt == 1 ? 17 : fmt == 2 ? 18 : 84; }
+static int fmt_bytes(int fmt) { return fmt == 1 ? 17 : fmt == 2 ? 18 : fmt == 4 ? 34 : 84; }
 
 /* decoded weight (row, col) of a [rows, K] matrix, exact, in double */
 static double weight_at(int fmt, const uint8_t* mat, int K, int64_t row, int col) {
@@ -497,6 +539,7 @@ static double weight_at(int fmt, const uint8_t* mat, int K, int64_t row, int col
   int j = col % bs;
   if (fmt == 1) return mxfp4_weight(blk, j);
   if (fmt == 2) return int4_weight(blk, j);
+  if (fmt == 4) return q8_weight(blk, j);
   return (double)q2k_weight_f32(blk, j);
 }
 
@@ -514,6 +557,8 @@ static void decode_matrix(int fmt, const uint8_t* mat, int64_t rows, int K, doub
     } else if (fmt == 2) {
       double s = int4_scale(blk);
       for (int j = 0; j < 32; ++j) out[b * 32 + j] = int4_code(blk, j) * s;
+    } else if (fmt == 4) {
+      for (int j = 0; j < 32; ++j) out[b * 32 + j] = q8_weight(blk, j);
     }
     else { orc_decode_q2k(blk, 1, tmp); for (int j = 0; j < 256; ++j) out[b * 256 + j] = (double)tmp[j]; }
   }

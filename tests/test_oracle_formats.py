@@ -258,6 +258,53 @@ def test_int4_encoder_is_grid_argmin():
     assert float(M.min(1).values.sum()) <= float(M[:, 3].sum())
 
 
+# ---------------------------------------------------------------- Q8_0 (the shared expert's format, defined by this build)
+def test_q8_0_layout_and_decode_closed_form():
+    """34 bytes per 32 weights (8.5 bits): fp16 d little-endian, then 32 two's-complement codes; w = d * q."""
+    rng = np.random.default_rng(21)
+    q = rng.integers(-127, 128, size=32)
+    d = np.float16(0.0123)
+    raw = np.zeros(34, np.uint8)
+    raw[0:2] = np.frombuffer(d.tobytes(), np.uint8)
+    raw[2:] = q.astype(np.int8).view(np.uint8)
+    assert oracle.BLOCK[oracle.Q8_0] == (32, 34) and 34 * 8 / 32 == 8.5
+    got = oracle.decode(oracle.Q8_0, raw)
+    assert np.array_equal(got, (q * np.float64(d)).astype(np.float32))
+
+
+def test_q8_0_encoder_against_torch():
+    """d = fp16(amax / 127), q = clamp(round_half_even(w / d), -127, 127), in fp32 (torch.round is half-even)."""
+    rng = np.random.default_rng(22)
+    w = (rng.standard_normal((400, 32)) * 0.02).astype(np.float32)
+    w[0] = 0.0                                # d = 0: all codes 0
+    w[1, 5] = -w[1].__abs__().max() * 2       # the largest magnitude negative: code -127
+    blk = oracle.encode(oracle.Q8_0, w).reshape(400, 34)
+    W = torch.from_numpy(w)
+    d = (W.abs().amax(-1, keepdim=True) / 127).to(torch.float16)
+    df = d.float()
+    qq = torch.where(df == 0, torch.zeros_like(W), torch.clamp(torch.round(W / torch.where(df == 0, 1, df)), -127, 127))
+    assert np.array_equal(blk[:, 0:2].copy().view(np.float16)[:, 0], d[:, 0].numpy())
+    assert np.array_equal(blk[:, 2:].view(np.int8).astype(np.int64), qq.long().numpy())
+    assert np.all(blk[0] == 0) and blk[1, 2 + 5].view(np.int8) == -127
+    dec = oracle.decode(oracle.Q8_0, blk).reshape(400, 32)
+    # every weight within half a step of its code (d / 2), the step being the stored fp16 d
+    assert np.all(np.abs(dec - w) <= df.numpy() / 2 * (1 + 1e-6) + 1e-30)
+
+
+def test_q8_0_encoder_ties_go_to_even_and_clamp():
+    """Exact half steps round to the even code (d a power of two, so w / d is exact); values past 127 d clamp."""
+    w = np.zeros((1, 32), np.float32)
+    w[0, 0] = 127.0 * 0.25                    # amax: d = 0.25 exactly
+    halves = [0.5, 1.5, 2.5, -0.5, -2.5, 126.5]
+    for i, h in enumerate(halves):
+        w[0, 1 + i] = h * 0.25
+    blk = oracle.encode(oracle.Q8_0, w)[0]
+    assert blk[0:2].view(np.float16)[0] == np.float16(0.25)
+    codes = blk[2:].view(np.int8)
+    assert codes[0] == 127
+    assert list(codes[1:7]) == [0, 2, 2, 0, -2, 126]
+
+
 # ---------------------------------------------------------------- Q2_K
 def test_q2k_handbuilt_block():
     (raw, vals), = _handbuilt("q2k_handbuilt.txt").values()

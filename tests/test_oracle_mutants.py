@@ -68,6 +68,12 @@ MUTANTS = {
                           [tf.test_q2k_size_and_encoder_bounds]),
     "q2k_offset_dropped": ("        float t = x[i] + off;", "        float t = x[i];",
                            [tf.test_q2k_size_and_encoder_bounds]),
+    "q8_0_scale_over_128": ("orc_f32_to_f16_rne(amax / 127.0f);", "orc_f32_to_f16_rne(amax / 128.0f);",
+                            [tf.test_q8_0_encoder_against_torch, tf.test_q8_0_encoder_ties_go_to_even_and_clamp]),
+    "q8_0_codes_unsigned": ("return (int)(int8_t)blk[2 + j];", "return (int)blk[2 + j];",
+                            [tf.test_q8_0_layout_and_decode_closed_form]),
+    "q8_0_codes_truncated": ("        qq = rne_int(x[j] / d);", "        qq = truncf(x[j] / d);",
+                             [tf.test_q8_0_encoder_against_torch, tf.test_q8_0_encoder_ties_go_to_even_and_clamp]),
 }
 
 

@@ -115,7 +115,7 @@ def test_ffn_integer_case_is_exact():
     assert np.allclose(out["d"], dv @ h, rtol=1e-13, atol=1e-12)
 
 
-@pytest.mark.parametrize("fmt", [oracle.MXFP4, oracle.INT4G32, oracle.Q2K])
+@pytest.mark.parametrize("fmt", [oracle.MXFP4, oracle.INT4G32, oracle.Q2K, oracle.Q8_0])
 def test_ffn_random_matches_numpy_path(fmt):
     H, I = 512, 256
     g, u, d = (oracle.encode(fmt, expert_matrix_f32(7, 0, 3, which, H, I)) for which in range(3))
@@ -129,7 +129,7 @@ def test_ffn_random_matches_numpy_path(fmt):
     assert np.allclose(out["dabs"], rabs, rtol=1e-12)
 
 
-@pytest.mark.parametrize("fmt", [oracle.MXFP4, oracle.Q2K])
+@pytest.mark.parametrize("fmt", [oracle.MXFP4, oracle.Q2K, oracle.Q8_0])
 def test_moe_combine_batch_and_token_agree_with_numpy(fmt):
     E, H, I, k, T = 8, 512, 256, 2, 5
     G, U, D = _layer(fmt, E, H, I, seed=2)
