@@ -65,6 +65,7 @@ def parse():
                         "auto = tc for MXFP4, decode otherwise")
     p.add_argument("--no-formats", action="store_true", help="measure only the --fmt / --layout path")
     p.add_argument("--no-stack", action="store_true", help="skip the 43-layer stack measurement")
+    p.add_argument("--no-shared", action="store_true", help="skip the routed + Q8_0 shared-expert measurement")
     p.add_argument("--stack-tokens", type=int, default=64, help="tokens per timed pass of the 43-layer stack")
     p.add_argument("--no-parity", action="store_true", help="skip the oracle comparison of the timed tokens")
     p.add_argument("--parity-tokens", type=int, default=32)
@@ -351,6 +352,11 @@ def run_ours(args):
         formats[key], rows = bench_format(m, torch, args, dev, stream, lx, wr, x, x_host, min(npar, 16))
         if rows is not None:
             checks.append((key, lx.fmt) + rows)
+    shared = None
+    if fused and world == 1 and not args.no_shared:
+        shared, rows = bench_shared(m, torch, args, dev, stream, layer, wr, x, x_host, min(npar, 8))
+        if rows is not None:
+            checks.append(("shared_expert", None) + rows)
     prefill = bench_prefill(m, torch, args, dev, stream, layer_p, E) if do_prefill else None
     stack = None
     if not args.no_stack and world == 1 and fmt == 1:
@@ -397,6 +403,7 @@ def run_ours(args):
                     "h2d_bytes_per_step": int(T * H * 2), "d2h_bytes_per_step": int(T * H * 4)},
             "clocks": clk,
             "formats": formats,
+            "shared_expert": shared,
             "stack": stack,
             "prefill": prefill,
             "verify": verify,
@@ -488,6 +495,87 @@ def bench_format(m, torch, args, dev, stream, layer, wr, x, x_host, npar):
            "e2e": {"value": round(T / (e2e_ms * 1e-3), 1), "unit": "tok/s", "h2d_bytes_per_step": int(T * H * 2),
                    "d2h_bytes_per_step": int(T * H * 4)}}
     rows = (y[:npar].cpu().numpy(), idx[:npar].cpu().numpy(), w[:npar].cpu().numpy()) if npar else None
+    return res, rows
+
+
+N_SHARED = 8   # shared-expert copies the tokens rotate over (8 x 26.7 MB > L2), standing in for 8 layers' own
+
+
+def bench_shared(m, torch, args, dev, stream, layer, wr, x, x_host, npar):
+    """The routed layer plus the always-on shared expert in Q8_0 (hidden 4096, intermediate 2048): per token the
+    fused router + routed FFN launch writes y, then the shared expert runs as a one-expert Q8_0 layer
+    (moe_expert_ffn_decode, idx 0 of its own layer, w 1, accumulate) and writes the bf16 copy. Token t reads shared
+    expert t % 8, so that the shared weights come from HBM as they do when every layer has its own. Reports the
+    combined step and the shared launch alone against the HBM roofline; returns the first npar tokens' rows for the
+    oracle comparison."""
+    from moe_inputs import GATE, UP, DOWN, expert_stack_f32
+    T = x.shape[0]
+    sh = m.Layer(4, H, I, N_SHARED, device=dev)
+    g, u, d = (torch.from_numpy(expert_stack_f32(args.seed, 1, range(N_SHARED), which, H, I)).to(dev)
+               for which in (GATE, UP, DOWN))
+    sh.pack(m.MOE_SRC_F32, g, u, d)
+    del g, u, d
+    ws_r, ws_s = layer.workspace(1, K_TOP), sh.workspace(1, 1)
+    idx = torch.zeros((T, K_TOP), dtype=torch.int32, device=dev)
+    w = torch.zeros((T, K_TOP), dtype=torch.float32, device=dev)
+    y = torch.zeros((T, H), dtype=torch.float32, device=dev)
+    yb = torch.zeros((T, H), dtype=torch.int16, device=dev)
+    sidx = (torch.arange(T, dtype=torch.int32, device=dev) % N_SHARED).reshape(T, 1).contiguous()
+    sw = torch.ones((T, 1), dtype=torch.float32, device=dev)
+
+    def step_launch():
+        for t in range(T):
+            m.moe_route_expert_ffn(layer, wr, x[t], 1, K_TOP, idx[t], w[t], y[t], None, False, ws_r, stream=stream)
+            m.moe_expert_ffn_decode(sh, x[t], sidx[t], sw[t], 1, y[t], yb[t], True, ws_s, stream=stream)
+
+    def shared_launch():
+        for t in range(T):
+            m.moe_expert_ffn_decode(sh, x[t], sidx[t], sw[t], 1, y[t], yb[t], True, ws_s, stream=stream)
+
+    with torch.cuda.stream(stream):
+        step_launch()
+    stream.synchronize()
+    if m.moe_get_device_status(ws_r, stream) != 0 or m.moe_get_device_status(ws_s, stream) != 0:
+        raise RuntimeError("device status after the shared-expert warm-up")
+    g_step, g_sh = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step, stream=stream):
+        step_launch()
+    with torch.cuda.graph(g_sh, stream=stream):
+        shared_launch()
+
+    def timed(gr, reps):
+        with torch.cuda.stream(stream):
+            for _ in range(max(1, args.warmup)):
+                gr.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(reps):
+                gr.replay()
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    reps = max(1, args.steps)
+    sh_us = timed(g_sh, reps) * 1e3 / T
+    ms_step = timed(g_step, reps)   # last: y holds one step's routed + shared output
+    if m.moe_get_device_status(ws_r, stream) != 0 or m.moe_get_device_status(ws_s, stream) != 0:
+        raise RuntimeError("device status after the shared-expert measurement")
+    alg = m.moe_packed_bytes(4, 0, 0, 1, H, I) + m.moe_packed_bytes(4, 0, 1, 1, H, I)
+    peak = peak_of(measured_peaks(), "hbm_gbs")
+    achieved = alg / (sh_us * 1e-6) / 1e9
+    res = {"format": "q8_0 (34 B per 32 weights)", "shared_experts": N_SHARED,
+           "step_kernels": "moe_route_expert_ffn (routed) + moe_expert_ffn_decode (shared, Q8_0, accumulate)",
+           "tok_s": round(T / (ms_step * 1e-3), 1), "us_per_token": round(ms_step * 1e3 / T, 3),
+           "shared_kernel_us": round(sh_us, 3), "gpu_launches": 2 * T * reps,
+           "roofline_shared": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak or 6800.0, "unit": "GB/s",
+                               "frac": round(achieved / (peak or 6800.0), 4), "traffic": None,
+                               "kernel": "ffn_kernel<q8_0>", "bytes_per_launch": alg,
+                               "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if peak else "fallback"}}
+    rows = None
+    if npar:
+        rows = (y[:npar].cpu().numpy(), idx[:npar].cpu().numpy(), w[:npar].cpu().numpy(),
+                sidx[:npar, 0].cpu().numpy(), yb[:npar].cpu().numpy().view(np.uint16))
     return res, rows
 
 
@@ -802,7 +890,27 @@ class CpuOracle:
                     return False
         return True
 
-    def parity(self, fmt, y_gpu, idx_gpu, w_gpu):
+    def parity_shared(self, y_gpu, idx_gpu, w_gpu, sidx, yb_gpu):
+        """Routed output (MXFP4, the GPU's routing) plus the Q8_0 shared expert sidx[t] (layer 1 of the same seed),
+        against the GPU's combined y within 1e-3 * (sum|routed terms| + sum|shared terms|) + 1e-6; the bf16 copy
+        equal to the round-to-nearest-even of y."""
+        par = self.parity(1, y_gpu, idx_gpu, w_gpu, extra=lambda t: self._shared(int(sidx[t]), t))
+        b = np.ascontiguousarray(y_gpu, np.float32).view(np.uint32).astype(np.uint64)
+        rne = ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
+        par["bf16_copy_exact"] = bool(np.array_equal(rne, yb_gpu))
+        par["ok"] = par["ok"] and par["bf16_copy_exact"]
+        return par
+
+    def _shared(self, e, t):
+        from moe_inputs import expert_matrix_f32
+        key = ("shared", e)
+        if key not in self.enc:
+            self.enc[key] = [self.oracle.encode(4, expert_matrix_f32(self.seed, 1, e, wh, H, I)) for wh in range(3)]
+        gb, ub, db = self.enc[key]
+        return self.oracle.moe_tokens(4, H, I, lambda _: gb, lambda _: ub, lambda _: db, np.zeros((1, 1), np.int32),
+                                      np.ones((1, 1), np.float32), self.x[t:t + 1])
+
+    def parity(self, fmt, y_gpu, idx_gpu, w_gpu, extra=None):
         """Compare the GPU's first tokens with the oracle: routing exactly (or up to proven near-ties), and y element
         by element within 1e-3 * sum|terms| + 1e-6 (the FFN of the GPU's own routing, so that a near-tie swap does
         not mask the FFN's check). NaN must match NaN."""
@@ -814,6 +922,11 @@ class CpuOracle:
             res = list(ex.map(lambda t: self._moe(fmt, idx_gpu[t:t + 1], w_gpu[t:t + 1], self.x[t:t + 1]), range(n)))
         y_ref = np.concatenate([r[0] for r in res])
         ab = np.concatenate([r[1] for r in res])
+        if extra is not None:   # a further term of every token's output (the shared expert), added in fp64
+            for t in range(n):
+                ye, abe = extra(t)
+                y_ref[t] += ye[0]
+                ab[t] += abe[0]
         y = np.asarray(y_gpu, dtype=np.float64)
         nan_ok = bool(np.array_equal(np.isnan(y), np.isnan(y_ref)))
         fin = ~np.isnan(y_ref)
@@ -855,13 +968,17 @@ def main():
     breach = False
     if single and (checks or not args.no_cpu_baseline):
         co = CpuOracle(args.seed, max([len(c[2]) for c in checks] + [0]), args.experts)
-        for key, fmt, y_rows, idx_rows, w_rows in checks:
-            par = co.parity(fmt, y_rows, idx_rows, w_rows)
-            breach |= not par["ok"]
-            if key is None:
-                out["parity"] = par
+        for key, fmt, y_rows, idx_rows, w_rows, *more in checks:
+            if key == "shared_expert":
+                par = co.parity_shared(y_rows, idx_rows, w_rows, *more)
+                out["shared_expert"]["parity"] = par
             else:
-                out["formats"][key]["parity"] = par
+                par = co.parity(fmt, y_rows, idx_rows, w_rows)
+                if key is None:
+                    out["parity"] = par
+                else:
+                    out["formats"][key]["parity"] = par
+            breach |= not par["ok"]
         if not args.no_cpu_baseline:
             out["cpu_baseline"] = co.timed(args.fmt, args.cpu_seconds)
     print(json.dumps(out))

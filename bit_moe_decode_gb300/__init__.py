@@ -14,7 +14,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe.so")
 
-MOE_FMT_MXFP4, MOE_FMT_INT4G32, MOE_FMT_Q2K = 1, 2, 3
+MOE_FMT_MXFP4, MOE_FMT_INT4G32, MOE_FMT_Q2K, MOE_FMT_Q8_0 = 1, 2, 3, 4
 MOE_SRC_BLOCKS, MOE_SRC_F32 = 0, 1
 MOE_LAYOUT_DECODE, MOE_LAYOUT_TC = 0, 1
 MOE_LAYOUT_PREFILL = MOE_LAYOUT_TC
@@ -24,7 +24,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_SHAPE", 3: "MOE_ERR
           4: "MOE_ERR_UNSUPPORTED_ARCH", 5: "MOE_ERR_WORKSPACE_TOO_SMALL", 6: "MOE_ERR_CUDA",
           7: "MOE_ERR_DEVICE_TIMEOUT", 8: "MOE_ERR_FAULT_INJECTED"}
 # canonical block geometry: (weights per block, bytes per block)
-BLOCK = {MOE_FMT_MXFP4: (32, 17), MOE_FMT_INT4G32: (32, 18), MOE_FMT_Q2K: (256, 84)}
+BLOCK = {MOE_FMT_MXFP4: (32, 17), MOE_FMT_INT4G32: (32, 18), MOE_FMT_Q2K: (256, 84), MOE_FMT_Q8_0: (32, 34)}
 
 # every symbol include/moe.h declares
 EXPORTS = ["moe_status_string", "moe_version", "moe_check_device", "moe_canonical_bytes", "moe_packed_bytes",

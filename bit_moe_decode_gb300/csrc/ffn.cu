@@ -68,7 +68,7 @@ template <int FMT> struct Cfg {
   static constexpr int CW = FMT == MOE_FMT_Q2K ? 8 : 16;
   static constexpr int PROD = CW, EPI = CW + 1, THREADS = (CW + 2) * 32;
   static constexpr int SB = F::CPS * F::CB;                                // stage bytes (2048 columns)
-  static constexpr int NS = FMT == MOE_FMT_Q2K ? 13 : 8;                   // ring stages
+  static constexpr int NS = FMT == MOE_FMT_Q2K ? 13 : FMT == MOE_FMT_Q8_0 ? 10 : 8;   // ring stages
   static constexpr int NCH = 4096 / F::CK / CW;                            // max chunks per warp per tile
   static constexpr int NPS = F::CPS / CW;                                  // chunks per warp per stage
   static constexpr int SXF = 0;
@@ -127,6 +127,41 @@ __device__ __forceinline__ void chunk_mma(const uint8_t* cp, int lane, const uin
       }
       const uint32_t sv = blk == 0 ? sc.x : sc.y;
       const float sr = bf16_bits_to_f32(sv & 0xFFFFu), sr8 = bf16_bits_to_f32(sv >> 16);
+      acc[0] = fmaf(c[0], sr, acc[0]);
+      acc[1] = fmaf(c[1], sr, acc[1]);
+      acc[2] = fmaf(c[2], sr8, acc[2]);
+      acc[3] = fmaf(c[3], sr8, acc[3]);
+    }
+  } else if constexpr (FMT == MOE_FMT_Q8_0) {
+    // Each 32-bit word holds registers 2i, 2i+1 of a step (4 codes). A code q (two's complement) becomes the fp16
+    // 1024 + (q ^ 0x80) = 1152 + q once the byte sits under the exponent byte 0x64; an exact fma subtracts 1152.
+    // |q| <= 128 is exact in fp16 and so is every product with an fp16 x in the fp32 sums; d scales each 32-block.
+    const uint4 c0 = *reinterpret_cast<const uint4*>(cp + lane * 32);
+    const uint4 c1 = *reinterpret_cast<const uint4*>(cp + lane * 32 + 16);
+    const uint2 sc = *reinterpret_cast<const uint2*>(cp + 1024 + (lane >> 2) * 8);
+    const uint32_t flip = 0x80808080u;
+    const uint32_t words[8] = {c0.x ^ flip, c0.y ^ flip, c0.z ^ flip, c0.w ^ flip,
+                               c1.x ^ flip, c1.y ^ flip, c1.z ^ flip, c1.w ^ flip};
+    const uint32_t one = 0x3C003C00u, m1152 = 0xE480E480u, e64 = 0x64646464u;
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+      float c[4];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int st = 2 * blk + h;
+        uint32_t a[4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          uint32_t v;
+          asm("prmt.b32 %0, %1, %2, %3;" : "=r"(v) : "r"(words[2 * st + (b >> 1)]), "r"(e64),
+              "r"((b & 1) ? 0x4342u : 0x4140u));
+          a[b] = hfma2(v, one, m1152);
+        }
+        if (h == 0) mma_f16(c, a[0], a[1], a[2], a[3], bx[st][0], bx[st][1], zero);
+        else mma_f16(c, a[0], a[1], a[2], a[3], bx[st][0], bx[st][1], c);
+      }
+      const uint32_t sv = blk == 0 ? sc.x : sc.y;
+      const float sr = h16_to_f32(sv & 0xFFFFu), sr8 = h16_to_f32(sv >> 16);
       acc[0] = fmaf(c[0], sr, acc[0]);
       acc[1] = fmaf(c[1], sr, acc[1]);
       acc[2] = fmaf(c[2], sr8, acc[2]);
@@ -642,7 +677,7 @@ static moe_status_t ffn_common(const char* site, const moe_layer_t* L, const voi
                                size_t ws_bytes, void* stream) {
   if (site && moe_internal::fault(site)) return MOE_ERR_FAULT_INJECTED;
   if (!L || !x || !idx || !w || !y || !ws) return MOE_ERR_INVALID_ARG;
-  if (L->fmt < MOE_FMT_MXFP4 || L->fmt > MOE_FMT_Q2K) return MOE_ERR_UNSUPPORTED_FORMAT;
+  if (L->fmt < MOE_FMT_MXFP4 || L->fmt > MOE_FMT_Q8_0) return MOE_ERR_UNSUPPORTED_FORMAT;
   if (L->layout != MOE_LAYOUT_DECODE && L->layout != MOE_LAYOUT_TC) return MOE_ERR_UNSUPPORTED_FORMAT;
   if (!L->gate_up || !L->down || ((uintptr_t)L->gate_up & 15) || ((uintptr_t)L->down & 15)) return MOE_ERR_INVALID_ARG;
   if (((uintptr_t)x & 3) || ((uintptr_t)ws & 255) || ((uintptr_t)y & 3)) return MOE_ERR_INVALID_ARG;
@@ -679,6 +714,7 @@ static moe_status_t ffn_common(const char* site, const moe_layer_t* L, const voi
   switch (L->fmt) {
     case MOE_FMT_MXFP4: return launch_ffn<MOE_FMT_MXFP4>(a, s);
     case MOE_FMT_INT4G32: return launch_ffn<MOE_FMT_INT4G32>(a, s);
+    case MOE_FMT_Q8_0: return launch_ffn<MOE_FMT_Q8_0>(a, s);
     default: return launch_ffn<MOE_FMT_Q2K>(a, s);
   }
 }

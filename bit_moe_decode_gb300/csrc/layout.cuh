@@ -1,6 +1,6 @@
 // layout.cuh -- the packed device layouts of expert weights.
 //
-// ---- MOE_LAYOUT_DECODE (all three formats; the mat-vec kernels of ffn.cu)
+// ---- MOE_LAYOUT_DECODE (all four formats; the mat-vec kernels of ffn.cu)
 //
 // A matrix is cut into TILES of 16 rows x K and each tile into CHUNKS of 16 rows x CK columns along K.
 //   Gate/Up: tile j holds gate rows 8j..8j+7 (tile rows 0..7) and up rows 8j..8j+7 (tile rows 8..15), so one
@@ -10,18 +10,22 @@
 //   MXFP4   CK = 64,  512 B codes + 32 B E8M0            = 544 B
 //   INT4    CK = 64,  512 B codes + 64 B bf16 scales     = 576 B
 //   Q2_K    CK = 256, 1024 B codes + 256 B sc|m + 64 B d,dmin = 1344 B
+//   Q8_0    CK = 64,  1024 B codes + 64 B fp16 scales     = 1088 B
 // Codes are in mma.m16n8k16 A-fragment order: lane l owns (CK/64) x 16 consecutive bytes; its rows are l/4 and
-// l/4 + 8 and its k offsets inside a 16-wide step are 2(l%4), 2(l%4)+1, +8, +9.
+// l/4 + 8 and its k offsets inside a 16-wide step are 2(l%4), 2(l%4)+1, +8, +9 (Q8_0: lane l owns 32 bytes).
 //   MXFP4: byte (l*16 + j*4 + b) = codes of (row l/4 + 8*(b&1), k = 16j + 2(l%4) + 8*(b>>1) + {0: low nibble,
 //          1: high nibble}) -- the byte feeds cvt.rn.f16x2.e2m1x2 directly.
 //   INT4:  32-bit word (l*16 + j*4): register b's lower-k nibble at bits 4b..4b+3, its higher-k nibble at bits
 //          16+4b..16+4b+3 (two's complement codes), decoded with an exponent-bias trick into exact fp16.
 //   Q2_K:  32-bit word (l*32 + w*4) holds steps 2w and 2w+1; step s = 2w + t, register b: lower-k 2-bit code at
 //          bits 8t + 2b, higher-k code at bits 16 + 8t + 2b.
+//   Q8_0:  byte (l*32 + j*8 + 2b + h) = the two's-complement code of (row l/4 + 8*(b&1), k = 16j + 2(l%4) +
+//          8*(b>>1) + h): register b of step j is one 32-bit half of an 8-byte word.
 // Scales: MXFP4 word r (r < 8) = {e[r][blk0], e[r+8][blk0], e[r][blk1], e[r+8][blk1]};
 //         INT4  8 bytes per r  = bf16 {s[r][blk0], s[r+8][blk0], s[r][blk1], s[r+8][blk1]};
 //         Q2_K  32 bytes per r = scales[16] of row r then of row r+8; then 8 bytes per r = fp16 {d[r], dmin[r],
-//               d[r+8], dmin[r+8]}.
+//               d[r+8], dmin[r+8]};
+//         Q8_0  8 bytes per r  = fp16 {d[r][blk0], d[r+8][blk0], d[r][blk1], d[r+8][blk1]}.
 #pragma once
 #include <cstdint>
 
@@ -40,12 +44,20 @@ template <> struct Fmt<MOE_FMT_Q2K> {
   static constexpr int BS = 256, BB = 84;
   static constexpr int CK = 256, CODE = 1024, CB = 1344, STEPS = 16, CPS = 8;
 };
-// CPS = chunks per pipeline stage: every stage covers 2048 columns of K.
+template <> struct Fmt<MOE_FMT_Q8_0> {
+  static constexpr int BS = 32, BB = 34;
+  static constexpr int CK = 64, CODE = 1024, CB = 1088, STEPS = 4, CPS = 16;
+};
+// CPS = chunks per pipeline stage: a stage covers 2048 columns of K (1024 for Q8_0, whose chunks are twice as big).
 
 __host__ __device__ inline int fmt_ck(int fmt) { return fmt == MOE_FMT_Q2K ? 256 : 64; }
-__host__ __device__ inline int fmt_cb(int fmt) { return fmt == MOE_FMT_MXFP4 ? 544 : fmt == MOE_FMT_INT4G32 ? 576 : 1344; }
+__host__ __device__ inline int fmt_cb(int fmt) {
+  return fmt == MOE_FMT_MXFP4 ? 544 : fmt == MOE_FMT_INT4G32 ? 576 : fmt == MOE_FMT_Q2K ? 1344 : 1088;
+}
 __host__ __device__ inline int fmt_bs(int fmt) { return fmt == MOE_FMT_Q2K ? 256 : 32; }
-__host__ __device__ inline int fmt_bb(int fmt) { return fmt == MOE_FMT_MXFP4 ? 17 : fmt == MOE_FMT_INT4G32 ? 18 : 84; }
+__host__ __device__ inline int fmt_bb(int fmt) {
+  return fmt == MOE_FMT_MXFP4 ? 17 : fmt == MOE_FMT_INT4G32 ? 18 : fmt == MOE_FMT_Q2K ? 84 : 34;
+}
 
 // bytes of one tile (16 rows x K)
 __host__ __device__ inline int64_t tile_bytes(int fmt, int64_t K) { return (K / fmt_ck(fmt)) * fmt_cb(fmt); }

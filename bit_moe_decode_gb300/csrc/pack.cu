@@ -2,6 +2,8 @@
 //
 // Formats: "quantization" glossary (ds4-learning.pages.dev), sections "MXFP4" and "core principle" (Q2_K);
 // INT4 group 32: "DeepSeek-V4-Flash-0731-W4A16" model card (alphaneural.io), "FP4 -> INT4 conversion" step 2.
+// Q8_0 (the shared expert's "Q8" of "Mixed-precision compression of DeepSeek-V4-Flash", "The recipe"; the pages
+// give no layout, so the library defines one scale per 32 weights like the other formats).
 // All encoder arithmetic is fp32 with round-to-nearest-even and no contraction (explicit __f*_rn intrinsics).
 #include "common.cuh"
 #include "layout.cuh"
@@ -103,6 +105,26 @@ __device__ void enc_q2k(const float* w, uint8_t* out /*84*/) {
   out[82] = (uint8_t)(mb & 255); out[83] = (uint8_t)(mb >> 8);
 }
 
+// Q8_0: d = fp16(amax / 127); q = clamp(rint(w / d), -127, 127), 0 where d = 0 or the quotient is NaN.
+__device__ void enc_q8_0(const float* w, uint8_t* out /*34*/) {
+  float amax = 0.f;
+  for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(w[j]));   // NaN inputs do not raise amax
+  const __half dh = __float2half_rn(__fdiv_rn(amax, 127.0f));
+  const float d = __half2float(dh);
+  const uint16_t db = __half_as_ushort(dh);
+  out[0] = (uint8_t)(db & 255);
+  out[1] = (uint8_t)(db >> 8);
+  for (int j = 0; j < 32; ++j) {
+    float q = 0.f;
+    if (d != 0.f) {
+      q = rintf(__fdiv_rn(w[j], d));
+      if (q != q) q = 0.f;                 // before the clamp: fminf / fmaxf would turn NaN into a bound
+      q = fminf(fmaxf(q, -127.f), 127.f);
+    }
+    out[2 + j] = (uint8_t)(int8_t)(int)q;
+  }
+}
+
 template <int FMT>
 __device__ __forceinline__ void get_block(const void* src, moe_src_t kind, int64_t blk, uint8_t* out) {
   constexpr int BS = Fmt<FMT>::BS, BB = Fmt<FMT>::BB;
@@ -115,6 +137,7 @@ __device__ __forceinline__ void get_block(const void* src, moe_src_t kind, int64
     for (int i = 0; i < BS; ++i) w[i] = p[i];
     if (FMT == MOE_FMT_MXFP4) enc_mxfp4(w, out);
     else if (FMT == MOE_FMT_INT4G32) enc_int4(w, out);
+    else if (FMT == MOE_FMT_Q8_0) enc_q8_0(w, out);
     else enc_q2k(w, out);
   }
 }
@@ -194,6 +217,17 @@ __global__ void pack_kernel(moe_src_t skind, moe_matrix_t kind, int64_t n_e, int
         uint32_t v = (uint32_t)blk[16] | ((uint32_t)blk[17] << 8);
         or_bits(tb, half & ~3LL, v << (8 * (int)(half & 3)));
       }
+    } else if (FMT == MOE_FMT_Q8_0) {
+      for (int j = 0; j < 32; ++j) {
+        CodePos p = code_pos(FMT, (int)tr, k0 + j);
+        int64_t byte = (int64_t)p.chunk * CB + p.lane * 32 + p.step * 8 + 2 * p.reg + p.hi;
+        or_bits(tb, byte & ~3LL, (uint32_t)blk[2 + j] << (8 * (int)(byte & 3)));
+      }
+      int chunk = k0 / CK, blk_in_chunk = (k0 % CK) / 32;
+      int r = (int)(tr % 8), hi_row = tr >= 8 ? 1 : 0;
+      int64_t half = (int64_t)chunk * CB + CODE + r * 8 + (blk_in_chunk * 2 + hi_row) * 2;
+      uint32_t v = (uint32_t)blk[0] | ((uint32_t)blk[1] << 8);
+      or_bits(tb, half & ~3LL, v << (8 * (int)(half & 3)));
     } else {  // Q2_K: one super-block = one chunk row
       int chunk = k0 / CK;
       int64_t cbase = (int64_t)chunk * CB;
@@ -254,6 +288,11 @@ __global__ void unpack_kernel(moe_matrix_t kind, int64_t H, int64_t I, const uin
       int blk = (int)((k % CK) / 32);
       uint16_t sb = *(const uint16_t*)(cb + CODE + r * 8 + (blk * 2 + hi_row) * 2);
       v = (float)q * __uint_as_float((uint32_t)sb << 16);
+    } else if (FMT == MOE_FMT_Q8_0) {
+      const int q = (int)(int8_t)cb[p.lane * 32 + p.step * 8 + 2 * p.reg + p.hi];
+      int blk = (int)((k % CK) / 32);
+      uint16_t db = *(const uint16_t*)(cb + CODE + r * 8 + (blk * 2 + hi_row) * 2);
+      v = (float)q * __half2float(__ushort_as_half(db));
     } else {
       uint32_t word = *(const uint32_t*)(cb + p.lane * 32 + (p.step / 2) * 4);
       int q = (word >> ((p.hi ? 16 : 0) + 8 * (p.step % 2) + 2 * p.reg)) & 3;
@@ -321,13 +360,13 @@ __global__ void unpack_tc_kernel(moe_matrix_t kind, int64_t H, int64_t I, const 
 using namespace moe;
 
 extern "C" size_t moe_canonical_bytes(moe_format_t fmt, int64_t rows, int64_t k) {
-  if (fmt < MOE_FMT_MXFP4 || fmt > MOE_FMT_Q2K || rows < 0 || k < 0 || k % fmt_bs(fmt)) return 0;
+  if (fmt < MOE_FMT_MXFP4 || fmt > MOE_FMT_Q8_0 || rows < 0 || k < 0 || k % fmt_bs(fmt)) return 0;
   return (size_t)(rows * (k / fmt_bs(fmt)) * fmt_bb(fmt));
 }
 
 extern "C" size_t moe_packed_bytes(moe_format_t fmt, moe_layout_t layout, moe_matrix_t kind, int64_t n_e, int64_t H,
                                    int64_t I) {
-  if (fmt < MOE_FMT_MXFP4 || fmt > MOE_FMT_Q2K || n_e < 0) return 0;
+  if (fmt < MOE_FMT_MXFP4 || fmt > MOE_FMT_Q8_0 || n_e < 0) return 0;
   if (!moe_internal::shape_ok(H, I)) return 0;
   if (layout == MOE_LAYOUT_PREFILL) {
     if (fmt != MOE_FMT_MXFP4 || (kind != MOE_MAT_GATE_UP && kind != MOE_MAT_DOWN)) return 0;
@@ -349,7 +388,7 @@ extern "C" moe_status_t moe_encode_blocks(moe_format_t fmt, const float* src, in
                                           void* stream) {
   MOE_NVTX("moe_encode_blocks");
   if (moe_internal::fault("encode")) return MOE_ERR_FAULT_INJECTED;
-  if (fmt < MOE_FMT_MXFP4 || fmt > MOE_FMT_Q2K) return MOE_ERR_UNSUPPORTED_FORMAT;
+  if (fmt < MOE_FMT_MXFP4 || fmt > MOE_FMT_Q8_0) return MOE_ERR_UNSUPPORTED_FORMAT;
   if (!src || !dst || rows < 0 || k < 0) return MOE_ERR_INVALID_ARG;
   if (k % fmt_bs(fmt)) return MOE_ERR_SHAPE;
   moe_status_t st = moe_check_device();
@@ -361,6 +400,7 @@ extern "C" moe_status_t moe_encode_blocks(moe_format_t fmt, const float* src, in
   switch (fmt) {
     case MOE_FMT_MXFP4: encode_kernel<MOE_FMT_MXFP4><<<grid_for(nblk, thr), thr, 0, s>>>(src, nblk, (uint8_t*)dst); break;
     case MOE_FMT_INT4G32: encode_kernel<MOE_FMT_INT4G32><<<grid_for(nblk, thr), thr, 0, s>>>(src, nblk, (uint8_t*)dst); break;
+    case MOE_FMT_Q8_0: encode_kernel<MOE_FMT_Q8_0><<<grid_for(nblk, thr), thr, 0, s>>>(src, nblk, (uint8_t*)dst); break;
     default: encode_kernel<MOE_FMT_Q2K><<<grid_for(nblk, thr), thr, 0, s>>>(src, nblk, (uint8_t*)dst); break;
   }
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
@@ -371,7 +411,7 @@ extern "C" moe_status_t moe_pack_weights(moe_format_t fmt, moe_src_t src_kind, m
                                          void* dst, size_t dst_bytes, void* stream) {
   MOE_NVTX("moe_pack_weights");
   if (moe_internal::fault("pack")) return MOE_ERR_FAULT_INJECTED;
-  if (fmt < MOE_FMT_MXFP4 || fmt > MOE_FMT_Q2K) return MOE_ERR_UNSUPPORTED_FORMAT;
+  if (fmt < MOE_FMT_MXFP4 || fmt > MOE_FMT_Q8_0) return MOE_ERR_UNSUPPORTED_FORMAT;
   if (src_kind != MOE_SRC_BLOCKS && src_kind != MOE_SRC_F32) return MOE_ERR_INVALID_ARG;
   if (kind != MOE_MAT_GATE_UP && kind != MOE_MAT_DOWN) return MOE_ERR_INVALID_ARG;
   if (!src_a || !dst || (kind == MOE_MAT_GATE_UP && !src_b)) return MOE_ERR_INVALID_ARG;
@@ -401,6 +441,9 @@ extern "C" moe_status_t moe_pack_weights(moe_format_t fmt, moe_src_t src_kind, m
     case MOE_FMT_INT4G32:
       pack_kernel<MOE_FMT_INT4G32><<<grid_for(nblk, thr), thr, 0, s>>>(src_kind, kind, n_e, H, I, src_a, src_b, (uint8_t*)dst);
       break;
+    case MOE_FMT_Q8_0:
+      pack_kernel<MOE_FMT_Q8_0><<<grid_for(nblk, thr), thr, 0, s>>>(src_kind, kind, n_e, H, I, src_a, src_b, (uint8_t*)dst);
+      break;
     default:
       pack_kernel<MOE_FMT_Q2K><<<grid_for(nblk, thr), thr, 0, s>>>(src_kind, kind, n_e, H, I, src_a, src_b, (uint8_t*)dst);
       break;
@@ -410,7 +453,7 @@ extern "C" moe_status_t moe_pack_weights(moe_format_t fmt, moe_src_t src_kind, m
 
 extern "C" moe_status_t moe_debug_unpack(moe_format_t fmt, moe_layout_t layout, moe_matrix_t kind, const void* packed,
                                          int64_t H, int64_t I, int64_t expert, float* out, void* stream) {
-  if (fmt < MOE_FMT_MXFP4 || fmt > MOE_FMT_Q2K) return MOE_ERR_UNSUPPORTED_FORMAT;
+  if (fmt < MOE_FMT_MXFP4 || fmt > MOE_FMT_Q8_0) return MOE_ERR_UNSUPPORTED_FORMAT;
   if (!packed || !out || expert < 0) return MOE_ERR_INVALID_ARG;
   if (!moe_internal::shape_ok(H, I)) return MOE_ERR_SHAPE;
   if (layout != MOE_LAYOUT_DECODE && layout != MOE_LAYOUT_PREFILL) return MOE_ERR_INVALID_ARG;
@@ -427,6 +470,7 @@ extern "C" moe_status_t moe_debug_unpack(moe_format_t fmt, moe_layout_t layout, 
   switch (fmt) {
     case MOE_FMT_MXFP4: unpack_kernel<MOE_FMT_MXFP4><<<grid_for(total, thr), thr, 0, s>>>(kind, H, I, (const uint8_t*)packed, expert, out); break;
     case MOE_FMT_INT4G32: unpack_kernel<MOE_FMT_INT4G32><<<grid_for(total, thr), thr, 0, s>>>(kind, H, I, (const uint8_t*)packed, expert, out); break;
+    case MOE_FMT_Q8_0: unpack_kernel<MOE_FMT_Q8_0><<<grid_for(total, thr), thr, 0, s>>>(kind, H, I, (const uint8_t*)packed, expert, out); break;
     default: unpack_kernel<MOE_FMT_Q2K><<<grid_for(total, thr), thr, 0, s>>>(kind, H, I, (const uint8_t*)packed, expert, out); break;
   }
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;

@@ -49,9 +49,13 @@ typedef enum {
                           byte 1+j, element 2j+1 = low nibble; value E2M1[code] * 2^(e-127), e=0 -> 0, e=255 -> NaN */
   MOE_FMT_INT4G32 = 2, /* 18 B per 32 weights: bytes 0..15 two's-complement 4-bit codes (same nibble order),
                           bytes 16..17 bf16 scale (little endian); value q * scale */
-  MOE_FMT_Q2K = 3      /* 84 B per 256 weights: scales[16] (sc = low nibble, m = high nibble, one per 16 weights),
+  MOE_FMT_Q2K = 3,     /* 84 B per 256 weights: scales[16] (sc = low nibble, m = high nibble, one per 16 weights),
                           qs[64] (weight i = bits 2(i%4)..2(i%4)+1 of qs[i/4]), fp16 d, fp16 dmin;
                           value d*sc*q - dmin*m */
+  MOE_FMT_Q8_0 = 4     /* 34 B per 32 weights: bytes 0..1 fp16 d (little endian), bytes 2..33 two's-complement
+                          8-bit codes; value d*q. The shared expert's format ("Q8" in the recipe of
+                          "Mixed-precision compression of DeepSeek-V4-Flash"; the pages give no layout, this library
+                          defines it). DECODE layout only. */
 } moe_format_t;
 
 typedef enum {
@@ -99,6 +103,8 @@ size_t moe_packed_bytes(moe_format_t fmt, moe_layout_t layout, moe_matrix_t kind
  * Q2_K:  per 16-weight group lo = min(0, min w), s_g = (max w - lo)/3, o_g = -lo; d = fp16(max s_g / 15),
  *        dmin = fp16(max o_g / 15); sc = rint(s_g/d), m = rint(o_g/dmin) clamped to [0,15];
  *        q = clamp(rint((w + dmin*m)/(d*sc)), 0, 3) (the pages give no encoder; this is the library's own).
+ * Q8_0:  per 32 weights d = fp16(amax / 127); q = clamp(rint(w / d), -127, 127), q = 0 where d = 0 or w / d is
+ *        NaN (the library's own; -128 is never produced).
  * All arithmetic fp32 round-to-nearest-even; bit-identical to the CPU oracle. k must be a multiple of the block
  * size. src and dst device pointers; dst 16-byte aligned is not required. */
 moe_status_t moe_encode_blocks(moe_format_t fmt, const float* src, int64_t rows, int64_t k, void* dst, void* stream);

@@ -11,8 +11,8 @@ import torch
 import oracle
 from moe_inputs import expert_matrix_f32, router_f16_bits, x_bf16_bits
 
-FMTS = [1, 2, 3]
-FMT_NAME = {1: "mxfp4", 2: "int4g32", 3: "q2k"}
+FMTS = [1, 2, 3, 4]
+FMT_NAME = {1: "mxfp4", 2: "int4g32", 3: "q2k", 4: "q8_0"}
 
 
 def tol_check(y_gpu: np.ndarray, y_ref: np.ndarray, absterm: np.ndarray, what: str = ""):

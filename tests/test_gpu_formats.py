@@ -124,4 +124,4 @@ def test_packed_bytes_equal_canonical_bytes(m):
     # active bytes per token-layer, DS4-Flash shape, top-6
     per_tok = {f: 6 * (m.moe_packed_bytes(f, 0, 0, 1, 4096, 2048) + m.moe_packed_bytes(f, 0, 1, 1, 4096, 2048))
                for f in FMTS}
-    assert per_tok == {1: 80216064, 2: 84934656, 3: 49545216}
+    assert per_tok == {1: 80216064, 2: 84934656, 3: 49545216, 4: 160432128}
