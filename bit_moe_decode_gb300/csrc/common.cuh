@@ -139,6 +139,17 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+// Release add: the caller's earlier writes, and those ordered before it by a CTA or warp barrier, are visible to
+// any thread that reads the counter with acquire semantics and sees the addition. Much cheaper under load than a
+// full fence (__threadfence) followed by a relaxed atomic.
+__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t atom_acq_rel_add(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 // Wait until *p >= target; false on timeout.
 __device__ __forceinline__ bool wait_counter(const uint32_t* p, uint32_t target, long long limit_ns) {
   if (ld_acquire_u32(p) >= target) return true;

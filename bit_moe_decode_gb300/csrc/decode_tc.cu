@@ -334,14 +334,6 @@ __device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, volatile i
     if (globaltimer_ns() - t0 > lim) { *abort_flag = 1; return false; }
   }
 }
-__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ uint32_t atom_acq_rel_add(uint32_t* p, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
 // K-major operand with 32-byte rows and the 32-byte swizzle (8-row atoms of 256 bytes)
 __device__ __forceinline__ uint64_t umma_desc_sw32(uint32_t saddr) { return umma_desc(saddr, 16, 256, 6); }
 // kind::mxf4 instruction descriptor with separate scale-byte selectors for A and B (0 or 2)

@@ -21,9 +21,12 @@
 //     projection; the combine sums the ranks in rank order with fp32 FMAs.
 //   * Width-1 exactness: a token's column goes through the same instructions whatever T is (column-independent
 //     MMA, per-token rescale, fixed warp and rank orders), so verify row t equals decode of token t bitwise.
-//   * Handoff G -> D: per-expert counters (acquire/release); D units wait (bounded) for all G tiles of their
-//     expert. The combine for a 16-row output tile is done by the CTA that finishes its last expert (counter),
-//     so no floating-point atomics are used anywhere. The last CTA to finish clears the counters.
+//   * Handoff G -> D: per-expert counters, published with release adds and read with acquire loads (a full
+//     fence before a relaxed atomic costs microseconds under load); D units wait (bounded) for all G tiles of
+//     their expert. Then a grid barrier and each CTA combines its share of the output rows in a fixed order, so no
+//     floating-point atomics are used anywhere. When every token has a single expert (a shared expert, k = 1) the
+//     owner of a down tile writes y directly with the same arithmetic and the grid barrier is skipped. The last
+//     CTA to finish clears the counters.
 #include <mutex>
 
 #include "common.cuh"
@@ -294,7 +297,7 @@ __global__ void __launch_bounds__(Cfg<FMT>::THREADS, 1) ffn_kernel(const FfnArgs
   __shared__ int s_nu[kMaxT];                   // per token: its union experts in ascending order ...
   __shared__ int s_ulist[kMaxT][kMaxK];
   __shared__ float s_uw[kMaxT][kMaxK];          // ... and their summed weights
-  __shared__ int s_U, s_last;
+  __shared__ int s_U, s_last, s_direct;
   __shared__ volatile int s_abort;
   __shared__ int s_sig[kMaxT];
   __shared__ float s_colmax[kMaxCW][kMaxT];
@@ -376,8 +379,11 @@ __global__ void __launch_bounds__(Cfg<FMT>::THREADS, 1) ffn_kernel(const FfnArgs
         if (s_routed[lane][u]) { s_ulist[lane][n] = u; s_uw[lane][n] = s_wsum[lane][u]; ++n; }
       s_nu[lane] = n;
     }
+    const int nu_lane = lane < T ? s_nu[lane] : 1;
+    const int direct = __all_sync(0xffffffffu, nu_lane == 1);
     if (lane == 0) {
       s_U = nfirst;
+      s_direct = direct;
       if (bad) { s_abort = 1; if (blockIdx.x == 0) record_error(&a.hdr->status, MOE_ERR_INVALID_ARG); }
     }
   }
@@ -385,10 +391,12 @@ __global__ void __launch_bounds__(Cfg<FMT>::THREADS, 1) ffn_kernel(const FfnArgs
   const int U = s_U;
   const int G = gridDim.x, bid = blockIdx.x;
   const int gt = I / 8, dt = H / 16;  // tiles per expert
-  const int64_t NG = (int64_t)U * gt, ND = (int64_t)U * dt;
-  const int64_t g0 = NG * bid / G, g1 = NG * (bid + 1) / G;
-  const int64_t d0 = ND * bid / G, d1 = ND * (bid + 1) / G;
-  const int m0 = (int)((int64_t)dt * bid / G), m1 = (int)((int64_t)dt * (bid + 1) / G);
+  // 32-bit unit arithmetic (U * gt <= 64 * 512 units): a 64-bit division is a long software sequence on the path
+  // from the prologue to the first weight copy
+  const uint32_t NG = (uint32_t)(U * gt), ND = (uint32_t)(U * dt), uG = (uint32_t)G, ub = (uint32_t)bid;
+  const int g0 = (int)(NG * ub / uG), g1 = (int)(NG * (ub + 1) / uG);
+  const int d0 = (int)(ND * ub / uG), d1 = (int)(ND * (ub + 1) / uG);
+  const int m0 = (int)((uint32_t)dt * ub / uG), m1 = (int)((uint32_t)dt * (ub + 1) / uG);
   const int ncg = H / F::CK, ncd = I / F::CK;                       // chunks per G / D tile
   const int64_t tbg = tile_bytes(FMT, H), tbd = tile_bytes(FMT, I);
   const int64_t sgu = gate_up_stride(FMT, H, I), sdn = down_stride(FMT, H, I);
@@ -411,12 +419,12 @@ __global__ void __launch_bounds__(Cfg<FMT>::THREADS, 1) ffn_kernel(const FfnArgs
           ++it;
         }
       };
-      for (int64_t gu = g0; gu < g1 && ok; ++gu) {
-        const int u = (int)(gu / gt), j = (int)(gu % gt);
+      for (int gu = g0; gu < g1 && ok; ++gu) {
+        const int u = gu / gt, j = gu % gt;
         issue_tile(a.gate_up + (size_t)s_union[u] * sgu + (size_t)j * tbg, ncg);
       }
-      for (int64_t du = d0; du < d1 && ok; ++du) {
-        const int u = (int)(du / dt), m = (int)(du % dt);
+      for (int du = d0; du < d1 && ok; ++du) {
+        const int u = du / dt, m = du % dt;
         issue_tile(a.down + (size_t)s_union[u] * sdn + (size_t)m * tbd, ncd);
       }
       if (!ok) {
@@ -446,9 +454,11 @@ __global__ void __launch_bounds__(Cfg<FMT>::THREADS, 1) ffn_kernel(const FfnArgs
       if (lane == 0) mbar_arrive(&redempty[r % kNR]);
     };
     int pend_u = -1, pend_n = 0;  // G tiles done but not yet published, for one expert
-    for (int64_t gu = g0; gu < g1; ++gu, ++ri) {
-      const int u = (int)(gu / gt), jt = (int)(gu % gt);
+    for (int gu = g0; gu < g1; ++gu, ++ri) {
+      const int u = gu / gt, jt = gu % gt;
       const float* rb = wait_red(ri);
+      uint32_t hmax[2] = {0u, 0u};
+      int htc[2] = {-1, -1};
 #pragma unroll
       for (int pp = 0; pp < 2; ++pp) {
         // output pair p -> fragment lane fl, column slot cc: g from c[cc] (row fl/4), u from c[cc+2] (row fl/4+8)
@@ -465,22 +475,32 @@ __global__ void __launch_bounds__(Cfg<FMT>::THREADS, 1) ffn_kernel(const FfnArgs
           const float g = gs * inv, uu = us * inv;
           const float h = g * __frcp_rn(1.0f + __expf(-g)) * uu;   // SiLU(g) * u
           a.hbuf[((size_t)u * kMaxT + tc) * I + (size_t)jt * 8 + r] = h;
-          atomicMax(&a.amax_h[u * kMaxT + tc], __float_as_uint(fabsf(h)));
+          hmax[pp] = __float_as_uint(fabsf(h));
+          htc[pp] = tc;
         }
       }
-      release_red(ri);
+      // max |h| per token: the warp's largest first (non-negative floats, NaN included, order like their bit
+      // patterns), then one atomic per token instead of one per lane
+      for (int t = 0; t < T; ++t) {
+        const uint32_t v = __reduce_max_sync(0xffffffffu, max(htc[0] == t ? hmax[0] : 0u, htc[1] == t ? hmax[1] : 0u));
+        if (lane == 0) atomicMax(&a.amax_h[u * kMaxT + t], v);
+      }
+      release_red(ri);   // its __syncwarp orders every lane's h writes before lane 0's release below
       // publish per expert: when the expert changes and after the CTA's last G tile
       if (pend_u != u) {
-        if (pend_u >= 0 && lane == 0) { __threadfence(); atomicAdd(&a.cnt_g[pend_u], (uint32_t)pend_n); }
+        if (pend_u >= 0 && lane == 0) red_release_add(&a.cnt_g[pend_u], (uint32_t)pend_n);
         pend_u = u;
         pend_n = 0;
       }
       ++pend_n;
     }
-    if (pend_u >= 0 && lane == 0) { __threadfence(); atomicAdd(&a.cnt_g[pend_u], (uint32_t)pend_n); }
+    if (pend_u >= 0 && lane == 0) red_release_add(&a.cnt_g[pend_u], (uint32_t)pend_n);
+    // With one expert per token (a shared expert, or k = 1) the owner of a down tile is the only contributor to its
+    // output rows: it writes y itself, with the combine's arithmetic, and no grid barrier is needed.
+    const bool direct = s_direct != 0;
     int hu = -1;
-    for (int64_t du = d0; du < d1; ++du, ++ri) {
-      const int u = (int)(du / dt), m = (int)(du % dt);
+    for (int du = d0; du < d1; ++du, ++ri) {
+      const int u = du / dt, m = du % dt;
       const float* rb = wait_red(ri);
       if (u != hu) {  // the consumers waited for this expert's G tiles before handing over this unit
         if (lane < T) s_hinv[lane] = exp2i_neg(rescale_exponent(__uint_as_float(__ldcg(&a.amax_h[u * kMaxT + lane]))));
@@ -495,7 +515,16 @@ __global__ void __launch_bounds__(Cfg<FMT>::THREADS, 1) ffn_kernel(const FfnArgs
           float ds = 0.f;
 #pragma unroll
           for (int w = 0; w < C::CW; ++w) ds += rb[(w * 32 + fl) * 4 + cc];
-          a.dbuf[((size_t)u * H + (size_t)m * 16 + row) * kMaxT + tc] = ds * s_hinv[tc];
+          const float dv = ds * s_hinv[tc];
+          if (direct) {
+            const size_t yi = (size_t)tc * H + (size_t)m * 16 + row;
+            const float acc2 = fmaf(s_uw[tc][0], dv, 0.f);
+            const float yv = a.accumulate ? a.y[yi] + acc2 : acc2;
+            a.y[yi] = yv;
+            if (a.y_bf16) a.y_bf16[yi] = __bfloat16_as_ushort(__float2bfloat16_rn(yv));
+          } else {
+            a.dbuf[((size_t)u * H + (size_t)m * 16 + row) * kMaxT + tc] = dv;
+          }
         }
       }
       release_red(ri);
@@ -503,16 +532,15 @@ __global__ void __launch_bounds__(Cfg<FMT>::THREADS, 1) ffn_kernel(const FfnArgs
     // ---- grid-wide barrier, then the CTA combines its output rows: y_t = sum over the token's own experts, in
     //      ascending expert id, of w * d (fp32 fma), so the result does not depend on the other tokens
     __syncwarp();
-    if (lane == 0) {
-      __threadfence();
-      atomicAdd(&a.hdr->gbar, 1u);
+    if (lane == 0 && !direct) {
+      red_release_add(&a.hdr->gbar, 1u);   // after the __syncwarp: every lane's down partials before it
       if (!s_abort && !wait_counter(&a.hdr->gbar, (uint32_t)G, a.wait_ns)) {
         record_error(&a.hdr->status, MOE_ERR_DEVICE_TIMEOUT);
         s_abort = 1;
       }
     }
     __syncwarp();
-    for (int i = lane; i < (m1 - m0) * 16 * T; i += 32) {
+    for (int i = lane; i < (direct ? 0 : (m1 - m0) * 16 * T); i += 32) {
       const int tok = i % T, row = (i / T) % 16, mi = i / T / 16;
       const size_t hrow = (size_t)(m0 + mi) * 16 + row;
       const int nu = s_nu[tok];
@@ -576,7 +604,7 @@ __global__ void __launch_bounds__(Cfg<FMT>::THREADS, 1) ffn_kernel(const FfnArgs
             bx[n][j][h] = *reinterpret_cast<const uint32_t*>(&hv);
           }
 
-      for (int64_t gu = g0; gu < g1; ++gu) {
+      for (int gu = g0; gu < g1; ++gu) {
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         if (!consume_tile<FMT>(ring, full, empty, it, ncg, warp, lane, bx, sxw, acc, a.wait_ns, &s_abort)) {
           record_error(&a.hdr->status, MOE_ERR_DEVICE_TIMEOUT);
@@ -590,16 +618,19 @@ __global__ void __launch_bounds__(Cfg<FMT>::THREADS, 1) ffn_kernel(const FfnArgs
     {
       uint32_t bh[C::NCH][F::STEPS][2];
       int loaded = -1;
-      for (int64_t du = d0; du < d1; ++du) {
-        const int u = (int)(du / dt);
+      for (int du = d0; du < d1; ++du) {
+        const int u = du / dt;
         if (u != loaded) {
-          if (lane == 0 && !s_abort) {
+          // one thread per CTA polls the expert's counter (a poller per warp, grid-wide, crowded the counter's L2
+          // line and delayed both the publishing adds and the observation); its acquire and the barrier order the
+          // other warps' reads of h after it. Every consumer warp walks the same units, so all reach the barrier.
+          if (warp == 0 && lane == 0 && !s_abort) {
             if (!wait_counter(&a.cnt_g[u], (uint32_t)gt, a.wait_ns)) {
               record_error(&a.hdr->status, MOE_ERR_DEVICE_TIMEOUT);
               s_abort = 1;
             }
           }
-          __syncwarp();
+          named_bar(2, C::CW * 32);
           load_h_fragments<FMT>(a, u, ncd, warp, lane, bh, sxw);
           loaded = u;
         }
@@ -616,13 +647,13 @@ __global__ void __launch_bounds__(Cfg<FMT>::THREADS, 1) ffn_kernel(const FfnArgs
   // ---------------- epilogue: the last CTA to finish clears the per-call counters
   __syncthreads();
   if (tid == 0) {
-    __threadfence();
-    const uint32_t prev = atomicAdd(&a.hdr->done, 1u);
+    // acq_rel: releases this CTA's reads of the counters (ordered before it by the barrier); the last CTA's acquire
+    // then orders its clears after every CTA's reads
+    const uint32_t prev = atom_acq_rel_add(&a.hdr->done, 1u);
     s_last = (prev == (uint32_t)(G - 1));
   }
   __syncthreads();
   if (s_last) {
-    __threadfence();
     for (int i = tid; i < U; i += blockDim.x) a.cnt_g[i] = 0u;
     for (int i = tid; i < U * kMaxT; i += blockDim.x) a.amax_h[i] = 0u;
     if (tid == 0) { a.hdr->gbar = 0u; a.hdr->done = 0u; }
