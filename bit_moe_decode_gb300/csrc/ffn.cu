@@ -40,9 +40,6 @@ constexpr int kNR = 4;                 // reduction slots between consumers and 
 constexpr int kMaxT = 8;
 constexpr int kMaxK = 8;
 constexpr int kMaxU = kMaxT * kMaxK;   // 64
-// Weight stages the producer issues before the CTA barrier (at most the ring's depth). More in flight at that
-// point slows the other warps' start: their first instruction fetches and x loads queue behind the copies.
-constexpr int kEarlyStages = 2;
 
 // workspace: [header 256][cnt_g 64 u32][amax_h 64*8 u32] -> 4096 bytes, then h [U, 8, I] and d [U, H, 8] fp32
 constexpr size_t kWsCounters = 4096;
@@ -239,7 +236,7 @@ __device__ __forceinline__ bool consume_tile(uint8_t* ring, uint64_t* full, uint
     if (n % C::NPS == 0 && s < nst) {
       slot = (int)((it + s) % C::NS);
       const uint32_t par = ((it + s) / C::NS) & 1;
-      if (*abort || !mbar_wait_poll(&full[slot], par, wait_ns)) ok = false;
+      if (*abort || !mbar_wait(&full[slot], par, wait_ns)) ok = false;
     }
     const int c = warp + C::CW * n;
     if (ok && c < nchunks) {
@@ -333,68 +330,14 @@ __global__ void __launch_bounds__(Cfg<FMT>::THREADS, 1) ffn_kernel(const FfnArgs
         bx[n][j][1] = v1;
       }
     }
-    // The warp's max |x| per token, formed before the CTA barrier: the x loads then complete before the weight
-    // stream fills the SM's memory pipeline (loads issued behind it waited microseconds).
-#pragma unroll
-    for (int n = 0; n < C::NCH; ++n)
-#pragma unroll
-      for (int j = 0; j < F::STEPS; ++j) {
-        const uint32_t v0 = bx[n][j][0], v1 = bx[n][j][1];
-        xmax = fmaxf(xmax, fmaxf(fmaxf(fabsf(bf16_bits_to_f32(v0 & 0xFFFFu)), fabsf(bf16_bits_to_f32(v0 >> 16))),
-                                 fmaxf(fabsf(bf16_bits_to_f32(v1 & 0xFFFFu)), fabsf(bf16_bits_to_f32(v1 >> 16)))));
-      }
-    xmax = fmaxf(xmax, __shfl_xor_sync(0xffffffffu, xmax, 1));
-    xmax = fmaxf(xmax, __shfl_xor_sync(0xffffffffu, xmax, 2));
-    if (q == 0) s_colmax[warp][col] = xmax;   // read by every consumer warp after the CTA barrier
   }
-  // The producer's copy stream: stage s of this CTA covers chunks [c0, c0 + CPS) of one tile, its G tiles first,
-  // then its D tiles. It starts before the CTA barrier below (the ring's first NS stages need no slot to be freed),
-  // so the first weights are in flight while the other warps start up.
-  const int gt = I / 8, dt = H / 16;                                // tiles per expert
-  const int ncg = H / F::CK, ncd = I / F::CK;                       // chunks per G / D tile
-  const int sgs = (ncg + F::CPS - 1) / F::CPS, sds = (ncd + F::CPS - 1) / F::CPS;   // stages per G / D tile
-  const int64_t tbg = tile_bytes(FMT, H), tbd = tile_bytes(FMT, I);
-  const int64_t sgu = gate_up_stride(FMT, H, I), sdn = down_stride(FMT, H, I);
-  const int G = gridDim.x, bid = blockIdx.x;
-  // 32-bit unit arithmetic (U * gt <= 64 * 512 units; 64-bit divisions are long software sequences)
-  auto unit_range = [&](int U, int per, int& lo, int& hi) {
-    const uint32_t n = (uint32_t)(U * per);
-    lo = (int)(n * (uint32_t)bid / (uint32_t)G);
-    hi = (int)(n * (uint32_t)(bid + 1) / (uint32_t)G);
-  };
-  uint32_t pit = 0;   // producer lane 0: stages issued so far
-  auto issue_stages = [&](uint32_t stop, int g0_, int d0_, int nstg, uint64_t pol) -> bool {
-    for (; pit < stop; ++pit) {
-      const int slot = (int)(pit % C::NS);
-      if (pit >= (uint32_t)C::NS) {
-        if (s_abort || !mbar_wait_poll(&empty[slot], ((pit / C::NS) - 1) & 1, a.wait_ns)) return false;
-      }
-      const uint8_t* base;
-      int c0, nch;
-      if ((int)pit < nstg) {
-        const int gu = g0_ + (int)pit / sgs, u = gu / gt, j = gu % gt;
-        base = a.gate_up + (size_t)s_union[u] * sgu + (size_t)j * tbg;
-        c0 = ((int)pit % sgs) * F::CPS;
-        nch = ncg;
-      } else {
-        const int q = (int)pit - nstg, du = d0_ + q / sds, u = du / dt, m = du % dt;
-        base = a.down + (size_t)s_union[u] * sdn + (size_t)m * tbd;
-        c0 = (q % sds) * F::CPS;
-        nch = ncd;
-      }
-      const int nc = min(F::CPS, nch - c0);
-      mbar_arrive_expect_tx(&full[slot], (uint32_t)(nc * F::CB));
-      bulk_g2s(ring + (size_t)slot * C::SB, base + (size_t)c0 * F::CB, (uint32_t)(nc * F::CB), &full[slot], pol);
-    }
-    return true;
-  };
+  if (tid == 0) {
+    for (int s = 0; s < C::NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], C::CW); }
+    for (int s = 0; s < kNR; ++s) { mbar_init(&redfull[s], C::CW); mbar_init(&redempty[s], 1); }
+    fence_mbar_init();
+    s_abort = 0;
+  }
   if (warp == C::PROD) {
-    if (lane == 0) {   // barriers first: this warp's own early copies complete on them
-      for (int s = 0; s < C::NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], C::CW); }
-      for (int s = 0; s < kNR; ++s) { mbar_init(&redfull[s], C::CW); mbar_init(&redempty[s], 1); }
-      fence_mbar_init();
-      s_abort = 0;
-    }
     int bad = 0;
     for (int i = lane; i < n_ent; i += 32) {
       const int v = a.idx[i];
@@ -425,13 +368,6 @@ __global__ void __launch_bounds__(Cfg<FMT>::THREADS, 1) ffn_kernel(const FfnArgs
     }
     nfirst = __reduce_add_sync(0xffffffffu, nfirst);
     __syncwarp();
-    if (lane == 0 && !bad) {   // the union is known: start the weight stream
-      int g0_, g1_, d0_, d1_;
-      unit_range(nfirst, gt, g0_, g1_);
-      unit_range(nfirst, dt, d0_, d1_);
-      const int nstg = (g1_ - g0_) * sgs, total = nstg + (d1_ - d0_) * sds;
-      issue_stages((uint32_t)min(total, min(kEarlyStages, C::NS)), g0_, d0_, nstg, policy_evict_first());
-    }
     if (lane < T) {  // rank order, so a token's weight sums do not depend on the other tokens
       for (int r = 0; r < k; ++r) {
         const int u = s_slot[lane * k + r];
@@ -453,21 +389,50 @@ __global__ void __launch_bounds__(Cfg<FMT>::THREADS, 1) ffn_kernel(const FfnArgs
   }
   __syncthreads();
   const int U = s_U;
-  int g0, g1, d0, d1;
-  unit_range(U, gt, g0, g1);
-  unit_range(U, dt, d0, d1);
-  const int m0 = (int)((uint32_t)dt * (uint32_t)bid / (uint32_t)G), m1 = (int)((uint32_t)dt * (uint32_t)(bid + 1) / (uint32_t)G);
+  const int G = gridDim.x, bid = blockIdx.x;
+  const int gt = I / 8, dt = H / 16;  // tiles per expert
+  // 32-bit unit arithmetic (U * gt <= 64 * 512 units): a 64-bit division is a long software sequence on the path
+  // from the prologue to the first weight copy
+  const uint32_t NG = (uint32_t)(U * gt), ND = (uint32_t)(U * dt), uG = (uint32_t)G, ub = (uint32_t)bid;
+  const int g0 = (int)(NG * ub / uG), g1 = (int)(NG * (ub + 1) / uG);
+  const int d0 = (int)(ND * ub / uG), d1 = (int)(ND * (ub + 1) / uG);
+  const int m0 = (int)((uint32_t)dt * ub / uG), m1 = (int)((uint32_t)dt * (ub + 1) / uG);
+  const int ncg = H / F::CK, ncd = I / F::CK;                       // chunks per G / D tile
+  const int64_t tbg = tile_bytes(FMT, H), tbd = tile_bytes(FMT, I);
+  const int64_t sgu = gate_up_stride(FMT, H, I), sdn = down_stride(FMT, H, I);
 
   if (warp == C::PROD) {
-    // ================= producer: the rest of the stream (the first stages went out before the barrier)
+    // ================= producer: G tiles of the CTA's range, then its D tiles (expert-major)
     if (lane == 0 && !s_abort) {
-      const int nstg = (g1 - g0) * sgs, total = nstg + (d1 - d0) * sds;
-      if (!issue_stages((uint32_t)total, g0, d0, nstg, policy_evict_first())) {
+      const uint64_t pol = policy_evict_first();
+      uint32_t it = 0;
+      bool ok = true;
+      auto issue_tile = [&](const uint8_t* base, int nchunks) {
+        for (int c0 = 0; c0 < nchunks && ok; c0 += F::CPS) {
+          const int nc = min(F::CPS, nchunks - c0);
+          const int slot = (int)(it % C::NS);
+          if (it >= (uint32_t)C::NS) {
+            if (s_abort || !mbar_wait(&empty[slot], ((it / C::NS) - 1) & 1, a.wait_ns)) { ok = false; break; }
+          }
+          mbar_arrive_expect_tx(&full[slot], (uint32_t)(nc * F::CB));
+          bulk_g2s(ring + (size_t)slot * C::SB, base + (size_t)c0 * F::CB, (uint32_t)(nc * F::CB), &full[slot], pol);
+          ++it;
+        }
+      };
+      for (int gu = g0; gu < g1 && ok; ++gu) {
+        const int u = gu / gt, j = gu % gt;
+        issue_tile(a.gate_up + (size_t)s_union[u] * sgu + (size_t)j * tbg, ncg);
+      }
+      for (int du = d0; du < d1 && ok; ++du) {
+        const int u = du / dt, m = du % dt;
+        issue_tile(a.down + (size_t)s_union[u] * sdn + (size_t)m * tbd, ncd);
+      }
+      if (!ok) {
         record_error(&a.hdr->status, MOE_ERR_DEVICE_TIMEOUT);
         s_abort = 1;
         // let the copies already in flight land before the CTA can exit
-        const uint32_t lo = pit > (uint32_t)C::NS ? pit - C::NS : 0;
-        for (uint32_t i = lo; i < pit; ++i) mbar_wait_poll(&full[i % C::NS], (i / C::NS) & 1, a.wait_ns);
+        const uint32_t lo = it > (uint32_t)C::NS ? it - C::NS : 0;
+        for (uint32_t i = lo; i < it; ++i) mbar_wait(&full[i % C::NS], (i / C::NS) & 1, a.wait_ns);
       }
     }
   } else if (warp == C::EPI) {
@@ -478,7 +443,7 @@ __global__ void __launch_bounds__(Cfg<FMT>::THREADS, 1) ffn_kernel(const FfnArgs
     uint32_t ri = 0;
     auto wait_red = [&](uint32_t r) -> const float* {
       const int slot = (int)(r % kNR);
-      if (s_abort || !mbar_wait_poll(&redfull[slot], (r / kNR) & 1, a.wait_ns)) {
+      if (s_abort || !mbar_wait(&redfull[slot], (r / kNR) & 1, a.wait_ns)) {
         record_error(&a.hdr->status, MOE_ERR_DEVICE_TIMEOUT);
         s_abort = 1;
       }
@@ -595,7 +560,7 @@ __global__ void __launch_bounds__(Cfg<FMT>::THREADS, 1) ffn_kernel(const FfnArgs
     auto hand_over = [&](const float (&acc)[4]) {
       const int slot = (int)(ri % kNR);
       if (ri >= (uint32_t)kNR) {
-        if (s_abort || !mbar_wait_poll(&redempty[slot], ((ri / kNR) - 1) & 1, a.wait_ns)) {
+        if (s_abort || !mbar_wait(&redempty[slot], ((ri / kNR) - 1) & 1, a.wait_ns)) {
           record_error(&a.hdr->status, MOE_ERR_DEVICE_TIMEOUT);
           s_abort = 1;
         }
@@ -609,6 +574,19 @@ __global__ void __launch_bounds__(Cfg<FMT>::THREADS, 1) ffn_kernel(const FfnArgs
 
     // ---- phase G: B fragments = x of the T tokens (fetched in the prologue), rescaled per token into fp16
     {
+      float mx = xmax;
+#pragma unroll
+      for (int n = 0; n < C::NCH; ++n)
+#pragma unroll
+        for (int j = 0; j < F::STEPS; ++j) {
+          const uint32_t v0 = bx[n][j][0], v1 = bx[n][j][1];
+          mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf16_bits_to_f32(v0 & 0xFFFFu)), fabsf(bf16_bits_to_f32(v0 >> 16))),
+                               fmaxf(fabsf(bf16_bits_to_f32(v1 & 0xFFFFu)), fabsf(bf16_bits_to_f32(v1 >> 16)))));
+        }
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      if (q == 0) s_colmax[warp][col] = mx;
+      named_bar(1, C::CW * 32);
       float cm = 0.f;
 #pragma unroll
       for (int w = 0; w < C::CW; ++w) cm = fmaxf(cm, s_colmax[w][col]);
