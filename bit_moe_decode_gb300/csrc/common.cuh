@@ -105,19 +105,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, long lon
   }
 }
 
-// The same wait with non-blocking tests and 32 ns sleeps in between. A thread parked in mbarrier.try_wait was
-// measured to slow the other warps of its SM several-fold (their shuffles and shared-memory work), so kernels
-// whose waiting warps share the SM with a busy one wait this way.
-__device__ __forceinline__ bool mbar_wait_poll(uint64_t* b, uint32_t parity, long long limit_ns) {
-  if (mbar_test_wait(b, parity)) return true;
-  const long long t0 = globaltimer_ns();
-  while (true) {
-    __nanosleep(32);
-    if (mbar_test_wait(b, parity)) return true;
-    if (globaltimer_ns() - t0 > limit_ns) return false;
-  }
-}
-
 // L2 policy: stream the expert weights through L2 with evict-first so small, reused data stays resident.
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
