@@ -583,18 +583,20 @@ def bench_stack(m, torch, args, dev, stream, n_layers=43, n_hash=3, vocab=32768)
     """The whole routed-expert stack: 43 layers x 256 MXFP4 experts in the tensor-core layout (147 GB, generated on
     the GPU: seeded N(0, 0.02) fp32 per expert, packed by the library's encoder), layers 0-2 routed by a seeded
     tid2eid table (vocab 32768, 6 distinct experts, w = 1/6), layers 3-42 by their own fp16 router (fused into the
-    FFN launch); layer L + 1's x = bf16(y_L). Decode: args.stack_tokens tokens one at a time, all layers, as a CUDA
+    FFN launch); layer L + 1's x = bf16(y_L). Each layer also holds a Q8_0 shared expert (intermediate 2048), timed
+    separately (`with_shared_experts`: decode and T = 8 verify with the shared expert after every routed call). Decode: args.stack_tokens tokens one at a time, all layers, as a CUDA
     graph; verify: the same tokens in batches of T = 2, 4, 8 (independent routing: each layer sweeps the union of
     the batch's experts). Algorithmic bytes = packed bytes of each layer's union of experts, summed over layers."""
     from bit_moe_decode_gb300.stack import RoutedStack
     from moe_inputs import tid2eid, token_ids, x_bf16_bits
     per_expert = m.moe_packed_bytes(1, 1, 0, 1, H, I) + m.moe_packed_bytes(1, 1, 1, 1, H, I)
-    need = n_layers * E * per_expert
+    per_shared = m.moe_packed_bytes(4, 0, 0, 1, H, I) + m.moe_packed_bytes(4, 0, 1, 1, H, I)   # Q8_0, intermediate I
+    need = n_layers * (E * per_expert + per_shared)
     free, _ = torch.cuda.mem_get_info(dev)
     if free < need + (8 << 30):
         return {"skipped": "needs %.1f GB of free device memory, %.1f GB free" % (need / 1e9, free / 1e9)}
     t0 = time.time()
-    st = RoutedStack(H, I, E, K_TOP, n_layers, n_hash, vocab, T_max=8, device=dev)
+    st = RoutedStack(H, I, E, K_TOP, n_layers, n_hash, vocab, T_max=8, device=dev, shared_I=I)
     gen = torch.Generator(device=dev)
     batch = 32
     for L in range(n_layers):
@@ -608,6 +610,11 @@ def bench_stack(m, torch, args, dev, stream, n_layers=43, n_hash=3, vocab=32768)
             st.tid2eid[L] = torch.from_numpy(tid2eid(args.seed, L, vocab, E, K_TOP)).to(dev)
         else:
             st.router[L] = (torch.randn((E, H), generator=gen, device=dev) * 0.02).half().view(torch.int16)
+        gen.manual_seed(args.seed * 1000 + 500 + L)   # the layer's shared expert, from a stream of its own
+        g = torch.randn((1, I, H), generator=gen, device=dev).mul_(0.02)
+        u = torch.randn((1, I, H), generator=gen, device=dev).mul_(0.02)
+        d = torch.randn((1, H, I), generator=gen, device=dev).mul_(0.02)
+        st.shared[L].pack(m.MOE_SRC_F32, g, u, d, stream=torch.cuda.current_stream(dev))
     del g, u, d
     torch.cuda.synchronize()
     setup_s = time.time() - t0
@@ -615,20 +622,21 @@ def bench_stack(m, torch, args, dev, stream, n_layers=43, n_hash=3, vocab=32768)
     toks = torch.from_numpy(token_ids(args.seed, N, vocab)).to(dev)
     xs = torch.from_numpy(x_bf16_bits(args.seed + 31, range(N), H).view(np.int16)).to(dev)
 
-    res, unions = {}, {}
-    for T in (1, 2, 4, 8):
-        def launch(T=T):
+    res, unions, res_sh = {}, {}, {}
+    for T, sh in ((1, False), (2, False), (4, False), (8, False), (1, True), (8, True)):
+        def launch(T=T, sh=sh):
             for j in range(N // T):
-                st.run(T, token_ids=toks[j * T:(j + 1) * T], x0=xs[j * T:(j + 1) * T], stream=stream)
+                st.run(T, token_ids=toks[j * T:(j + 1) * T], x0=xs[j * T:(j + 1) * T], stream=stream, shared=sh)
         # the routing of every pass (eager, once): each layer's union of experts over the batch
         us = []
         for j in range(N // T):
             with torch.cuda.stream(stream):
-                st.run(T, token_ids=toks[j * T:(j + 1) * T], x0=xs[j * T:(j + 1) * T], stream=stream)
+                st.run(T, token_ids=toks[j * T:(j + 1) * T], x0=xs[j * T:(j + 1) * T], stream=stream, shared=sh)
             stream.synchronize()
             us.append([len(np.unique(st.idx[L][:T].cpu().numpy())) for L in range(n_layers)])
-        unions[T] = float(np.mean(np.sum(us, axis=1)))   # union sizes summed over the layers, per pass
-        if m.moe_get_device_status(st.ws, stream) != 0:
+        if not sh:
+            unions[T] = float(np.mean(np.sum(us, axis=1)))   # union sizes summed over the layers, per pass
+        if m.moe_get_device_status(st.ws, stream) != 0 or m.moe_get_device_status(st.ws_shared, stream) != 0:
             raise RuntimeError("device status after the stack's eager pass (T = %d)" % T)
         g_ = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_, stream=stream):
@@ -645,12 +653,20 @@ def bench_stack(m, torch, args, dev, stream, n_layers=43, n_hash=3, vocab=32768)
             e1.record(stream)
             e1.synchronize()
             times.append(e0.elapsed_time(e1))
-        res[T] = float(np.median(times)) / (N // T)   # ms per pass of T tokens
-        if m.moe_get_device_status(st.ws, stream) != 0:
+        (res_sh if sh else res)[T] = float(np.median(times)) / (N // T)   # ms per pass of T tokens
+        if m.moe_get_device_status(st.ws, stream) != 0 or m.moe_get_device_status(st.ws_shared, stream) != 0:
             raise RuntimeError("device status after the stack (T = %d)" % T)
     peak = peak_of(measured_peaks(), "hbm_gbs") or 6800.0
     t1 = res[1]
     bytes1 = unions[1] * per_expert
+    # each layer's Q8_0 shared expert (intermediate I) after its routed call: one more launch per layer
+    ts1, bs1 = res_sh[1], bytes1 + n_layers * per_shared
+    shared_line = {"decode": {"tok_s": round(1e3 / ts1, 2), "us_per_token": round(ts1 * 1e3, 2),
+                              "bytes_per_token": bs1, "gbs": round(bs1 / (ts1 * 1e-3) / 1e9, 1),
+                              "frac": round(bs1 / (ts1 * 1e-3) / 1e9 / peak, 4),
+                              "gpu_launches_per_token": st.launches_per_run(shared=True)},
+                   "verify_T8": {"us_per_pass": round(res_sh[8] * 1e3, 2), "raw_ratio": round(res_sh[8] / ts1, 3)},
+                   "shared_bytes_per_layer": per_shared}
     out = {"workload": "%d layers x %d MXFP4 experts (%.1f GB resident, generated on the GPU), layers 0-%d hash-routed "
                        "(tid2eid, vocab %d), the rest softmax top-%d (router fused), layer L+1's x = bf16(y_L); %d "
                        "tokens per timed pass" % (n_layers, E, st.packed_bytes() / 1e9, n_hash - 1, vocab, K_TOP, N),
@@ -665,6 +681,7 @@ def bench_stack(m, torch, args, dev, stream, n_layers=43, n_hash=3, vocab=32768)
                       "union_experts_over_layers": {str(T): round(unions[T], 1) for T in res},
                       "raw_ratio": {str(T): round(res[T] / t1, 3) for T in res},
                       "per_union_byte_ratio": {str(T): round(res[T] / (t1 * unions[T] / unions[1]), 3) for T in res}},
+           "with_shared_experts": shared_line,
            "setup_s": round(setup_s, 1)}
     del st
     torch.cuda.empty_cache()

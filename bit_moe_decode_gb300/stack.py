@@ -10,12 +10,17 @@ Per layer L of a call with T tokens (1 <= T <= 8):
 Layer L + 1's x is the bf16 (round-to-nearest-even) copy of layer L's y, which the FFN call writes itself; there
 is no attention or residual in between (they are not on the routed-expert path). Everything here only orders
 library calls on one stream; all arithmetic runs in the library's kernels.
+
+With shared experts (shared_I > 0; the recipe of "Mixed-precision compression of DeepSeek-V4-Flash" keeps each
+layer's always-on shared expert in 8 bits, here Q8_0) every layer adds its shared expert after the routed call:
+the routed call writes y only, then moe_expert_ffn_verify on the layer's one-expert Q8_0 layer (idx 0, w 1)
+accumulates into y and writes the bf16 copy that feeds the next layer.
 """
 from __future__ import annotations
 
 import torch
 
-from . import (MOE_FMT_MXFP4, MOE_LAYOUT_TC, Layer, moe_expert_ffn_verify, moe_route_expert_ffn,
+from . import (MOE_FMT_MXFP4, MOE_FMT_Q8_0, MOE_LAYOUT_TC, Layer, moe_expert_ffn_verify, moe_route_expert_ffn,
                moe_route_topk)
 
 
@@ -27,7 +32,7 @@ class RoutedStack:
     fp32 output), one shared workspace (the calls run one after another on the stream)."""
 
     def __init__(self, H: int, I: int, E: int, k: int, n_layers: int, n_hash: int, vocab: int, T_max: int = 8,
-                 device="cuda"):
+                 device="cuda", shared_I: int = 0):
         assert 0 <= n_hash <= n_layers and 1 <= T_max <= 8
         self.H, self.I, self.E, self.k, self.n, self.n_hash, self.vocab, self.T_max = \
             H, I, E, k, n_layers, n_hash, vocab, T_max
@@ -39,27 +44,38 @@ class RoutedStack:
         self.w = [torch.zeros((T_max, k), dtype=torch.float32, device=device) for _ in range(n_layers)]
         self.y = [torch.zeros((T_max, H), dtype=torch.float32, device=device) for _ in range(n_layers)]
         self.ws = self.layers[0].workspace(T_max, k) if n_layers else None
+        # optional shared experts: one Q8_0 expert per layer (intermediate size shared_I) and their own workspace
+        self.shared = [Layer(MOE_FMT_Q8_0, H, shared_I, 1, device=device) for _ in range(n_layers)] if shared_I else []
+        self.ws_shared = self.shared[0].workspace(T_max, 1) if self.shared else None
+        self.one_idx = torch.zeros((T_max, 1), dtype=torch.int32, device=device)
+        self.one_w = torch.ones((T_max, 1), dtype=torch.float32, device=device)
 
-    def packed_bytes(self) -> int:
-        return sum(L.gate_up.numel() + L.down.numel() for L in self.layers)
+    def packed_bytes(self, shared: bool = False) -> int:
+        mats = self.layers + (self.shared if shared else [])
+        return sum(L.gate_up.numel() + L.down.numel() for L in mats)
 
-    def run(self, T: int, token_ids=None, x0=None, stream=None):
+    def run(self, T: int, token_ids=None, x0=None, stream=None, shared: bool = None):
         """One decode (T = 1) or verify (T <= 8) pass of T tokens through every layer: the first layer reads x0
         (bf16 [T, H], device) or, if None, x[0][:T]. token_ids (int32 [T], device) is needed when the stack has
-        hash layers."""
+        hash layers. shared (default: whether the stack has shared experts) adds each layer's shared expert."""
         assert 1 <= T <= self.T_max
+        use_shared = bool(self.shared) if shared is None else (bool(shared) and bool(self.shared))
         for L in range(self.n):
             xin = x0 if (L == 0 and x0 is not None) else self.x[L][:T]
             xout = self.x[L + 1][:T]
+            xr = None if use_shared else xout       # the last call of the layer writes the bf16 copy
             idx, w = self.idx[L][:T], self.w[L][:T]
             if L < self.n_hash:
                 moe_route_topk(None, None, T, self.H, self.E, self.k, token_ids, self.tid2eid[L], self.vocab, idx, w,
                                stream=stream)
-                moe_expert_ffn_verify(self.layers[L], xin, T, idx, w, self.k, self.y[L][:T], xout, False, self.ws,
+                moe_expert_ffn_verify(self.layers[L], xin, T, idx, w, self.k, self.y[L][:T], xr, False, self.ws,
                                       stream=stream)
             else:
-                moe_route_expert_ffn(self.layers[L], self.router[L], xin, T, self.k, idx, w, self.y[L][:T], xout,
+                moe_route_expert_ffn(self.layers[L], self.router[L], xin, T, self.k, idx, w, self.y[L][:T], xr,
                                      False, self.ws, stream=stream)
+            if use_shared:
+                moe_expert_ffn_verify(self.shared[L], xin, T, self.one_idx[:T], self.one_w[:T], 1, self.y[L][:T],
+                                      xout, True, self.ws_shared, stream=stream)
 
-    def launches_per_run(self) -> int:
-        return 2 * self.n_hash + (self.n - self.n_hash)
+    def launches_per_run(self, shared: bool = False) -> int:
+        return 2 * self.n_hash + (self.n - self.n_hash) + (self.n if shared and self.shared else 0)

@@ -86,3 +86,64 @@ def test_stack_verify_rows_equal_decode(stack):
             assert np.array_equal(idd[L][0], iv[L][t]), "layer %d token %d: routing differs in the verify" % (L, t)
             assert np.array_equal(yd[L][0].view(np.uint32), yv[L][t].view(np.uint32)), \
                 "layer %d: verify row %d differs from its decode" % (L, t)
+
+
+# ---------------------------------------------------------------- the same stack with a Q8_0 shared expert per layer
+Q8_0, IS = 4, 512   # the shared expert's format and intermediate size
+
+
+@pytest.fixture(scope="module")
+def stack_shared():
+    import bit_moe_decode_gb300 as m
+    from bit_moe_decode_gb300.stack import RoutedStack
+    st = RoutedStack(H, I, E, K, NL, NH, V, T_max=8, device=DEV, shared_I=IS)
+    Ws = [Weights(SEED, H, I, layer=L) for L in range(NL)]
+    Wsh = [Weights(SEED + 50, H, IS, layer=L) for L in range(NL)]
+    for L in range(NL):
+        g, u, d = (torch.from_numpy(np.stack([Ws[L].f32(e, which) for e in range(E)])).to(DEV) for which in range(3))
+        st.layers[L].pack(m.MOE_SRC_F32, g, u, d, e0=0)
+        gs, us, ds = (torch.from_numpy(Wsh[L].f32(0, which)[None]).to(DEV) for which in range(3))
+        st.shared[L].pack(m.MOE_SRC_F32, gs, us, ds, e0=0)
+        if L < NH:
+            st.tid2eid[L] = torch.from_numpy(tid2eid(SEED, L, V, E, K)).to(DEV)
+        else:
+            st.router[L] = dev_bits(router_f16_bits(SEED, L, E, H), DEV)
+    torch.cuda.synchronize()
+    return st, Ws, Wsh
+
+
+def test_stack_with_shared_experts_against_oracle(stack_shared):
+    st, Ws, Wsh = stack_shared
+    T = 3
+    tok = token_ids(SEED + 2, T, V)
+    x0 = x_bf16_bits(SEED + 2, range(T), H)
+    xs, idx, w, ys = _run(st, T, tok, x0)
+    worst = 0.0
+    for L in range(NL):
+        if L < NH:
+            ri, _ = oracle.route_hash(tok, tid2eid(SEED, L, V, E, K), K)
+            assert np.array_equal(idx[L], ri), "layer %d: hash routing differs" % L
+        else:
+            ri, _, lg, ab = oracle.route_topk(router_f16_bits(SEED, L, E, H), xs[L], K)
+            for t in range(T):
+                assert near_tie_ok(idx[L][t], ri[t], lg[t], ab[t], H), "layer %d token %d: routing differs" % (L, t)
+        yr, yab = oracle_moe(MXFP4, Ws[L], idx[L], w[L], xs[L])
+        ysh, ysab = oracle_moe(Q8_0, Wsh[L], np.zeros((T, 1), np.int32), np.ones((T, 1), np.float32), xs[L])
+        for t in range(T):
+            worst = max(worst, tol_check(ys[L][t], yr[t] + ysh[t], yab[t] + ysab[t], "layer %d token %d" % (L, t)))
+        assert np.array_equal(xs[L + 1], _bf16_rne_bits(ys[L])), "layer %d: next x is not bf16(y)" % L
+    print("stack with shared experts, T=%d: max err/bound %.3g" % (T, worst))
+
+
+def test_stack_with_shared_experts_verify_rows_equal_decode(stack_shared):
+    st, _, _ = stack_shared
+    T = 4
+    tok = token_ids(SEED + 3, T, V)
+    x0 = x_bf16_bits(SEED + 3, range(T), H)
+    _, iv, _, yv = _run(st, T, tok, x0)
+    for t in range(T):
+        _, idd, _, yd = _run(st, 1, tok[t:t + 1], x0[t:t + 1])
+        for L in range(NL):
+            assert np.array_equal(idd[L][0], iv[L][t])
+            assert np.array_equal(yd[L][0].view(np.uint32), yv[L][t].view(np.uint32)), \
+                "layer %d: verify row %d differs from its decode" % (L, t)
