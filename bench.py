@@ -583,7 +583,9 @@ def bench_stack(m, torch, args, dev, stream, n_layers=43, n_hash=3, vocab=32768)
     """The whole routed-expert stack: 43 layers x 256 MXFP4 experts in the tensor-core layout (147 GB, generated on
     the GPU: seeded N(0, 0.02) fp32 per expert, packed by the library's encoder), layers 0-2 routed by a seeded
     tid2eid table (vocab 32768, 6 distinct experts, w = 1/6), layers 3-42 by their own fp16 router (fused into the
-    FFN launch); layer L + 1's x = bf16(y_L). Each layer also holds a Q8_0 shared expert (intermediate 2048), timed
+    FFN launch); layer L + 1's x = bf16(y_L / rms(y_L)) (moe_rms_norm_bf16: the model normalises before each MoE
+    layer, and an unnormalised chain of random layers collapses to zero, where routing degenerates to ties). Each
+    layer also holds a Q8_0 shared expert (intermediate 2048), timed
     separately (`with_shared_experts`: decode and T = 8 verify with the shared expert after every routed call). Decode: args.stack_tokens tokens one at a time, all layers, as a CUDA
     graph; verify: the same tokens in batches of T = 2, 4, 8 (independent routing: each layer sweeps the union of
     the batch's experts). Algorithmic bytes = packed bytes of each layer's union of experts, summed over layers."""
@@ -636,8 +638,10 @@ def bench_stack(m, torch, args, dev, stream, n_layers=43, n_hash=3, vocab=32768)
             us.append([len(np.unique(st.idx[L][:T].cpu().numpy())) for L in range(n_layers)])
         if not sh:
             unions[T] = float(np.mean(np.sum(us, axis=1)))   # union sizes summed over the layers, per pass
-        if m.moe_get_device_status(st.ws, stream) != 0 or m.moe_get_device_status(st.ws_shared, stream) != 0:
-            raise RuntimeError("device status after the stack's eager pass (T = %d)" % T)
+        s1, s2 = m.moe_get_device_status(st.ws, stream), m.moe_get_device_status(st.ws_shared, stream)
+        if s1 != 0 or s2 != 0:
+            raise RuntimeError("device status after the stack's eager pass (T = %d, shared = %d): routed %d, shared %d"
+                               % (T, sh, s1, s2))
         g_ = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_, stream=stream):
             launch()
@@ -654,8 +658,10 @@ def bench_stack(m, torch, args, dev, stream, n_layers=43, n_hash=3, vocab=32768)
             e1.synchronize()
             times.append(e0.elapsed_time(e1))
         (res_sh if sh else res)[T] = float(np.median(times)) / (N // T)   # ms per pass of T tokens
-        if m.moe_get_device_status(st.ws, stream) != 0 or m.moe_get_device_status(st.ws_shared, stream) != 0:
-            raise RuntimeError("device status after the stack (T = %d)" % T)
+        s1, s2 = m.moe_get_device_status(st.ws, stream), m.moe_get_device_status(st.ws_shared, stream)
+        if s1 != 0 or s2 != 0:
+            raise RuntimeError("device status after the stack (T = %d, shared = %d): routed %d, shared %d"
+                               % (T, sh, s1, s2))
     peak = peak_of(measured_peaks(), "hbm_gbs") or 6800.0
     t1 = res[1]
     bytes1 = unions[1] * per_expert
@@ -668,7 +674,7 @@ def bench_stack(m, torch, args, dev, stream, n_layers=43, n_hash=3, vocab=32768)
                    "verify_T8": {"us_per_pass": round(res_sh[8] * 1e3, 2), "raw_ratio": round(res_sh[8] / ts1, 3)},
                    "shared_bytes_per_layer": per_shared}
     out = {"workload": "%d layers x %d MXFP4 experts (%.1f GB resident, generated on the GPU), layers 0-%d hash-routed "
-                       "(tid2eid, vocab %d), the rest softmax top-%d (router fused), layer L+1's x = bf16(y_L); %d "
+                       "(tid2eid, vocab %d), the rest softmax top-%d (router fused), layer L+1's x = bf16(rmsnorm(y_L)); %d "
                        "tokens per timed pass" % (n_layers, E, st.packed_bytes() / 1e9, n_hash - 1, vocab, K_TOP, N),
            "decode": {"tok_s": round(1e3 / t1, 2), "us_per_token": round(t1 * 1e3, 2),
                       "bytes_per_token": bytes1, "gbs": round(bytes1 / (t1 * 1e-3) / 1e9, 1),

@@ -32,7 +32,7 @@ EXPORTS = ["moe_status_string", "moe_version", "moe_check_device", "moe_canonica
            "moe_get_device_status", "moe_expert_ffn_decode", "moe_expert_ffn_verify", "moe_route_expert_ffn",
            "moe_debug_unpack", "moe_debug_timeout_probe", "moe_expert_ffn_decode_static", "moe_static_device_status",
            "moe_prefill_workspace_bytes",
-           "moe_expert_grouped_gemm_prefill", "moe_debug_prefill", "moe_spec_accept"]
+           "moe_expert_grouped_gemm_prefill", "moe_debug_prefill", "moe_spec_accept", "moe_rms_norm_bf16"]
 
 
 class MoeError(RuntimeError):
@@ -68,6 +68,7 @@ def lib() -> C.CDLL:
             "moe_pack_weights": (C.c_int, [C.c_int, C.c_int, C.c_int, C.c_int, i64, i64, i64, P, P, P, sz, P]),
             "moe_route_topk": (C.c_int, [P, P, i32, i32, i32, i32, P, P, i32, P, P, P]),
             "moe_spec_accept": (C.c_int, [P, P, i32, i32, P, P, P, P]),
+            "moe_rms_norm_bf16": (C.c_int, [P, i32, i32, C.c_float, P, P]),
             "moe_workspace_bytes": (sz, [LP, i32, i32]),
             "moe_workspace_init": (C.c_int, [P, sz, P]),
             "moe_get_device_status": (C.c_int, [P, P]),
@@ -150,6 +151,11 @@ def moe_spec_accept(p, q, K: int, V: int, draft, u, result, stream=None):
     """Acceptance of K drafted tokens (see include/moe.h): result[0] = drafts kept, result[1] = the drawn token."""
     _check(lib().moe_spec_accept(_ptr(p), _ptr(q), K, V, _ptr(draft), _ptr(u), _ptr(result), _stream(stream)),
            "moe_spec_accept")
+
+
+def moe_rms_norm_bf16(y, T: int, H: int, eps: float, x_bf16, stream=None):
+    """x_bf16[t] = bf16(y[t] / sqrt(mean(y[t]^2) + eps)) (see include/moe.h)."""
+    _check(lib().moe_rms_norm_bf16(_ptr(y), T, H, eps, _ptr(x_bf16), _stream(stream)), "moe_rms_norm_bf16")
 
 
 def moe_workspace_bytes(layer: "Layer", T_max: int, k: int) -> int:

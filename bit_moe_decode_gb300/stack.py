@@ -6,29 +6,31 @@ hash table, tid2eid).
 Per layer L of a call with T tokens (1 <= T <= 8):
   hash layers (L < n_hash):  moe_route_topk in hash mode (idx = tid2eid[token id], w = 1/k), then
                              moe_expert_ffn_verify;
-  softmax layers:            moe_route_expert_ffn (router top-k and FFN in one launch).
-Layer L + 1's x is the bf16 (round-to-nearest-even) copy of layer L's y, which the FFN call writes itself; there
-is no attention or residual in between (they are not on the routed-expert path). Everything here only orders
-library calls on one stream; all arithmetic runs in the library's kernels.
-
-With shared experts (shared_I > 0; the recipe of "Mixed-precision compression of DeepSeek-V4-Flash" keeps each
-layer's always-on shared expert in 8 bits, here Q8_0) every layer adds its shared expert after the routed call:
-the routed call writes y only, then moe_expert_ffn_verify on the layer's one-expert Q8_0 layer (idx 0, w 1)
-accumulates into y and writes the bf16 copy that feeds the next layer.
+  softmax layers:            moe_route_expert_ffn (router top-k and FFN in one launch);
+  with shared experts:       moe_expert_ffn_verify on the layer's one-expert Q8_0 layer (idx 0, w 1), accumulating
+                             into y (the recipe of "Mixed-precision compression of DeepSeek-V4-Flash" keeps each
+                             layer's always-on shared expert in 8 bits);
+  then                       moe_rms_norm_bf16: layer L + 1's x = bf16(y_L / rms(y_L)).
+The model normalises the hidden state before each MoE layer; without it a stack of random layers drifts (the FFN
+maps an activation of rms r to about c r^2, so the chain collapses to zero, where every router sees ties, or
+overflows). There is no attention or residual in between (not on the routed-expert path). Everything here only
+orders library calls on one stream; all arithmetic runs in the library's kernels.
 """
 from __future__ import annotations
 
 import torch
 
-from . import (MOE_FMT_MXFP4, MOE_FMT_Q8_0, MOE_LAYOUT_TC, Layer, moe_expert_ffn_verify, moe_route_expert_ffn,
-               moe_route_topk)
+from . import (MOE_FMT_MXFP4, MOE_FMT_Q8_0, MOE_LAYOUT_TC, Layer, moe_expert_ffn_verify, moe_rms_norm_bf16,
+               moe_route_expert_ffn, moe_route_topk)
+
+NORM_EPS = 1e-6
 
 
 class RoutedStack:
     """n_layers MXFP4 layers in the tensor-core layout (H, I, E experts each), hash routing in the first n_hash.
 
-    Buffers (device): x[L] bf16 [T_max, H] for L = 0..n_layers (x[0] is the default input, x[L + 1] the output of
-    layer L), idx[L] int32 / w[L] fp32 [T_max, k] (the routing each layer used), y[L] fp32 [T_max, H] (each layer's
+    Buffers (device): x[L] bf16 [T_max, H] for L = 0..n_layers (x[0] is the default input, x[L + 1] the normalised
+    output of layer L), idx[L] int32 / w[L] fp32 [T_max, k] (the routing each layer used), y[L] fp32 [T_max, H] (each layer's
     fp32 output), one shared workspace (the calls run one after another on the stream)."""
 
     def __init__(self, H: int, I: int, E: int, k: int, n_layers: int, n_hash: int, vocab: int, T_max: int = 8,
@@ -63,19 +65,19 @@ class RoutedStack:
         for L in range(self.n):
             xin = x0 if (L == 0 and x0 is not None) else self.x[L][:T]
             xout = self.x[L + 1][:T]
-            xr = None if use_shared else xout       # the last call of the layer writes the bf16 copy
             idx, w = self.idx[L][:T], self.w[L][:T]
             if L < self.n_hash:
                 moe_route_topk(None, None, T, self.H, self.E, self.k, token_ids, self.tid2eid[L], self.vocab, idx, w,
                                stream=stream)
-                moe_expert_ffn_verify(self.layers[L], xin, T, idx, w, self.k, self.y[L][:T], xr, False, self.ws,
+                moe_expert_ffn_verify(self.layers[L], xin, T, idx, w, self.k, self.y[L][:T], None, False, self.ws,
                                       stream=stream)
             else:
-                moe_route_expert_ffn(self.layers[L], self.router[L], xin, T, self.k, idx, w, self.y[L][:T], xr,
+                moe_route_expert_ffn(self.layers[L], self.router[L], xin, T, self.k, idx, w, self.y[L][:T], None,
                                      False, self.ws, stream=stream)
             if use_shared:
                 moe_expert_ffn_verify(self.shared[L], xin, T, self.one_idx[:T], self.one_w[:T], 1, self.y[L][:T],
-                                      xout, True, self.ws_shared, stream=stream)
+                                      None, True, self.ws_shared, stream=stream)
+            moe_rms_norm_bf16(self.y[L][:T], T, self.H, NORM_EPS, xout, stream=stream)
 
     def launches_per_run(self, shared: bool = False) -> int:
-        return 2 * self.n_hash + (self.n - self.n_hash) + (self.n if shared and self.shared else 0)
+        return 2 * self.n_hash + (self.n - self.n_hash) + self.n + (self.n if shared and self.shared else 0)

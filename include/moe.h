@@ -30,7 +30,7 @@
  *     per device for the others; one process drives one GPU) and the static scratch of
  *     moe_expert_ffn_decode_static.
  *   - Host-side fault injection for tests: if the environment variable MOE_FAULT names a call
- *     ("pack", "route", "decode", "verify", "route_ffn", "prefill", "encode", "spec"), that call returns
+ *     ("pack", "route", "decode", "verify", "route_ffn", "prefill", "encode", "spec", "norm"), that call returns
  *     MOE_ERR_FAULT_INJECTED
  *     without launching anything.
  */
@@ -266,6 +266,18 @@ size_t moe_prefill_workspace_bytes(const moe_layer_t* layer, int32_t T_max, int3
 moe_status_t moe_expert_grouped_gemm_prefill(const moe_layer_t* layer, const void* x_bf16, int32_t T,
                                              const int32_t* idx, const float* w, int32_t k, float* y, void* y_bf16,
                                              void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------- between layers --------------------------------- */
+
+/* RMS normalisation of a layer's output into the next layer's bf16 input, for stacks of layers (the model of
+ * "Mixed-precision compression of DeepSeek-V4-Flash", "The recipe", normalises the hidden state before each MoE
+ * layer; a stack that passed y on unnormalised would drift to zero or overflow):
+ *   x_bf16[t, i] = bf16_rne( y[t, i] * r ), r = fp32( 1 / sqrt(mean_i y[t, i]^2 + eps) ), no learned gain;
+ *   the sum of squares (fixed order per token) and r in fp64, the product in fp32.
+ *   y [T, H] fp32 (4-byte aligned), x_bf16 [T, H] bf16 (2-byte aligned); 1 <= H <= 2^20, T >= 1, eps >= 0.
+ *   A token's result does not depend on the other tokens. NaN and infinity propagate.
+ *   Errors: MOE_ERR_INVALID_ARG (null or misaligned pointer), MOE_ERR_SHAPE, before any launch. */
+moe_status_t moe_rms_norm_bf16(const float* y, int32_t T, int32_t H, float eps, void* x_bf16, void* stream);
 
 /* ---------------------------------------------------------------- debug (tests only) ----------------------------- */
 

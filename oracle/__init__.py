@@ -70,6 +70,7 @@ def bind(path: str) -> C.CDLL:
         "orc_topk_from_logits": (None, [P, i32, i32, i32, P, P]),
         "orc_route_topk": (None, [P, P, i32, i32, i32, i32, P, P, P, P]),
         "orc_route_hash": (None, [P, P, i32, i32, P, P]),
+        "orc_rms_norm": (None, [P, i32, i32, C.c_double, P]),
         "orc_weight_at": (dbl, [i32, P, i32, i64, i32]),
         "orc_expert_ffn": (None, [i32, i32, i32, P, P, P, P, P, P, P, P, P]),
         "orc_moe_token": (None, [i32, i32, i32, i32, P, P, P, P, P, P, P]),
@@ -227,6 +228,15 @@ def route_hash(token_ids: np.ndarray, tid2eid: np.ndarray, k: int):
     w = np.empty((T, k), dtype=np.float32)
     lib().orc_route_hash(_p(tok), _p(tab), T, k, _p(idx), _p(w))
     return idx, w
+
+
+def rms_norm(y: np.ndarray, eps: float) -> np.ndarray:
+    """y [T, H] fp32 -> y / sqrt(mean(y^2) + eps) per row, exact in fp64 (the library rounds it to bf16)."""
+    yy = _c(y, np.float32)
+    T, H = yy.shape
+    out = np.empty((T, H))
+    lib().orc_rms_norm(_p(yy), T, H, float(eps), _p(out))
+    return out
 
 
 # ---------------------------------------------------------------- FFN

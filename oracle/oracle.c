@@ -479,6 +479,19 @@ void orc_route_hash(const int32_t* tok, const int32_t* tid2eid, int T, int k, in
     }
 }
 
+/* RMS normalisation between the layers of a stack (the model normalises the hidden state before each MoE layer:
+ * "Mixed-precision compression of DeepSeek-V4-Flash", "The recipe"); no learned gain. Exact values in fp64:
+ * out[t, i] = y[t, i] / sqrt(mean_i y[t, i]^2 + eps). The library rounds them to bf16. */
+void orc_rms_norm(const float* y, int T, int H, double eps, double* out) {
+  for (int t = 0; t < T; ++t) {
+    const float* yr = y + (int64_t)t * H;
+    double ss = 0.0;
+    for (int i = 0; i < H; ++i) ss += (double)yr[i] * (double)yr[i];
+    const double r = 1.0 / sqrt(ss / H + eps);
+    for (int i = 0; i < H; ++i) out[(int64_t)t * H + i] = (double)yr[i] * r;
+  }
+}
+
 /* ------------------------------------------------------------------------------------------------
  * Q8_0: the shared expert's 8-bit format ("Mixed-precision compression of DeepSeek-V4-Flash", "The recipe"
  * names Q8 for it and gives no layout; this build's definition): 34 bytes per 32 weights, bytes 0..1 a binary16

@@ -134,3 +134,20 @@ def test_spec_accept_writes_inside_its_buffer(m):
                       dev(np.asarray(u).reshape(-1), np.float32), g["res"].view(torch.int32, (2,)))
     _check(g, "spec accept")
     assert tuple(int(v) for v in g["res"].view(torch.int32, (2,)).cpu()) == oracle.spec_accept(p, q, d, u)
+
+
+@pytest.mark.parametrize("T", [1, 8])
+def test_tc_full_shape_writes_inside_its_buffers(m, T):
+    """hidden 4096, intermediate 2048, 256 experts, top-6 (split slices, exports, imports, the h images): the
+    tensor-core decode / verify with the routing given, workspace sized for 8 tokens"""
+    E, H, I, k = 256, 4096, 2048, 6
+    W = Weights(70, H, I)
+    x = x_bf16_bits(70, range(T), H)
+    idx, w, _, _ = oracle.route_topk(router_f16_bits(70, 0, E, H), x, k)
+    layer = make_layer(m, 1, W, E, np.unique(idx), DEV, layout=1)
+    g = _outs(T, H)
+    g["ws"] = Guarded(m.moe_workspace_bytes(layer, 8, k))
+    m.moe_expert_ffn_verify(layer, dev_bits(x, DEV), T, torch.from_numpy(idx).to(DEV), torch.from_numpy(w).to(DEV), k,
+                            g["y"].view(torch.float32, (T, H)), g["yb"].view(torch.int16, (T, H)), False, g["ws"].body)
+    _check(g, "tc full shape T=%d" % T)
+    assert m.moe_get_device_status(g["ws"].body) == 0

@@ -1,8 +1,8 @@
 """The routed-expert stack end to end at a small shape: 3 hash-routed layers ("quant surgery", section 4: tid2eid)
 then 2 softmax-routed layers ("Mixed-precision compression of DeepSeek-V4-Flash", "The recipe"), layer L + 1's x
-= bf16(y_L). Every layer is checked against the oracle on the GPU's own input to that layer: routing exactly (hash)
-or up to proven near-ties (softmax), y within 1e-3 * sum|terms| + 1e-6 per element, and the next layer's x equal
-to the round-to-nearest-even bf16 copy of y. A verify pass of T tokens gives, at every layer, rows bit-identical to
+= bf16(y_L / rms(y_L)) (the model normalises before each MoE layer). Every layer is checked against the oracle on
+the GPU's own input to that layer: routing exactly (hash) or up to proven near-ties (softmax), y within
+1e-3 * sum|terms| + 1e-6 per element, and the next layer's x within bf16 rounding of the oracle's normalised y. A verify pass of T tokens gives, at every layer, rows bit-identical to
 decoding each token alone ("Width drift")."""
 import numpy as np
 import pytest
@@ -38,9 +38,11 @@ def stack():
     return st, Ws
 
 
-def _bf16_rne_bits(y: np.ndarray) -> np.ndarray:
-    return torch.from_numpy(np.ascontiguousarray(y, dtype=np.float32)).to(torch.bfloat16).view(torch.int16) \
-        .numpy().view(np.uint16)
+def _next_x_ok(x_bits: np.ndarray, y: np.ndarray) -> bool:
+    """the next layer's bf16 x against the oracle's exact y / sqrt(mean(y^2) + eps), within bf16 rounding"""
+    x = (x_bits.astype(np.uint32) << 16).view(np.float32)
+    ref = oracle.rms_norm(y, 1e-6)
+    return bool(np.all(np.abs(x - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-30))
 
 
 def _run(st, T, tok, x0):
@@ -70,7 +72,7 @@ def test_stack_layers_against_oracle(stack):
         yr, yab = oracle_moe(MXFP4, Ws[L], idx[L], w[L], xs[L])
         for t in range(T):
             worst = max(worst, tol_check(ys[L][t], yr[t], yab[t], "layer %d token %d" % (L, t)))
-        assert np.array_equal(xs[L + 1], _bf16_rne_bits(ys[L])), "layer %d: next x is not bf16(y)" % L
+        assert _next_x_ok(xs[L + 1], ys[L]), "layer %d: next x is not the normalised y" % L
     print("stack of %d layers (%d hash), T=%d: max err/bound %.3g" % (NL, NH, T, worst))
 
 
@@ -131,7 +133,7 @@ def test_stack_with_shared_experts_against_oracle(stack_shared):
         ysh, ysab = oracle_moe(Q8_0, Wsh[L], np.zeros((T, 1), np.int32), np.ones((T, 1), np.float32), xs[L])
         for t in range(T):
             worst = max(worst, tol_check(ys[L][t], yr[t] + ysh[t], yab[t] + ysab[t], "layer %d token %d" % (L, t)))
-        assert np.array_equal(xs[L + 1], _bf16_rne_bits(ys[L])), "layer %d: next x is not bf16(y)" % L
+        assert _next_x_ok(xs[L + 1], ys[L]), "layer %d: next x is not the normalised y" % L
     print("stack with shared experts, T=%d: max err/bound %.3g" % (T, worst))
 
 

@@ -205,3 +205,19 @@ def test_prefill_token_matches_torch_float8_path():
     oxq = np.array([oracle.e4m3_value(c) for c in out["xq_codes"]]) * \
         np.repeat([oracle.e8m0_scale(s) for s in out["xq_scales"]], 32)
     assert np.array_equal(oxq, xq)
+
+
+# ---------------------------------------------------------------- RMS normalisation between stacked layers
+def test_rms_norm_closed_forms():
+    """[3, 4]: mean square 12.5; a constant row c: every output c / sqrt(c^2 + eps); zeros stay zeros; the result
+    has unit mean square when eps = 0; scaling a row does not change it (eps = 0)."""
+    y = np.array([[3.0, 4.0], [2.5, 2.5], [0.0, 0.0]], np.float32)
+    out = oracle.rms_norm(y, 1e-6)
+    assert np.allclose(out[0], np.array([3.0, 4.0]) / np.sqrt(12.5 + 1e-6), rtol=1e-15, atol=0)
+    assert np.allclose(out[1], 2.5 / np.sqrt(6.25 + 1e-6), rtol=1e-15, atol=0)
+    assert np.array_equal(out[2], [0.0, 0.0])
+    rng = np.random.default_rng(5)
+    z = (rng.standard_normal((4, 1000)) * 7.0).astype(np.float32)
+    n0 = oracle.rms_norm(z, 0.0)
+    assert np.allclose(np.mean(n0 ** 2, axis=1), 1.0, rtol=1e-13)
+    assert np.allclose(oracle.rms_norm(z * np.float32(0.25), 0.0), n0, rtol=1e-13)   # exact power-of-two scale
