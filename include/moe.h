@@ -143,6 +143,9 @@ typedef struct {
  *   Softmax mode (token_ids == NULL): logits[t,e] = sum_h W_r[e,h] * x[t,h] (fp16 x bf16 products, fp32 sums),
  *     idx[t, 0..k) = the k largest logits in decreasing order, ties to the lower expert index,
  *     weights[t, r] = exp(l_r - l_0) / sum_j exp(l_j - l_0) over the k chosen (fp32).
+ *     An expert whose logit is NaN or -inf is never chosen (NaN is not ordered). If fewer than k experts remain,
+ *     the missing ranks get idx 0x7fffffff and weight 0 (NaN weights when none remains); an FFN call given such
+ *     ids, and moe_route_expert_ffn, record MOE_ERR_INVALID_ARG and leave y alone.
  *   Hash mode (token_ids != NULL): idx[t, r] = tid2eid[token_ids[t] * k + r], weights = 1/k.
  * router_w_f16 [E, H] fp16; x_bf16 [T, H] bf16; idx [T, k] int32; weights [T, k] fp32.
  * Limits: 1 <= k <= 8, k <= E <= 1024, H multiple of 256 and <= 8192, T >= 1.
@@ -158,7 +161,8 @@ moe_status_t moe_route_topk(const void* router_w_f16, const void* x_bf16, int32_
  * It must be zeroed once with moe_workspace_init() before first use; the kernels leave it zeroed. */
 size_t moe_workspace_bytes(const moe_layer_t* layer, int32_t T_max, int32_t k);
 moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
-/* Synchronises `stream`, returns the device status word (MOE_OK or MOE_ERR_DEVICE_TIMEOUT) and clears it. */
+/* Synchronises `stream`, returns the device status word (MOE_OK, MOE_ERR_DEVICE_TIMEOUT, or MOE_ERR_INVALID_ARG for
+ * an expert id outside [0, E)) and clears it. */
 moe_status_t moe_get_device_status(void* ws, void* stream);
 
 /* Decode, one token: y[H] (=, or += if accumulate) sum_r w[r] * FFN_{idx[r]}(x).
