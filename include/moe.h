@@ -145,7 +145,7 @@ typedef struct {
  *     weights[t, r] = exp(l_r - l_0) / sum_j exp(l_j - l_0) over the k chosen (fp32).
  *     An expert whose logit is NaN or -inf is never chosen (NaN is not ordered). If fewer than k experts remain,
  *     the missing ranks get idx 0x7fffffff and weight 0 (NaN weights when none remains); an FFN call given such
- *     ids, and moe_route_expert_ffn, record MOE_ERR_INVALID_ARG and leave y alone.
+ *     ids, and moe_route_expert_ffn, record MOE_ERR_INVALID_ARG (see the decode call for what y holds then).
  *   Hash mode (token_ids != NULL): idx[t, r] = tid2eid[token_ids[t] * k + r], weights = 1/k.
  * router_w_f16 [E, H] fp16; x_bf16 [T, H] bf16; idx [T, k] int32; weights [T, k] fp32.
  * Limits: 1 <= k <= 8, k <= E <= 1024, H multiple of 256 and <= 8192, T >= 1.
@@ -168,6 +168,9 @@ moe_status_t moe_get_device_status(void* ws, void* stream);
 /* Decode, one token: y[H] (=, or += if accumulate) sum_r w[r] * FFN_{idx[r]}(x).
  *   x_bf16 [H] bf16; idx [k] int32 (expert ids < E); w [k] fp32; y [H] fp32; y_bf16 [H] bf16 or NULL
  *   (round-to-nearest-even copy of y). Equivalent to moe_expert_ffn_verify with T = 1.
+ * An expert id outside [0, E) is device data: the call records MOE_ERR_INVALID_ARG in the workspace status word.
+ *   y is then untouched for MOE_LAYOUT_TC; for MOE_LAYOUT_DECODE its contents are unspecified. After any device
+ *   error, re-zero the workspace with moe_workspace_init() before its next use. */
  * Numerics depend on the layer's layout; in both the weights are exact and the sums are fp32.
  *   MOE_LAYOUT_DECODE (mat-vec kernels, every format): x is rescaled per token by a power of two and held in
  *   binary16 (exact for every element within 2^-28 of the token's largest |x|); h is fp32, rescaled per (expert,
