@@ -170,7 +170,7 @@ moe_status_t moe_get_device_status(void* ws, void* stream);
  *   (round-to-nearest-even copy of y). Equivalent to moe_expert_ffn_verify with T = 1.
  * An expert id outside [0, E) is device data: the call records MOE_ERR_INVALID_ARG in the workspace status word.
  *   y is then untouched for MOE_LAYOUT_TC; for MOE_LAYOUT_DECODE its contents are unspecified. After any device
- *   error, re-zero the workspace with moe_workspace_init() before its next use. */
+ *   error, re-zero the workspace with moe_workspace_init() before its next use.
  * Numerics depend on the layer's layout; in both the weights are exact and the sums are fp32.
  *   MOE_LAYOUT_DECODE (mat-vec kernels, every format): x is rescaled per token by a power of two and held in
  *   binary16 (exact for every element within 2^-28 of the token's largest |x|); h is fp32, rescaled per (expert,
