@@ -158,3 +158,24 @@ def test_prefill_argument_checks(m):
     assert pre(C.byref(layer(E=4)), x, 16, idx, w, 6, y, None, ws, 1 << 20, None) == 2     # k > E
     assert pre(C.byref(lay), C.c_void_p(x.value + 4), 16, idx, w, 6, y, None, ws, 1 << 20, None) == 1
     assert pre(C.byref(lay), x, 16, idx, w, 6, y, None, ws, 16, None) == 5                # workspace too small
+
+
+def test_header_is_plain_c_and_links(m, tmp_path):
+    """include/moe.h compiles as C11 with warnings as errors, and a C program that calls through it links against
+    libmoe.so: the boundary needs no C++ and no torch"""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    prog = tmp_path / "use_moe.c"
+    prog.write_text('#include "moe.h"\n#include <stdio.h>\n'
+                    'int main(void) { printf("%d %s\\n", (int)moe_version(), moe_status_string(MOE_OK));\n'
+                    '  return moe_canonical_bytes(MOE_FMT_Q8_0, 4, 64) == 4 * 2 * 34 ? 0 : 1; }\n')
+    exe = tmp_path / "use_moe"
+    lib_dir = os.path.dirname(m.LIB_PATH)
+    subprocess.run([cc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                    str(prog), "-o", str(exe), "-L", lib_dir, "-lmoe", "-Wl,-rpath," + lib_dir], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.split() == [str(m.lib().moe_version()), m.lib().moe_status_string(0).decode()]
