@@ -79,6 +79,15 @@ template <int FMT> struct Cfg {
   static constexpr size_t SMEM = (size_t)NS * SB + (size_t)(RED + SXF) * 4;
 };
 
+// Every instance fits a CTA's 227 KB of shared memory (the kernel's static arrays add ~6.5 KB), splits each stage
+// evenly over its consumer warps, and moves chunks whose size the 1-D bulk copy accepts (multiples of 16 bytes).
+template <int FMT> constexpr bool cfg_ok() {
+  return Cfg<FMT>::SMEM + 8192 <= 232448 && Fmt<FMT>::CPS % Cfg<FMT>::CW == 0 && Fmt<FMT>::CB % 16 == 0 &&
+         4096 % (Fmt<FMT>::CK * Cfg<FMT>::CW) == 0;
+}
+static_assert(cfg_ok<MOE_FMT_MXFP4>() && cfg_ok<MOE_FMT_INT4G32>() && cfg_ok<MOE_FMT_Q2K>() && cfg_ok<MOE_FMT_Q8_0>(),
+              "mat-vec kernel configuration");
+
 __device__ __forceinline__ float e8m0_to_f32(uint32_t e) {
   return e == 255u ? __uint_as_float(0x7fc00000u) : __uint_as_float(e << 23);
 }
