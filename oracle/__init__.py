@@ -5,7 +5,7 @@ The CUDA library never calls it and shares no code with it. The arithmetic lives
 fp64 accumulation, built with -O2 -ffp-contract=off); this file only builds it and marshals numpy arrays.
 
 Formats: fmt 1 = MXFP4 (17-byte blocks of 32), 2 = INT4 group-32 (18-byte blocks), 3 = Q2_K (84-byte blocks
-of 256), 4 = Q8_0 (34-byte blocks of 32, the shared expert's format as this build defines it). A matrix
+of 256), 4 = Q8_0 (34-byte blocks of 32, the shared expert's format as the library defines it). A matrix
 [rows, K] is rows*K/bs consecutive canonical blocks (blocks run along K).
 
 Parity pins: every function here is pinned by tests/test_oracle_*.py against values the pages print

@@ -494,8 +494,8 @@ void orc_rms_norm(const float* y, int T, int H, double eps, double* out) {
 
 /* ------------------------------------------------------------------------------------------------
  * Q8_0: the shared expert's 8-bit format ("Mixed-precision compression of DeepSeek-V4-Flash", "The recipe"
- * names Q8 for it and gives no layout; this build's definition): 34 bytes per 32 weights, bytes 0..1 a binary16
- * scale d (little-endian), bytes 2..33 signed 8-bit codes q_j; w_j = d * q_j.
+ * names Q8 for it and gives no layout; the library's own definition): 34 bytes per 32 weights, bytes 0..1 a
+ * binary16 scale d (little-endian), bytes 2..33 signed 8-bit codes q_j; w_j = d * q_j.
  * ------------------------------------------------------------------------------------------------ */
 
 static double q8_scale(const uint8_t* blk) { return orc_f16_to_f64(rd16(blk)); }

@@ -258,7 +258,7 @@ def test_int4_encoder_is_grid_argmin():
     assert float(M.min(1).values.sum()) <= float(M[:, 3].sum())
 
 
-# ---------------------------------------------------------------- Q8_0 (the shared expert's format, defined by this build)
+# ---------------------------------------------------------------- Q8_0 (the shared expert's format, defined by the library)
 def test_q8_0_layout_and_decode_closed_form():
     """34 bytes per 32 weights (8.5 bits): fp16 d little-endian, then 32 two's-complement codes; w = d * q."""
     rng = np.random.default_rng(21)
